@@ -1,0 +1,233 @@
+// Container life cycle on the host: info, serialization (header + CRC-32),
+// validation of serialized bytes, upload, release, status strings.
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "wcomp_impl.cuh"
+
+namespace wc {
+
+int map_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return WCOMP_OK;
+  if (e == cudaErrorMemoryAllocation) return WCOMP_ENOMEM;
+  return WCOMP_ECUDA;
+}
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+int sm_count(int device) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  std::lock_guard<std::mutex> g(mu);
+  if (device < 0 || device >= 64) return 148;
+  if (!cache[device]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
+    cache[device] = v;
+  }
+  return cache[device];
+}
+
+// CRC-32 (IEEE 802.3 polynomial, reflected, initial value and final xor 0xFFFFFFFF).
+static uint32_t crc_table[256];
+static std::once_flag crc_once;
+
+static void crc_init() {
+  for (uint32_t i = 0; i < 256; ++i) {
+    uint32_t c = i;
+    for (int k = 0; k < 8; ++k) c = (c & 1) ? (0xEDB88320u ^ (c >> 1)) : (c >> 1);
+    crc_table[i] = c;
+  }
+}
+
+uint32_t crc32_update(uint32_t crc, const uint8_t* p, size_t len) {
+  std::call_once(crc_once, crc_init);
+  crc = ~crc;
+  for (size_t i = 0; i < len; ++i) crc = crc_table[(crc ^ p[i]) & 0xFF] ^ (crc >> 8);
+  return ~crc;
+}
+
+static void put16(uint8_t* p, uint16_t v) { memcpy(p, &v, 2); }
+static void put32(uint8_t* p, uint32_t v) { memcpy(p, &v, 4); }
+static void put64(uint8_t* p, uint64_t v) { memcpy(p, &v, 8); }
+static uint16_t get16(const uint8_t* p) { uint16_t v; memcpy(&v, p, 2); return v; }
+static uint32_t get32(const uint8_t* p) { uint32_t v; memcpy(&v, p, 4); return v; }
+static uint64_t get64(const uint8_t* p) { uint64_t v; memcpy(&v, p, 8); return v; }
+
+}  // namespace wc
+
+using namespace wc;
+
+extern "C" int wcomp_version(void) { return WCOMP_VERSION; }
+
+extern "C" uint64_t wcomp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char* wcomp_strerror(int s) {
+  switch (s) {
+    case WCOMP_OK: return "ok";
+    case WCOMP_EINVAL: return "invalid argument";
+    case WCOMP_ENOMEM: return "out of memory";
+    case WCOMP_ECORRUPT: return "corrupt container";
+    case WCOMP_ECUDA: return "CUDA error";
+    case WCOMP_EUNSUPPORTED: return "unsupported size";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int wcomp_info(const wcomp_container* c, wcomp_info_t* info) {
+  if (!c || !info) return WCOMP_EINVAL;
+  const Layout& L = c->L;
+  memset(info, 0, sizeof(*info));
+  info->scheme = L.scheme;
+  info->version = WCOMP_VERSION;
+  info->N = L.N;
+  info->K = L.K;
+  info->n = int64_t(L.n);
+  info->n_escapes = L.E;
+  info->tile_elems = kTile;
+  info->n_tiles = uint32_t(L.n_tiles);
+  for (int i = 0; i < kTableSize; ++i) info->table[i] = c->table[i];
+  info->bytes_codes = padsec(L.sz_codes);
+  info->bytes_raw = padsec(L.sz_raw) + padsec(L.sz_a) + padsec(L.sz_b) + padsec(L.sz_c);
+  info->bytes_index = padsec(L.sz_tile) + padsec(L.sz_row);
+  info->bytes_escapes = L.esc_payload;
+  info->serialized_bytes = L.serialized();
+  const double sym_bits = L.scheme == WCOMP_BYTESPLIT ? 8.0 : 9.0;
+  const double raw_bits = L.scheme == WCOMP_BYTESPLIT ? 8.0 : 7.0;
+  info->entropy_bpw = 4.0 + raw_bits + (double(L.E) + kTableSize) * sym_bits / double(L.n);
+  info->physical_bpw = 8.0 * double(L.serialized()) / double(L.n);
+  return WCOMP_OK;
+}
+
+static void write_header(const wcomp_container* c, uint32_t payload_crc, uint8_t* h) {
+  const Layout& L = c->L;
+  memset(h, 0, kHeaderBytes);
+  memcpy(h, "WCMP", 4);
+  put16(h + 4, WCOMP_VERSION);
+  h[6] = uint8_t(L.scheme);
+  put64(h + 8, uint64_t(L.N));
+  put64(h + 16, uint64_t(L.K));
+  put64(h + 24, L.E);
+  put32(h + 32, kTile);
+  for (int i = 0; i < kTableSize; ++i) put16(h + 40 + 2 * i, c->table[i]);
+  put64(h + 72, L.main_payload + L.esc_payload);
+  put32(h + 80, payload_crc);
+  put32(h + 92, crc32_update(0, h, 92));
+}
+
+extern "C" int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_t cap, uint64_t* len,
+                               void* stream) {
+  if (!c || !len) return WCOMP_EINVAL;
+  const Layout& L = c->L;
+  *len = L.serialized();
+  if (!host_buf) return WCOMP_OK;
+  if (cap < L.serialized()) return WCOMP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* out = static_cast<uint8_t*>(host_buf);
+  cudaError_t e = cudaMemcpyAsync(out + kHeaderBytes, c->d_main, L.main_payload, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && L.esc_payload)
+    e = cudaMemcpyAsync(out + kHeaderBytes + L.main_payload, c->d_esc, L.esc_payload, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return map_cuda(e);
+  uint32_t crc = crc32_update(0, out + kHeaderBytes, L.main_payload + L.esc_payload);
+  write_header(c, crc, out);
+  return WCOMP_OK;
+}
+
+// Host-side validation of a serialized container (nothing reaches the device
+// unless every check passes, so the kernels never see out-of-range positions).
+static int validate(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table) {
+  if (len < uint64_t(kHeaderBytes)) return WCOMP_ECORRUPT;
+  if (memcmp(b, "WCMP", 4) != 0) return WCOMP_ECORRUPT;
+  if (get32(b + 92) != crc32_update(0, b, 92)) return WCOMP_ECORRUPT;
+  if (get16(b + 4) != WCOMP_VERSION) return WCOMP_ECORRUPT;
+  int scheme = b[6];
+  if (scheme != WCOMP_BYTESPLIT && scheme != WCOMP_K15) return WCOMP_ECORRUPT;
+  int64_t N = int64_t(get64(b + 8)), K = int64_t(get64(b + 16));
+  uint64_t E = get64(b + 24);
+  if (get32(b + 32) != kTile) return WCOMP_ECORRUPT;
+  if (N <= 0 || K <= 0 || N > (int64_t(1) << 32) || K > (int64_t(1) << 32)) return WCOMP_ECORRUPT;
+  uint64_t n = uint64_t(N) * uint64_t(K);
+  if (n >= (uint64_t(1) << 32) || E > n) return WCOMP_ECORRUPT;
+  L.compute(scheme, N, K, E);
+  if (get64(b + 72) != L.main_payload + L.esc_payload) return WCOMP_ECORRUPT;
+  if (len != L.serialized()) return WCOMP_ECORRUPT;
+  const uint8_t* p = b + kHeaderBytes;
+  if (get32(b + 80) != crc32_update(0, p, L.main_payload + L.esc_payload)) return WCOMP_ECORRUPT;
+  const int nb = scheme == WCOMP_BYTESPLIT ? 256 : 512;
+  for (int i = 0; i < kTableSize; ++i) {
+    table[i] = get16(b + 40 + 2 * i);
+    if (table[i] >= nb) return WCOMP_ECORRUPT;
+    for (int j = 0; j < i; ++j)
+      if (table[j] == table[i]) return WCOMP_ECORRUPT;
+  }
+  // escape positions: strictly ascending, below n, exactly the elements coded 15
+  const uint8_t* codes = p + L.off_codes;
+  const uint8_t* pos = p + L.main_payload + L.off_pos;
+  uint64_t e = 0;
+  for (uint64_t i = 0; i < n; ++i) {
+    uint32_t code = (codes[i >> 1] >> (4 * (i & 1))) & 0xF;
+    if (code == kEscape) {
+      if (e >= E || get32(pos + 4 * e) != i) return WCOMP_ECORRUPT;
+      ++e;
+    }
+  }
+  if (e != E) return WCOMP_ECORRUPT;
+  // tile and row indexes: escapes below each boundary
+  const uint8_t* ti = p + L.off_tile;
+  uint64_t k = 0;
+  for (uint64_t t = 0; t <= L.n_tiles; ++t) {
+    uint64_t bound = t * kTile;
+    while (k < E && get32(pos + 4 * k) < bound) ++k;
+    if (get32(ti + 4 * t) != k) return WCOMP_ECORRUPT;
+  }
+  const uint8_t* ri = p + L.off_row;
+  k = 0;
+  for (uint64_t r = 0; r <= uint64_t(N); ++r) {
+    uint64_t bound = r * uint64_t(K);
+    while (k < E && get32(pos + 4 * k) < bound) ++k;
+    if (get32(ri + 4 * r) != k) return WCOMP_ECORRUPT;
+  }
+  return WCOMP_OK;
+}
+
+extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* stream, wcomp_container** out) {
+  if (!host_buf || !out) return WCOMP_EINVAL;
+  *out = nullptr;
+  Layout L;
+  uint16_t table[kTableSize];
+  int st = validate(static_cast<const uint8_t*>(host_buf), len, L, table);
+  if (st != WCOMP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  wcomp_container* c = new (std::nothrow) wcomp_container();
+  if (!c) return WCOMP_ENOMEM;
+  c->L = L;
+  memcpy(c->table, table, sizeof(table));
+  cudaGetDevice(&c->device);
+  const uint8_t* p = static_cast<const uint8_t*>(host_buf) + kHeaderBytes;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
+  if (e == cudaSuccess && L.esc_payload) e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_main, p, L.main_payload, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && L.esc_payload)
+    e = cudaMemcpyAsync(c->d_esc, p + L.main_payload, L.esc_payload, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    wcomp_free(c, stream);
+    return map_cuda(e);
+  }
+  *out = c;
+  return WCOMP_OK;
+}
+
+extern "C" void wcomp_free(wcomp_container* c, void* stream) {
+  if (!c) return;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->d_main) cudaFreeAsync(c->d_main, s);
+  if (c->d_esc) cudaFreeAsync(c->d_esc, s);
+  delete c;
+}

@@ -1,0 +1,201 @@
+/*
+ * wcomp.h - lossless BF16 weight coding (byte-split and K15) with a standalone
+ * decode and a fused decode-GEMV, for NVIDIA GB300 (sm_103a).
+ *
+ * The method.  "Prueba de GLM-5.2 reduce la memoria BF16 en casi un 25%"
+ * (forgeeks.dev), section "Cómo funciona la compresión": a BF16 weight is
+ * 1 sign, 8 exponent and 7 mantissa bits; trained weights reuse a narrow set
+ * of sign+exponent symbols.
+ *   - byte-split: the high byte (sign + exponent bits 7..1) becomes a 4-bit
+ *     code into a per-tensor 15-entry dictionary, code 15 meaning "escape";
+ *     escaped high bytes are kept exactly in a (position, byte) stream and
+ *     the low byte is stored unchanged (12.005 bits/weight on the pages'
+ *     checkpoint, every tensor bit-exact);
+ *   - K15: the 9-bit sign+exponent symbol becomes a 4-bit code into a
+ *     15-entry table with the same escape rule; the 7-bit mantissa is stored
+ *     unchanged (11.173 bits/weight with all overhead on the pages' checkpoint).
+ * "Compresión de pesos LLM sin pérdida vs 8-bit GGUF" (wavect.io), section
+ * "¿Qué significa “sin pérdida” para los pesos de un LLM?": lossless means the
+ * round trip rebuilds every bit; a GPU may keep the weights encoded and rebuild
+ * exact BF16 in registers for the matrix product.  Section "Qué queda por
+ * demostrar" of the forgeeks page names the open step this library builds: a
+ * GEMV that rebuilds the weights in registers and applies the sparse escape
+ * correction in the same kernel.
+ *
+ * Conventions for every entry point below.
+ *   - Weights and activations are BF16 bit patterns passed as 16-bit words;
+ *     the codec never does float arithmetic on weights, so NaN, Inf, -0 and
+ *     subnormals round-trip.
+ *   - A weight tensor is W[N, K], row-major (y = x W^T).  n = N * K must be
+ *     in [1, 2^32); otherwise WCOMP_EUNSUPPORTED.
+ *   - Pointers named d_* are device pointers on the current CUDA device and
+ *     are owned by the caller.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).  Calls are stream-ordered and
+ *     asynchronous unless stated otherwise.
+ *   - Every call returns a wcomp_status and never aborts; CUDA errors are
+ *     WCOMP_ECUDA.  A failed call leaves its outputs unspecified and frees
+ *     what it allocated.
+ *   - Containers are opaque, owned by the library, and released with
+ *     wcomp_free.  A container lives on the device that was current when it
+ *     was made.
+ */
+#ifndef WCOMP_H
+#define WCOMP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WCOMP_VERSION 1
+
+#if defined(__GNUC__)
+#define WCOMP_API __attribute__((visibility("default")))
+#else
+#define WCOMP_API
+#endif
+
+typedef enum { WCOMP_BYTESPLIT = 0, WCOMP_K15 = 1 } wcomp_scheme;
+
+typedef enum {
+  WCOMP_OK = 0,
+  WCOMP_EINVAL = -1,        /* bad argument (null pointer, size, scheme, B) */
+  WCOMP_ENOMEM = -2,        /* device or host allocation failed */
+  WCOMP_ECORRUPT = -3,      /* serialized container failed validation */
+  WCOMP_ECUDA = -4,         /* a CUDA runtime call failed */
+  WCOMP_EUNSUPPORTED = -5   /* size outside the supported range */
+} wcomp_status;
+
+typedef struct wcomp_container wcomp_container;
+
+/* Description of a container (filled by wcomp_info). */
+typedef struct {
+  int32_t scheme;            /* wcomp_scheme */
+  int32_t version;           /* container format version */
+  int64_t N, K, n;           /* shape and element count */
+  uint64_t n_escapes;        /* E: elements whose symbol is not in the table */
+  uint32_t tile_elems;       /* granule of the tile escape index (8192) */
+  uint32_t n_tiles;
+  uint16_t table[15];        /* the 15 symbols, most frequent first */
+  uint16_t pad_;
+  uint64_t bytes_codes;      /* 4-bit code stream */
+  uint64_t bytes_raw;        /* raw low bytes (byte-split) or mantissa planes (K15) */
+  uint64_t bytes_index;      /* tile and row escape indexes */
+  uint64_t bytes_escapes;    /* escape positions and values */
+  uint64_t serialized_bytes; /* header + padded payload */
+  double entropy_bpw;        /* 4 + raw bits + (E + 15) * symbol bits / n */
+  double physical_bpw;       /* 8 * serialized_bytes / n */
+} wcomp_info_t;
+
+/*
+ * Encode one BF16 tensor.
+ *   d_w     device, uint16[N*K] row-major BF16 bits (any alignment; 16-byte
+ *           aligned input takes the vector path).
+ *   scheme  WCOMP_BYTESPLIT or WCOMP_K15.
+ *   out     receives a new container (NULL on failure).
+ * Steps (all on the GPU): per-tensor symbol histogram (256 or 512 bins),
+ * table of the 15 most frequent symbols (count descending, symbol ascending),
+ * 4-bit packing of codes and raw bits, per-tile escape counts and their scan,
+ * escape compaction in ascending position order, tile and row escape indexes.
+ * Synchronizes `stream` once to learn the escape count, which sizes the
+ * escape stream.  Output is deterministic and byte-identical to the CPU oracle.
+ */
+WCOMP_API int wcomp_encode(const uint16_t* d_w, int64_t N, int64_t K, int scheme, void* stream,
+                 wcomp_container** out);
+
+/*
+ * Decode a container to exact BF16 bits.
+ *   d_out   device, uint16[N*K]; the caller's buffer.
+ * The code stream is expanded through the 15-entry table, joined with the raw
+ * bits, and escaped elements are patched from the escape stream.
+ * Definition: forgeeks page, "Cómo funciona la compresión" (byte-split
+ * reconstruction of the high byte; K15 symbol + mantissa).
+ */
+WCOMP_API int wcomp_decode(const wcomp_container* c, uint16_t* d_out, void* stream);
+
+/*
+ * Fused decode-GEMV:  y[b, r] = sum_k x[b, k] * W[r, k]  for b < B, r < N.
+ *   d_x     device, uint16[B*K] BF16 bits, row-major, contiguous.
+ *   B       batch, 1 <= B <= 16.
+ *   d_y     device, float[B*N], row-major; overwritten.
+ * W is rebuilt in registers from the codes and raw bits; escaped weights are
+ * corrected inside the same kernel (y += x * (w_true - w_placeholder)).
+ * Products and sums are fp32; the summation order is fixed (no atomics), so
+ * repeated calls give identical bits.
+ * Definition: forgeeks page, "Qué queda por demostrar" (GEMV on codes rebuilt
+ * in registers, escape correction); wavect page on rebuilding exact BF16 in
+ * registers for the matmul.
+ */
+WCOMP_API int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream);
+
+/*
+ * Plain BF16 GEMV over an uncompressed W[N, K] with the same contract as
+ * wcomp_gemv; the comparison kernel for the fused path ("0.733x the BF16 GEMV
+ * time", forgeeks page, "Qué queda por demostrar").
+ */
+WCOMP_API int wcomp_gemv_bf16(const uint16_t* d_w, int64_t N, int64_t K, const uint16_t* d_x, int B,
+                    float* d_y, void* stream);
+
+/*
+ * Batched forms: one launch over `count` containers (any mix of schemes and
+ * shapes).  Arrays are host arrays of length count; every d_outs[i] /
+ * d_x[i] / d_y[i] is a device buffer sized for containers[i].  All
+ * containers must live on the current device.  count may be any positive
+ * number (large batches are split into several launches).
+ */
+WCOMP_API int wcomp_decode_batched(const wcomp_container* const* containers, uint16_t* const* d_outs,
+                         int count, void* stream);
+WCOMP_API int wcomp_gemv_batched(const wcomp_container* const* containers, const uint16_t* const* d_x,
+                       int B, float* const* d_y, int count, void* stream);
+
+/* Describe a container (host-side, no device work). */
+WCOMP_API int wcomp_info(const wcomp_container* c, wcomp_info_t* info);
+
+/*
+ * Serialize to a host buffer: a 96-byte header (magic "WCMP", version,
+ * scheme, N, K, E, tile size, table, payload length, CRC-32 of the payload,
+ * CRC-32 of the header) followed by the payload sections, each padded to 32
+ * bytes.  With host_buf == NULL only *len is set.  Returns WCOMP_EINVAL if
+ * cap is too small.  Synchronizes `stream`.
+ */
+WCOMP_API int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_t cap, uint64_t* len,
+                    void* stream);
+
+/*
+ * Rebuild a container from serialized bytes (host buffer).  The header, both
+ * checksums, the section sizes, the escape positions (strictly ascending,
+ * below n), both escape indexes and the agreement between escape codes and
+ * positions are validated on the host before anything is copied to the
+ * device; any mismatch returns WCOMP_ECORRUPT ("inject corruption" and
+ * "validate hashes", wavect page, "Un piloto de producción de 14 días").
+ * Synchronizes `stream`.
+ */
+WCOMP_API int wcomp_deserialize(const void* host_buf, uint64_t len, void* stream, wcomp_container** out);
+
+/*
+ * Release a container.  The device memory is returned in stream order on
+ * `stream`: work queued earlier on that stream may still use it.  NULL is a
+ * no-op.
+ */
+WCOMP_API void wcomp_free(wcomp_container* c, void* stream);
+
+/* Human-readable text for a status code (static string). */
+WCOMP_API const char* wcomp_strerror(int status);
+
+/* WCOMP_VERSION of the library that was loaded. */
+WCOMP_API int wcomp_version(void);
+
+/*
+ * Number of CUDA kernels this library has launched in the calling process
+ * (all devices, all threads).  Host-side counter, no device work; used to
+ * report how many of the library's own kernels a timed region ran.
+ */
+WCOMP_API uint64_t wcomp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WCOMP_H */

@@ -66,14 +66,14 @@ ESCAPE = 15
 TILE = 8192  # elements per decode tile (granule of the tile escape index)
 GROUP = 32  # elements per K15 raw-plane group
 HEADER_BYTES = 96
-ALIGN = 16
+ALIGN = 32  # every payload section starts on a 32-byte boundary (256-bit loads)
 
 SYM_BITS = {BYTESPLIT: 8, K15: 9}
 RAW_BITS = {BYTESPLIT: 8, K15: 7}
 NBINS = {BYTESPLIT: 256, K15: 512}
 
 
-def _pad16(nbytes: int) -> int:
+def _pad(nbytes: int) -> int:
     return (nbytes + ALIGN - 1) // ALIGN * ALIGN
 
 
@@ -354,7 +354,7 @@ def serialize(c: Container) -> bytes:
     for (name, arr), (name2, size) in zip(parts, sizes):
         assert name == name2 and arr.size == size, (name, arr.size, size)
         payload += arr.tobytes()
-        payload += b"\0" * (_pad16(size) - size)
+        payload += b"\0" * (_pad(size) - size)
     table16 = struct.pack("<15H", *[int(t) for t in c.table])
     head = (MAGIC + struct.pack("<HBB", VERSION, c.scheme, 0) +
             struct.pack("<qqQ", c.N, c.K, c.E) + struct.pack("<II", TILE, 0) +
@@ -387,7 +387,7 @@ def deserialize(buf: bytes) -> Container:
     if tile != TILE or N <= 0 or K <= 0 or not N * K < 2**32 or E > N * K:
         raise CorruptContainer("sizes")
     sizes = section_sizes(scheme, N, K, E)
-    if plen != sum(_pad16(s) for _, s in sizes) or len(buf) != HEADER_BYTES + plen:
+    if plen != sum(_pad(s) for _, s in sizes) or len(buf) != HEADER_BYTES + plen:
         raise CorruptContainer("payload length")
     payload = np.frombuffer(buf, dtype=np.uint8, offset=HEADER_BYTES)
     if zlib.crc32(payload.tobytes()) != pcrc:
@@ -396,7 +396,7 @@ def deserialize(buf: bytes) -> Container:
     off = 0
     for name, size in sizes:
         sec[name] = payload[off: off + size]
-        off += _pad16(size)
+        off += _pad(size)
     n = N * K
     esc_pos = sec["esc_pos"].view("<u4").astype(np.uint32)
     esc_val = sec["esc_val"].copy() if scheme == BYTESPLIT else sec["esc_val"].view("<u2").astype(np.uint16)
@@ -459,7 +459,7 @@ def physical_bpw(serialized_len: int, n: int) -> float:
 
 
 def serialized_len(scheme: int, N: int, K: int, E: int) -> int:
-    return HEADER_BYTES + sum(_pad16(s) for _, s in section_sizes(scheme, N, K, E))
+    return HEADER_BYTES + sum(_pad(s) for _, s in section_sizes(scheme, N, K, E))
 
 
 def reduction_pct(bpw: float) -> float:

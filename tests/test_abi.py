@@ -1,0 +1,130 @@
+"""The C-ABI library loads and exports every entry point that include/wcomp.h
+declares; host-side checks (argument errors, corrupt serialized containers)
+run without a GPU and agree with the CPU oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from decode_gemv_sign_gb300 import synth, wcomp
+from oracle import wcomp_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wcomp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_gemv_sign_gb300 import build
+
+    build.build()
+    return wcomp.lib()
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"WCOMP_API\s+[\w\s\*]+?\b(wcomp_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_api():
+    names = declared()
+    for n in ["wcomp_encode", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_decode_batched",
+              "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_free",
+              "wcomp_strerror", "wcomp_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared():
+        assert hasattr(lib, n), n
+    assert lib.wcomp_version() == 1
+    assert lib.wcomp_strerror(-3) == b"corrupt container"
+
+
+def test_argument_errors_without_gpu(lib):
+    h = ctypes.c_void_p()
+    assert lib.wcomp_encode(None, 4, 4, 0, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_encode(ctypes.c_void_p(256), 4, 4, 7, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_encode(ctypes.c_void_p(256), 0, 4, 0, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_encode(ctypes.c_void_p(256), 1 << 20, 1 << 12, 0, None, ctypes.byref(h)) == wcomp.EUNSUPPORTED
+    assert lib.wcomp_encode(ctypes.c_void_p(256), 4, 4, 0, None, None) == wcomp.EINVAL
+    assert lib.wcomp_info(None, None) == wcomp.EINVAL
+    assert lib.wcomp_decode(None, None, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv(None, None, 1, None, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16(ctypes.c_void_p(256), 4, 4, ctypes.c_void_p(256), 0, ctypes.c_void_p(256),
+                               None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16(ctypes.c_void_p(256), 4, 4, ctypes.c_void_p(256), 17, ctypes.c_void_p(256),
+                               None) == wcomp.EINVAL
+    lib.wcomp_free(None, None)  # no-op
+
+
+def _deser_status(lib, buf: bytes) -> int:
+    h = ctypes.c_void_p()
+    b = ctypes.create_string_buffer(buf, len(buf))
+    return lib.wcomp_deserialize(b, len(buf), None, ctypes.byref(h))
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_host_validation_matches_oracle(lib, scheme):
+    """Corrupt bytes are rejected on the host (before any device call); intact
+    oracle containers pass validation (the call then proceeds to the device)."""
+    w = synth.gen_weights_np(synth.WeightSpec("t", 16, 1000, "t4", 0.02, 0.02, "normal", 1.0, seed=5))
+    buf = bytearray(O.serialize(O.encode(w, scheme)))
+    ok = _deser_status(lib, bytes(buf))
+    assert ok != wcomp.ECORRUPT  # OK on a GPU machine, a CUDA error without a device
+    rng = np.random.default_rng(1)
+    for off in [0, 4, 6, 8, 24, 32, 40, 72, 80, 92] + list(rng.integers(96, len(buf), size=16)):
+        bad = bytearray(buf)
+        bad[off] ^= 0x04
+        with pytest.raises(O.CorruptContainer):
+            O.deserialize(bytes(bad))
+        assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    assert _deser_status(lib, bytes(buf[:-32])) == wcomp.ECORRUPT
+    assert _deser_status(lib, bytes(buf[:40])) == wcomp.ECORRUPT
+
+
+def _recrc(buf: bytearray):
+    import struct
+    import zlib
+    payload = bytes(buf[96:])
+    struct.pack_into("<I", buf, 80, zlib.crc32(payload))
+    struct.pack_into("<I", buf, 92, zlib.crc32(bytes(buf[:92])))
+
+
+def test_semantic_corruption_with_valid_checksums(lib):
+    """Checksums re-computed after tampering: the structural checks still catch it."""
+    import struct
+    w = synth.gen_weights_np(synth.WeightSpec("t", 8, 4096, "t4", 0.02, 0.02, "normal", 1.0, seed=6))
+    c = O.encode(w, O.BYTESPLIT)
+    assert c.E >= 2
+    buf = bytearray(O.serialize(c))
+    sizes = O.section_sizes(c.scheme, c.N, c.K, c.E)
+    off = {}
+    p = 96
+    for name, sz in sizes:
+        off[name] = p
+        p += O._pad(sz)
+    # 1. escape positions out of order
+    bad = bytearray(buf)
+    a, b = struct.unpack_from("<II", bad, off["esc_pos"])
+    struct.pack_into("<II", bad, off["esc_pos"], b, a)
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    # 2. a position beyond n
+    bad = bytearray(buf)
+    struct.pack_into("<I", bad, off["esc_pos"] + 4 * (c.E - 1), c.n + 5)
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    # 3. tile index disagreeing with the positions
+    bad = bytearray(buf)
+    struct.pack_into("<I", bad, off["tile_index"] + 4, 0xFFFF)
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    # 4. a duplicate table symbol
+    bad = bytearray(buf)
+    t0 = struct.unpack_from("<H", bad, 40)[0]
+    struct.pack_into("<H", bad, 42, t0)
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Bars: container bytes and decoded BF16 bit-exact; GEMV within
+max|y - y_oracle| <= 1e-4 * max|y_oracle| (fp32 accumulation against the
+float64 oracle); one-hot x reproduces the weight column exactly.
+"""
+import numpy as np
+import pytest
+
+from decode_gemv_sign_gb300 import synth
+from oracle import wcomp_oracle as O
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+GEMV_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def W():
+    from decode_gemv_sign_gb300 import build, wcomp
+
+    build.build()
+    wcomp.lib()
+    return wcomp
+
+
+def dev(a: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def host(t) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+def check_gemv(y_gpu, y_ref):
+    y = y_gpu.cpu().numpy().astype(np.float64)
+    scale = np.abs(y_ref).max()
+    err = np.abs(y - y_ref).max()
+    assert err <= GEMV_TOL * scale, (err, scale)
+
+
+CASES = {
+    "fixture5x200": lambda: synth.gen_weights_np(synth.WeightSpec("g", 5, 200, "t4", 0.02, 0.05, "normal", 100.0, seed=77)),
+    "all65536": lambda: np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256),
+    "shuffled65536": lambda: np.random.default_rng(3).permutation(np.arange(65536, dtype=np.uint32).astype(np.uint16)).reshape(128, 512),
+    "n1": lambda: np.array([[0x3F80]], dtype=np.uint16),
+    "n3": lambda: np.array([[0x3F80, 0xFF80, 0x0001]], dtype=np.uint16),
+    "n31": lambda: np.random.default_rng(31).integers(0, 65536, size=(1, 31)).astype(np.uint16),
+    "n33": lambda: np.random.default_rng(33).integers(0, 65536, size=(3, 11)).astype(np.uint16),
+    "n8191": lambda: np.random.default_rng(8191).integers(0, 65536, size=(1, 8191)).astype(np.uint16),
+    "n8193": lambda: synth.gen_weights_np(synth.WeightSpec("r", 1, 8193, "normal", 0.02, 0.01, "normal", 1.0, seed=8)),
+    "ragged7x301": lambda: synth.gen_weights_np(synth.WeightSpec("r", 7, 301, "t4", 0.02, 0.01, "normal", 1.0, seed=11)),
+    "tiles_40000x3": lambda: synth.gen_weights_np(synth.WeightSpec("r", 3, 40000, "t4", 0.02, 0.01, "normal", 1.0, seed=12)),
+    "specials": lambda: np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0xFFC1, 0x0001, 0x807F] * 100, dtype=np.uint16).reshape(8, 100),
+    "one_symbol": lambda: np.full((64, 64), 0x3C11, dtype=np.uint16),
+    "w1024": lambda: synth.gen_weights_np(synth.workload_small()[0]),
+}
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+@pytest.mark.parametrize("case", list(CASES))
+def test_container_and_decode_bit_exact(W, case, scheme):
+    w = CASES[case]()
+    ref = O.encode(w, scheme)
+    c = W.encode(dev(w), scheme)
+    inf = c.info()
+    assert inf["n_escapes"] == ref.E
+    assert inf["table"] == [int(t) for t in ref.table]
+    assert W.serialize(c) == O.serialize(ref)
+    out = W.decode(c)
+    assert np.array_equal(host(out).reshape(w.shape), w)
+    c.free()
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_unaligned_pointers(W, scheme):
+    w = synth.gen_weights_np(synth.WeightSpec("u", 9, 4096, "t4", 0.02, 0.01, "normal", 1.0, seed=21))
+    flat = np.concatenate([np.zeros(1, np.uint16), w.reshape(-1), np.zeros(1, np.uint16)])
+    big = dev(flat)
+    c = W.encode(big[1:1 + w.size].view(9, 4096), scheme)  # input offset by 2 bytes
+    assert W.serialize(c) == O.serialize(O.encode(w, scheme))
+    out = torch.zeros(w.size + 1, dtype=torch.int16, device="cuda")
+    W.decode(c, out[1:])  # output offset by 2 bytes
+    assert np.array_equal(host(out[1:]).reshape(w.shape), w)
+    xb = synth.gen_x_np(2, 4096, 5)
+    xf = dev(np.concatenate([np.zeros(1, np.uint16), xb.reshape(-1)]))
+    y = W.gemv(c, xf[1:].view(2, 4096))  # x offset: element path
+    check_gemv(y, O.gemv(w, xb))
+    c.free()
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_deserialize_roundtrip_on_gpu(W, scheme):
+    w = synth.gen_weights_np(synth.WeightSpec("d", 33, 1024, "t4", 0.02, 0.01, "normal", 1.0, seed=13))
+    buf = O.serialize(O.encode(w, scheme))
+    c = W.deserialize(buf)
+    assert np.array_equal(host(W.decode(c)).reshape(w.shape), w)
+    assert W.serialize(c) == buf
+    bad = bytearray(buf)
+    bad[200] ^= 1
+    with pytest.raises(W.CorruptContainer):
+        W.deserialize(bytes(bad))
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 8, 12, 16])
+def test_gemv_matches_oracle(W, scheme, B):
+    spec = synth.WeightSpec("g", 300, 2048, "t4", 0.02, 0.005, "normal", 1.0, seed=100 + B)
+    w = synth.gen_weights_np(spec)
+    x = synth.gen_x_np(B, spec.K, 200 + B)
+    c = W.encode(dev(w), scheme)
+    y = W.gemv(c, dev(x))
+    check_gemv(y, O.gemv(w, x))
+    # deterministic: same bits on a second call
+    y2 = W.gemv(c, dev(x))
+    assert torch.equal(y, y2)
+    c.free()
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+@pytest.mark.parametrize("B", [1, 4, 16])
+def test_gemv_ragged_k_element_path(W, scheme, B):
+    spec = synth.WeightSpec("g", 37, 1000, "t4", 0.02, 0.01, "normal", 1.0, seed=300 + B)
+    w = synth.gen_weights_np(spec)
+    x = synth.gen_x_np(B, spec.K, 301)
+    c = W.encode(dev(w), scheme)
+    check_gemv(W.gemv(c, dev(x)), O.gemv(w, x))
+    c.free()
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_gemv_one_hot_exact_and_zero(W, scheme):
+    spec = synth.WeightSpec("o", 64, 256, "normal", 0.02, 0.05, "normal", 1.0, seed=5)
+    w = synth.gen_weights_np(spec)
+    ref = O.encode(w, scheme)
+    assert ref.E > 0
+    c = W.encode(dev(w), scheme)
+    ks = sorted(set([0, 1, 31, 32, 255] + [int(p) % spec.K for p in ref.esc_pos[:12]]))
+    x = np.zeros((len(ks), spec.K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80
+    for b0 in range(0, len(ks), 16):
+        xb = x[b0:b0 + 16]
+        y = W.gemv(c, dev(xb)).cpu().numpy()
+        for i in range(xb.shape[0]):
+            col = (w[:, ks[b0 + i]].astype(np.uint32) << 16).view(np.float32)
+            assert np.array_equal(y[i], col)
+    y0 = W.gemv(c, torch.zeros((4, spec.K), dtype=torch.int16, device="cuda"))
+    assert not y0.any()
+    c.free()
+
+
+@pytest.mark.parametrize("B", [1, 3, 4, 16])
+def test_plain_bf16_gemv(W, B):
+    spec = synth.WeightSpec("p", 257, 4096, "normal", 0.02, seed=7)
+    w = synth.gen_weights_np(spec)
+    x = synth.gen_x_np(B, spec.K, 8)
+    check_gemv(W.gemv_bf16(dev(w), dev(x)), O.gemv(w, x))
+    w2 = synth.gen_weights_np(synth.WeightSpec("p", 13, 1000, "normal", 0.02, seed=9))
+    x2 = synth.gen_x_np(B, 1000, 10)
+    check_gemv(W.gemv_bf16(dev(w2), dev(x2)), O.gemv(w2, x2))
+
+
+def test_batched_matches_single(W):
+    specs = [synth.WeightSpec(f"b{i}", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=400 + i)
+             for i, (N, K) in enumerate([(64, 1024), (200, 640), (33, 1000), (128, 2048), (1, 4096)])]
+    ws = [synth.gen_weights_np(s) for s in specs]
+    cs = [W.encode(dev(w), i % 2) for i, w in enumerate(ws)]
+    outs = W.decode_batched(cs)
+    for w, o in zip(ws, outs):
+        assert np.array_equal(host(o).reshape(w.shape), w)
+    for B in (1, 4):
+        xs = [synth.gen_x_np(B, s.K, 500 + i) for i, s in enumerate(specs)]
+        ys = W.gemv_batched(cs, [dev(x) for x in xs])
+        for c, w, x, y in zip(cs, ws, xs, ys):
+            check_gemv(y, O.gemv(w, x))
+            assert torch.equal(y, W.gemv(c, dev(x)))
+    for c in cs:
+        c.free()
+
+
+def test_many_tensors_batch_over_limit(W):
+    # more containers than one launch carries
+    ws = [synth.gen_weights_np(synth.WeightSpec(f"m{i}", 16, 512, "normal", 0.02, 0.01, "normal", 1.0, seed=600 + i))
+          for i in range(70)]
+    cs = [W.encode(dev(w), i % 2) for i, w in enumerate(ws)]
+    outs = W.decode_batched(cs)
+    for w, o in zip(ws, outs):
+        assert np.array_equal(host(o).reshape(w.shape), w)
+    xs = [synth.gen_x_np(1, 512, 700 + i) for i in range(70)]
+    ys = W.gemv_batched(cs, [dev(x) for x in xs])
+    for w, x, y in zip(ws, xs, ys):
+        check_gemv(y, O.gemv(w, x))
+
+
+def test_argument_errors(W):
+    w = dev(np.zeros((4, 64), np.uint16))
+    c = W.encode(w, 0)
+    with pytest.raises(W.WcompError):
+        W.gemv(c, torch.zeros((17, 64), dtype=torch.int16, device="cuda"))
+    with pytest.raises(ValueError):
+        W.decode(c, torch.zeros(10, dtype=torch.int16, device="cuda"))
+    c.free()

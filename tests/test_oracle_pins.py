@@ -27,7 +27,7 @@ PAGES = json.load(open(os.path.join(HERE, "golden", "pages_figures.json")))
 # An independent reader of serialized containers, one element at a time.
 # ---------------------------------------------------------------------------
 def _pad(x):
-    return (x + 15) // 16 * 16
+    return (x + 31) // 32 * 32
 
 
 def read_element_pure(buf: bytes, i: int) -> int:
@@ -227,12 +227,12 @@ def test_serialized_size_closed_form(scheme):
     buf = O.serialize(c)
     E = c.E
     if scheme == 0:
-        # header 96, codes 524288, raw 1048576, tile index 129*4=516->528,
-        # row index 1025*4=4100->4112, positions 4E, values E (each padded to 16)
-        expect = 96 + 524288 + 1048576 + 528 + 4112 + _pad(4 * E) + _pad(E)
+        # header 96, codes 524288, raw 1048576, tile index 129*4=516->544,
+        # row index 1025*4=4100->4128, positions 4E, values E (each padded to 32)
+        expect = 96 + 524288 + 1048576 + 544 + 4128 + _pad(4 * E) + _pad(E)
     else:
         # 32768 groups: planes 524288 + 262144 + 131072; values 2E
-        expect = 96 + 524288 + 524288 + 262144 + 131072 + 528 + 4112 + _pad(4 * E) + _pad(2 * E)
+        expect = 96 + 524288 + 524288 + 262144 + 131072 + 544 + 4128 + _pad(4 * E) + _pad(2 * E)
     assert len(buf) == expect
     assert O.serialized_len(scheme, c.N, c.K, E) == expect
     # checksums are standard CRC-32 values over header / payload
