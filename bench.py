@@ -8,7 +8,8 @@ N(0, 0.5) outliers), in both schemes (byte-split and K15):
      compaction, row index)
   2. decode all 14 containers to exact BF16 in one batched launch
   3. fused decode-GEMV over all 14 containers at batch 1 and batch 4
-  4. plain BF16 GEMV over the 7 raw tensors at batch 1 and batch 4
+  4. plain BF16 GEMV over the 7 raw tensors at batch 1 and batch 4 (one
+     batched launch each, the same launch structure as the fused GEMV)
 
 `value` is the step's algorithmic HBM bytes (the minimum each launch must
 move, see `bytes_*` below) divided by the device time of the step, in GB/s.
@@ -83,33 +84,57 @@ REASON_FIELDS = ["clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_th
 
 
 class ClockSampler:
+    """nvidia-smi sampled every 20 ms in the background; only samples taken
+    between mark_start() and mark_end() count."""
+
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/.clocks_{os.getpid()}.csv"
+        self.rows = []
+        self.t0 = self.t1 = None
 
     def start(self):
+        import threading
+
         q = "clocks.sm,clocks.max.sm,power.draw," + ",".join(REASON_FIELDS)
         try:
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.time(), line))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        # let the sampler come up before the timed region starts
+        deadline = time.time() + 3.0
+        while not self.rows and time.time() < deadline:
+            time.sleep(0.01)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        self.f.close()
         sm, mx, reasons = [], [], set()
-        for line in open(self.path):
+        inside = [r for r in self.rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e30)]
+        use = inside if inside else self.rows[-3:]
+        for _, line in use:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 3 + len(REASON_FIELDS):
                 continue
@@ -121,14 +146,10 @@ class ClockSampler:
             for name, v in zip(REASON_FIELDS, parts[3:]):
                 if v.lower() == "active":
                     reasons.add(name.split(".")[-1])
-        try:
-            os.remove(self.path)
-        except OSError:
-            pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
 def measured_peaks() -> dict:
@@ -289,8 +310,7 @@ class HotPath:
             marks.append((f"gemv_fused_b{B}", prev, e))
             prev = e
         for B in BATCHES:
-            for w, x, y in zip(self.weights, self.xs[B], self.yp[B]):
-                W.gemv_bf16(w, x, y, stream=self.stream)
+            W.gemv_bf16_batched(self.weights, self.xs[B], self.yp[B], stream=self.stream)
             e = mark() if ev is not None else None
             marks.append((f"gemv_plain_b{B}", prev, e))
             prev = e
@@ -342,8 +362,7 @@ def time_scheme_split(hp, W, torch, B: int, reps: int = 5) -> dict:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(hp.stream)
-        for w, x, y in zip(hp.weights, hp.xs[B], hp.yp[B]):
-            W.gemv_bf16(w, x, y, stream=hp.stream)
+        W.gemv_bf16_batched(hp.weights, hp.xs[B], hp.yp[B], stream=hp.stream)
         b.record(hp.stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
@@ -379,6 +398,7 @@ def run_ours(args):
     ev = []
     barrier(dist)
     torch.cuda.synchronize()
+    clocks.mark_start()
     n0 = W.launch_count()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -387,6 +407,7 @@ def run_ours(args):
         hp.step(ev)
     end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     barrier(dist)
     launches = W.launch_count() - n0
     clk = clocks.stop()

@@ -9,19 +9,30 @@
 // sin pérdida vs 8-bit GGUF", section "¿Qué significa “sin pérdida” para los
 // pesos de un LLM?": exact BF16 rebuilt in registers and used at once.
 //
-// Work decomposition: a warp owns a set of R consecutive rows and walks the
-// whole row; lane l takes the 32-element groups l, l+32, ... .  For each group
-// the lane loads 16 code bytes and 32 raw bytes (byte-split) or 28 plane bytes
-// (K15) per row with streaming vector loads that bypass L1, rebuilds BF16
-// pairs with prmt lookups, widens them to fp32 with a shift / mask and
-// accumulates with packed fp32x2 FMAs.  x is read through L1 (it is shared by
-// every warp of the SM).  Escaped weights decode to the placeholder (symbol
-// 0, |w| < 2^-125); each lane then adds x * (w_true - w_placeholder) for a
-// share of the row's escapes, found in O(1) through the row index.  Lanes are
-// combined with a fixed butterfly, so results do not depend on scheduling.
+// Work decomposition.  A unit of work is a set of R consecutive rows of one
+// tensor; a launch covers the units of every tensor in the batch.  The grid is
+// persistent (as many CTAs as fit on the GPU at once) and every warp grabs
+// units from a global counter, one at a time, so the GPU drains evenly even
+// when the tensors differ in shape.  Inside a unit the warp walks the rows:
+// lane l takes the 32-element groups l, l+32, ..., keeps the next group's
+// loads in flight while it computes the current one (register double
+// buffering), loads each stream with vector loads that bypass L1, rebuilds
+// BF16 pairs with prmt lookups, widens them to fp32 with a shift / mask and
+// accumulates with packed fp32x2 FMAs.  x is read through L1, where it stays
+// (every warp of the SM reads the same x).
+//
+// Escapes.  An escaped weight decodes to the placeholder (symbol 0, so
+// |w| < 2^-125).  Each lane adds x * (w_true - w_placeholder) for a share of
+// the unit's escapes, found in O(1) through the row index; their positions
+// and values are requested before the main loop so the loads overlap it.
+// Lanes are combined with a fixed butterfly: results do not depend on which
+// warp ran which unit.
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "wcomp_impl.cuh"
 
@@ -30,6 +41,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSlots = 1024;  // work-counter slots per device (one per launch, round robin)
+
+enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
 struct F2 {
   float x, y;
@@ -48,31 +62,119 @@ __device__ __forceinline__ void fma2(F2& acc, uint32_t w_pair, float x0, float x
 
 __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
   uint4 v;
-  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  asm("ld.global.nc.L1::evict_last.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
   return v;
 }
 
-// Find the tensor that owns global row set `set`.
-__device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t set) {
+// Find the tensor that owns global unit `u`.
+__device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t u) {
   int i = 0;
-  while (i + 1 < count && prefix[i + 1] <= set) ++i;
+  while (i + 1 < count && prefix[i + 1] <= u) ++i;
   return i;
 }
 
-// Escape correction for row r: lane-strided share of the row's escapes.
-template <int BT>
-__device__ __forceinline__ void escape_correction(const TensorDesc& d, const uint16_t* __restrict__ x, int B,
-                                                  int64_t r, int lane, float (&s)[BT]) {
-  const uint32_t e0 = d.row_index[r], e1 = d.row_index[r + 1];
-  for (uint32_t e = e0 + lane; e < e1; e += 32) {
-    const uint32_t p = d.esc_pos[e];
-    const int64_t k = int64_t(p) - r * d.K;
-    const uint32_t wt = escape_word(d, e, p);
-    const uint32_t wph = d.scheme == WCOMP_BYTESPLIT ? (wt & 0xFFu) : (wt & 0x7Fu);
-    const float delta = __uint_as_float(wt << 16) - __uint_as_float(wph << 16);
+// ---------------------------------------------------------------------------
+// Weight sources: one 32-element group of one row.
+// ---------------------------------------------------------------------------
+struct GroupBuf {
+  uint32_t v[16];
+};
+
+template <int SRC>
+__device__ __forceinline__ void load_buf(const TensorDesc& d, uint64_t g, GroupBuf& b) {
+  if (SRC == kBytesplit) {
+    const uint4 c = ld_stream_v4(d.codes + 16 * g);
+    b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
+    uint32_t r[8];
+    ld_stream_v8(d.raw + 32 * g, r);
 #pragma unroll
-    for (int b = 0; b < BT; ++b)
-      if (b < B) s[b] = fmaf(__uint_as_float(uint32_t(x[int64_t(b) * d.K + k]) << 16), delta, s[b]);
+    for (int i = 0; i < 8; ++i) b.v[4 + i] = r[i];
+  } else if (SRC == kK15) {
+    const uint4 c = ld_stream_v4(d.codes + 16 * g);
+    const uint4 a = ld_stream_v4(d.pa + 16 * g);
+    const uint2 pb = ld_stream_v2(d.pb + 8 * g);
+    b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
+    b.v[4] = a.x; b.v[5] = a.y; b.v[6] = a.z; b.v[7] = a.w;
+    b.v[8] = pb.x; b.v[9] = pb.y;
+    b.v[10] = ld_stream_u32(d.pc + 4 * g);
+  } else {
+    uint32_t r[8];
+    const uint8_t* w = d.raw + 64 * g;
+    ld_stream_v8(w, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b.v[i] = r[i];
+    ld_stream_v8(w + 32, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b.v[8 + i] = r[i];
+  }
+}
+
+// BF16 pairs of code word I (elements 8I .. 8I+7) of a loaded group.
+template <int SRC, int I>
+__device__ __forceinline__ void pairs8(const RegTable& t, const GroupBuf& b, uint32_t (&w)[4]) {
+  if (SRC == kPlain) {
+    w[0] = b.v[4 * I + 0]; w[1] = b.v[4 * I + 1]; w[2] = b.v[4 * I + 2]; w[3] = b.v[4 * I + 3];
+    return;
+  }
+  const uint32_t cw = b.v[I];
+  const QuadMasks m = code_masks(cw);
+  const uint32_t m7 = cw & 0x77777777u;
+  uint32_t h0, h1, l0, l1;
+  lookup8(t.hi, m7, m, h0, h1);
+  if (SRC == kBytesplit) {
+    l0 = b.v[4 + 2 * I];
+    l1 = b.v[5 + 2 * I];
+  } else {
+    const uint32_t a[4] = {b.v[4], b.v[5], b.v[6], b.v[7]};
+    const uint32_t pb[2] = {b.v[8], b.v[9]};
+    uint32_t e0, e1;
+    lookup8(t.e0, m7, m, e0, e1);
+    l0 = k15_mant<2 * I>(a, pb, b.v[10]) | e0;
+    l1 = k15_mant<2 * I + 1>(a, pb, b.v[10]) | e1;
+  }
+  w[0] = prmt(l0, h0, 0x5140);
+  w[1] = prmt(l0, h0, 0x7362);
+  w[2] = prmt(l1, h1, 0x5140);
+  w[3] = prmt(l1, h1, 0x7362);
+}
+
+template <int SRC, int BT, int R>
+__device__ __forceinline__ void compute_group(const TensorDesc& d, const uint16_t* __restrict__ xg, int64_t K, int B,
+                                              const GroupBuf (&buf)[R], const bool (&live)[R], F2 (&acc)[R][BT]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float xf[BT][8];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      if (b < B) {
+        const uint4 v = ld_x_v4(xg + int64_t(b) * K + 8 * i);
+        xf[b][0] = bf16_lo(v.x); xf[b][1] = bf16_hi(v.x);
+        xf[b][2] = bf16_lo(v.y); xf[b][3] = bf16_hi(v.y);
+        xf[b][4] = bf16_lo(v.z); xf[b][5] = bf16_hi(v.z);
+        xf[b][6] = bf16_lo(v.w); xf[b][7] = bf16_hi(v.w);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xf[b][k] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (!live[j]) continue;
+      uint32_t w[4];
+      if (i == 0) pairs8<SRC, 0>(d.t, buf[j], w);
+      else if (i == 1) pairs8<SRC, 1>(d.t, buf[j], w);
+      else if (i == 2) pairs8<SRC, 2>(d.t, buf[j], w);
+      else pairs8<SRC, 3>(d.t, buf[j], w);
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        fma2(acc[j][b], w[0], xf[b][0], xf[b][1]);
+        fma2(acc[j][b], w[1], xf[b][2], xf[b][3]);
+        fma2(acc[j][b], w[2], xf[b][4], xf[b][5]);
+        fma2(acc[j][b], w[3], xf[b][6], xf[b][7]);
+      }
+    }
   }
 }
 
@@ -88,104 +190,137 @@ __device__ __forceinline__ void warp_reduce_store(float (&s)[BT], int B, float* 
   }
 }
 
+// x * (w_true - w_placeholder) for one escape of the row starting at element rowbase.
+template <int BT>
+__device__ __forceinline__ void add_escape(const TensorDesc& d, const uint16_t* __restrict__ x, int B, uint64_t rowbase,
+                                           uint32_t p, uint32_t val, float (&s)[BT]) {
+  uint32_t wt, wph;
+  if (d.scheme == WCOMP_BYTESPLIT) {
+    wph = d.raw[p];
+    wt = (val << 8) | wph;
+  } else {
+    wt = val;
+    wph = val & 0x7Fu;
+  }
+  const float delta = __uint_as_float(wt << 16) - __uint_as_float(wph << 16);
+  const int64_t k = int64_t(uint64_t(p) - rowbase);
+#pragma unroll
+  for (int b = 0; b < BT; ++b)
+    if (b < B) s[b] = fmaf(__uint_as_float(uint32_t(x[int64_t(b) * d.K + k]) << 16), delta, s[b]);
+}
+
+__device__ __forceinline__ uint32_t load_esc_val(const TensorDesc& d, uint32_t e) {
+  return d.scheme == WCOMP_BYTESPLIT ? uint32_t(d.esc_val[e]) : uint32_t(reinterpret_cast<const uint16_t*>(d.esc_val)[e]);
+}
+
+__device__ __forceinline__ uint32_t grab(uint32_t* slot, int lane) {
+  uint32_t u = 0;
+  if (lane == 0) u = atomicAdd(slot, 1u);
+  return __shfl_sync(0xffffffffu, u, 0);
+}
+
 // ---------------------------------------------------------------------------
-// Fused decode-GEMV, vector path (K % 32 == 0, 16-byte aligned x).
+// The kernel (vector path: K % 32 == 0, aligned streams and x).
 // ---------------------------------------------------------------------------
-template <int SCHEME, int BT, int R>
-__global__ void __launch_bounds__(kThreads) gemv_fused_kernel(const __grid_constant__ GemvBatch p, uint32_t total_sets,
-                                                              int B) {
+template <int SRC, int BT, int R, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    gemv_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
   const int lane = threadIdx.x & 31;
-  const uint32_t warp_id = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const uint32_t nwarps = gridDim.x * kWarps;
-  for (uint32_t set = warp_id; set < total_sets; set += nwarps) {
-    const int ti = owner(p.set_prefix, p.count, set);
+  uint32_t u = grab(slot, lane);
+  while (u < total_units) {
+    const uint32_t u_next = grab(slot, lane);  // in flight while this unit runs
+    const int ti = owner(p.set_prefix, p.count, u);
     const TensorDesc& d = p.d[ti];
     const uint16_t* __restrict__ x = p.x[ti];
-    const int64_t r0 = int64_t(set - p.set_prefix[ti]) * R;
+    const int64_t r0 = int64_t(u - p.set_prefix[ti]) * R;
     const int64_t K = d.K;
     const uint64_t KG = uint64_t(K) / kGroup;
+    bool live[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
     F2 acc[R][BT];
 #pragma unroll
     for (int j = 0; j < R; ++j)
 #pragma unroll
       for (int b = 0; b < BT; ++b) acc[j][b] = F2{0.f, 0.f};
-    bool live[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
 
-    for (uint64_t gk = lane; gk < KG; gk += 32) {
-      uint32_t cw[R][4], rw[R][8];
+    GroupBuf b0[R], b1[R];
+    uint64_t gk = lane;
+    if (gk < KG) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        if (live[j]) {
-          load_group<SCHEME>(d, uint64_t(r0 + j) * KG + gk, cw[j], rw[j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) cw[j][i] = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) rw[j][i] = 0;
-        }
+      for (int j = 0; j < R; ++j)
+        if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk, b0[j]);
+    }
+    // escape slice of the unit: index now, first entries right after
+    uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
+    if (SRC != kPlain) {
+      const int64_t r_end = r0 + R < d.N ? r0 + R : d.N;
+      e_lo = d.row_index[r0];
+      e_hi = d.row_index[r_end];
+      if (e_lo + lane < e_hi) {
+        p0 = d.esc_pos[e_lo + lane];
+        v0 = load_esc_val(d, e_lo + lane);
       }
-      const uint16_t* xg = x + gk * kGroup;
+    }
+    for (; gk < KG; gk += 64) {
+      const bool more = gk + 32 < KG;
+      if (more) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {  // 8 elements per code word
-        float xf[BT][8];
+        for (int j = 0; j < R; ++j)
+          if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 32, b1[j]);
+      }
+      compute_group<SRC, BT, R>(d, x + gk * kGroup, K, B, b0, live, acc);
+      if (!more) break;
+      if (gk + 64 < KG) {
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (b < B) {
-            const uint4 v = ld_x_v4(xg + int64_t(b) * K + 8 * i);
-            xf[b][0] = bf16_lo(v.x); xf[b][1] = bf16_hi(v.x);
-            xf[b][2] = bf16_lo(v.y); xf[b][3] = bf16_hi(v.y);
-            xf[b][4] = bf16_lo(v.z); xf[b][5] = bf16_hi(v.z);
-            xf[b][6] = bf16_lo(v.w); xf[b][7] = bf16_hi(v.w);
-          } else {
+        for (int j = 0; j < R; ++j)
+          if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 64, b0[j]);
+      }
+      compute_group<SRC, BT, R>(d, x + (gk + 32) * kGroup, K, B, b1, live, acc);
+    }
+
+    float s[R][BT];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) xf[b][k] = 0.f;
-          }
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) s[j][b] = acc[j][b].x + acc[j][b].y;
+    if (SRC != kPlain) {
+      // escapes of the unit, lane-strided; each goes to the row that holds it
+      for (uint32_t e = e_lo + lane; e < e_hi; e += 32) {
+        uint32_t pos = p0, val = v0;
+        if (e != e_lo + lane) {
+          pos = d.esc_pos[e];
+          val = load_esc_val(d, e);
         }
+        const int64_t j = int64_t(pos / uint64_t(K)) - r0;
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const QuadMasks m = code_masks(cw[j][i]);
-          const uint32_t m7 = cw[j][i] & 0x77777777u;
-          uint32_t h0, h1;
-          lookup8(d.t.hi, m7, m, h0, h1);
-          uint32_t l0 = rw[j][2 * i], l1 = rw[j][2 * i + 1];
-          if (SCHEME == WCOMP_K15) {
-            uint32_t e0, e1;
-            lookup8(d.t.e0, m7, m, e0, e1);
-            l0 |= e0;
-            l1 |= e1;
-          }
-          const uint32_t w01 = prmt(l0, h0, 0x5140), w23 = prmt(l0, h0, 0x7362);
-          const uint32_t w45 = prmt(l1, h1, 0x5140), w67 = prmt(l1, h1, 0x7362);
-#pragma unroll
-          for (int b = 0; b < BT; ++b) {
-            fma2(acc[j][b], w01, xf[b][0], xf[b][1]);
-            fma2(acc[j][b], w23, xf[b][2], xf[b][3]);
-            fma2(acc[j][b], w45, xf[b][4], xf[b][5]);
-            fma2(acc[j][b], w67, xf[b][6], xf[b][7]);
-          }
-        }
+        for (int jj = 0; jj < R; ++jj)
+          if (jj == j) add_escape<BT>(d, x, B, uint64_t(r0 + jj) * uint64_t(K), pos, val, s[jj]);
       }
     }
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      if (!live[j]) continue;  // uniform across the warp
-      float s[BT];
-#pragma unroll
-      for (int b = 0; b < BT; ++b) s[b] = acc[j][b].x + acc[j][b].y;
-      escape_correction<BT>(d, x, B, r0 + j, lane, s);
-      warp_reduce_store<BT>(s, B, p.y[ti], d.N, r0 + j, lane);
+    for (int j = 0; j < R; ++j)
+      if (live[j]) warp_reduce_store<BT>(s[j], B, p.y[ti], d.N, r0 + j, lane);
+    u = u_next;
+  }
+  // The last warp to finish returns the counter slot to zero for the next launch.
+  if (lane == 0) {
+    __threadfence();
+    const uint32_t total_warps = gridDim.x * kWarps;
+    if (atomicAdd(slot + 1, 1u) == total_warps - 1) {
+      atomicExch(slot, 0u);
+      atomicExch(slot + 1, 0u);
+      __threadfence();
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Fused decode-GEMV, element path (any K, any alignment): one warp per row.
+// Element path (any K, any alignment): one warp per row, static schedule.
 // ---------------------------------------------------------------------------
-template <int BT>
-__global__ void __launch_bounds__(kThreads) gemv_fused_generic_kernel(const __grid_constant__ GemvBatch p,
-                                                                      uint32_t total_rows, int B) {
+template <int SRC, int BT>
+__global__ void __launch_bounds__(kThreads) gemv_generic_kernel(const __grid_constant__ GemvBatch p,
+                                                                uint32_t total_rows, int B) {
   const int lane = threadIdx.x & 31;
   const uint32_t warp_id = blockIdx.x * kWarps + (threadIdx.x >> 5);
   for (uint32_t row = warp_id; row < total_rows; row += gridDim.x * kWarps) {
@@ -197,146 +332,89 @@ __global__ void __launch_bounds__(kThreads) gemv_fused_generic_kernel(const __gr
 #pragma unroll
     for (int b = 0; b < BT; ++b) s[b] = 0.f;
     for (int64_t k = lane; k < d.K; k += 32) {
-      const float w = __uint_as_float(decode_elem_placeholder(d, uint64_t(r * d.K + k)) << 16);
+      const uint64_t i = uint64_t(r * d.K + k);
+      const uint32_t wb = SRC == kPlain ? uint32_t(reinterpret_cast<const uint16_t*>(d.raw)[i])
+                                        : decode_elem_placeholder(d, i);
+      const float w = __uint_as_float(wb << 16);
 #pragma unroll
       for (int b = 0; b < BT; ++b)
         if (b < B) s[b] = fmaf(w, __uint_as_float(uint32_t(x[int64_t(b) * d.K + k]) << 16), s[b]);
     }
-    escape_correction<BT>(d, x, B, r, lane, s);
+    if (SRC != kPlain) {
+      const uint32_t e0 = d.row_index[r], e1 = d.row_index[r + 1];
+      for (uint32_t e = e0 + lane; e < e1; e += 32)
+        add_escape<BT>(d, x, B, uint64_t(r) * uint64_t(d.K), d.esc_pos[e], load_esc_val(d, e), s);
+    }
     warp_reduce_store<BT>(s, B, p.y[ti], d.N, r, lane);
   }
 }
 
 // ---------------------------------------------------------------------------
-// Plain BF16 GEMV (the comparison kernel): same decomposition, W read raw.
-// ---------------------------------------------------------------------------
-struct PlainArgs {
-  const uint16_t* w;
-  const uint16_t* x;
-  float* y;
-  int64_t N, K;
-};
-
-template <int BT, int R>
-__global__ void __launch_bounds__(kThreads) gemv_bf16_kernel(const __grid_constant__ PlainArgs a, int B) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t warp_id = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const uint32_t nwarps = gridDim.x * kWarps;
-  const int64_t K = a.K;
-  const uint64_t KG = uint64_t(K) / kGroup;
-  const uint32_t sets = uint32_t(cdiv(uint64_t(a.N), R));
-  for (uint32_t set = warp_id; set < sets; set += nwarps) {
-    const int64_t r0 = int64_t(set) * R;
-    F2 acc[R][BT];
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[j][b] = F2{0.f, 0.f};
-    bool live[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) live[j] = r0 + j < a.N;
-    for (uint64_t gk = lane; gk < KG; gk += 32) {
-      uint32_t wv[R][16];
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        if (live[j]) {
-          const uint16_t* src = a.w + (uint64_t(r0 + j) * KG + gk) * kGroup;
-          ld_stream_v8(src, *reinterpret_cast<uint32_t(*)[8]>(&wv[j][0]));
-          ld_stream_v8(src + 16, *reinterpret_cast<uint32_t(*)[8]>(&wv[j][8]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) wv[j][i] = 0;
-        }
-      }
-      const uint16_t* xg = a.x + gk * kGroup;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float xf[BT][8];
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (b < B) {
-            const uint4 v = ld_x_v4(xg + int64_t(b) * K + 8 * i);
-            xf[b][0] = bf16_lo(v.x); xf[b][1] = bf16_hi(v.x);
-            xf[b][2] = bf16_lo(v.y); xf[b][3] = bf16_hi(v.y);
-            xf[b][4] = bf16_lo(v.z); xf[b][5] = bf16_hi(v.z);
-            xf[b][6] = bf16_lo(v.w); xf[b][7] = bf16_hi(v.w);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) xf[b][k] = 0.f;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-#pragma unroll
-          for (int b = 0; b < BT; ++b) {
-            fma2(acc[j][b], wv[j][4 * i + 0], xf[b][0], xf[b][1]);
-            fma2(acc[j][b], wv[j][4 * i + 1], xf[b][2], xf[b][3]);
-            fma2(acc[j][b], wv[j][4 * i + 2], xf[b][4], xf[b][5]);
-            fma2(acc[j][b], wv[j][4 * i + 3], xf[b][6], xf[b][7]);
-          }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      if (!live[j]) continue;
-      float s[BT];
-#pragma unroll
-      for (int b = 0; b < BT; ++b) s[b] = acc[j][b].x + acc[j][b].y;
-      warp_reduce_store<BT>(s, B, a.y, a.N, r0 + j, lane);
-    }
-  }
-}
-
-template <int BT>
-__global__ void __launch_bounds__(kThreads) gemv_bf16_generic_kernel(const __grid_constant__ PlainArgs a, int B) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t warp_id = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  for (int64_t r = warp_id; r < a.N; r += int64_t(gridDim.x) * kWarps) {
-    float s[BT];
-#pragma unroll
-    for (int b = 0; b < BT; ++b) s[b] = 0.f;
-    for (int64_t k = lane; k < a.K; k += 32) {
-      const float w = __uint_as_float(uint32_t(a.w[r * a.K + k]) << 16);
-#pragma unroll
-      for (int b = 0; b < BT; ++b)
-        if (b < B) s[b] = fmaf(w, __uint_as_float(uint32_t(a.x[int64_t(b) * a.K + k]) << 16), s[b]);
-    }
-    warp_reduce_store<BT>(s, B, a.y, a.N, r, lane);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Host dispatch.
+// Host side.
 // ---------------------------------------------------------------------------
 int pow2_batch(int B) { return B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16; }
 
-template <int SCHEME, int BT, int R>
-void launch_fused(const GemvBatch& b, uint32_t sets, int B, int sms, cudaStream_t s) {
-  const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(sets, kWarps), uint64_t(sms) * 8));
-  gemv_fused_kernel<SCHEME, BT, R><<<blocks, kThreads, 0, s>>>(b, sets, B);
-  count_launches(1);
+// Per-device scratch: kSlots work-counter pairs, zeroed once at allocation.
+// Each launch takes the next slot; its last warp zeroes the slot again.
+std::mutex g_scratch_mu;
+uint32_t* g_scratch[64] = {nullptr};
+std::atomic<uint32_t> g_slot_rr{0};
+
+int counter_slot(int dev, uint32_t** slot) {
+  if (dev < 0 || dev >= 64) return WCOMP_EUNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    if (!g_scratch[dev]) {
+      uint32_t* p = nullptr;
+      cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p), kSlots * 2 * sizeof(uint32_t));
+      if (e == cudaSuccess) e = cudaMemset(p, 0, kSlots * 2 * sizeof(uint32_t));
+      if (e != cudaSuccess) return map_cuda(e);
+      g_scratch[dev] = p;
+    }
+  }
+  *slot = g_scratch[dev] + 2 * (g_slot_rr.fetch_add(1, std::memory_order_relaxed) % kSlots);
+  return WCOMP_OK;
 }
 
-template <int SCHEME>
-void dispatch_fused(GemvBatch& b, const int64_t* Ns, int B, int sms, cudaStream_t s) {
-  const int BT = pow2_batch(B);
-  const int R = BT >= 16 ? 1 : 2;
-  uint32_t sets = 0;
+template <int SRC, int BT, int R, int MINB>
+int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
-    b.set_prefix[j] = sets;
-    sets += uint32_t(cdiv(uint64_t(Ns[j]), R));
+    b.set_prefix[j] = units;
+    units += uint32_t(cdiv(uint64_t(Ns[j]), R));
   }
-  b.set_prefix[b.count] = sets;
-  switch (BT) {
-    case 1: launch_fused<SCHEME, 1, 2>(b, sets, B, sms, s); break;
-    case 2: launch_fused<SCHEME, 2, 2>(b, sets, B, sms, s); break;
-    case 4: launch_fused<SCHEME, 4, 2>(b, sets, B, sms, s); break;
-    case 8: launch_fused<SCHEME, 8, 2>(b, sets, B, sms, s); break;
-    default: launch_fused<SCHEME, 16, 1>(b, sets, B, sms, s); break;
+  b.set_prefix[b.count] = units;
+  uint32_t* slot = nullptr;
+  int st = counter_slot(dev, &slot);
+  if (st != WCOMP_OK) return st;
+  static int per_sm_cache = 0;
+  if (!per_sm_cache) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB>, kThreads, 0) !=
+            cudaSuccess ||
+        per_sm <= 0)
+      per_sm = 1;
+    per_sm_cache = per_sm;
+  }
+  const int blocks = per_sm_cache * sms;
+  gemv_kernel<SRC, BT, R, MINB><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
+  count_launches(1);
+  return map_cuda(cudaGetLastError());
+}
+
+template <int SRC>
+int dispatch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  switch (pow2_batch(B)) {
+    case 1: return launch_vec<SRC, 1, 1, 3>(b, Ns, B, dev, sms, s);
+    case 2: return launch_vec<SRC, 2, 1, 3>(b, Ns, B, dev, sms, s);
+    case 4: return launch_vec<SRC, 4, 2, 2>(b, Ns, B, dev, sms, s);
+    case 8: return launch_vec<SRC, 8, 1, 2>(b, Ns, B, dev, sms, s);
+    default: return launch_vec<SRC, 16, 1, 1>(b, Ns, B, dev, sms, s);
   }
 }
 
-void dispatch_generic(GemvBatch& b, const int64_t* Ns, int B, int sms, cudaStream_t s) {
+template <int SRC>
+int dispatch_generic(GemvBatch& b, const int64_t* Ns, int B, int sms, cudaStream_t s) {
   uint32_t rows = 0;
   for (int j = 0; j < b.count; ++j) {
     b.set_prefix[j] = rows;
@@ -345,58 +423,104 @@ void dispatch_generic(GemvBatch& b, const int64_t* Ns, int B, int sms, cudaStrea
   b.set_prefix[b.count] = rows;
   const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(rows, kWarps), uint64_t(sms) * 8));
   switch (pow2_batch(B)) {
-    case 1: gemv_fused_generic_kernel<1><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
-    case 2: gemv_fused_generic_kernel<2><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
-    case 4: gemv_fused_generic_kernel<4><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
-    case 8: gemv_fused_generic_kernel<8><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
-    default: gemv_fused_generic_kernel<16><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
+    case 1: gemv_generic_kernel<SRC, 1><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
+    case 2: gemv_generic_kernel<SRC, 2><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
+    case 4: gemv_generic_kernel<SRC, 4><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
+    case 8: gemv_generic_kernel<SRC, 8><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
+    default: gemv_generic_kernel<SRC, 16><<<blocks, kThreads, 0, s>>>(b, rows, B); break;
   }
   count_launches(1);
+  return map_cuda(cudaGetLastError());
 }
 
-bool fast_ok(const wcomp_container* c, const uint16_t* x) {
-  return c->L.K % kGroup == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-         (reinterpret_cast<uintptr_t>(c->d_main) & 31) == 0;
-}
+// One tensor of a launch request.
+struct Item {
+  TensorDesc d;
+  const uint16_t* x;
+  float* y;
+  int kind;  // Src for the vector path, 3 + Src for the element path
+};
 
-int launch_gemv(const wcomp_container* const* cs, const uint16_t* const* xs, int B, float* const* ys, int count,
-                cudaStream_t s) {
-  if (B < 1 || B > 16) return WCOMP_EINVAL;
-  for (int i = 0; i < count; ++i) {
-    if (!cs[i] || !xs[i] || !ys[i]) return WCOMP_EINVAL;
-    if (cs[i]->L.N >= (int64_t(1) << 31)) return WCOMP_EUNSUPPORTED;
-  }
+int run_items(Item* items, int count, int B, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   const int sms = sm_count(dev);
-  // Three kinds of launches: vector path per scheme, element path for the rest.
-  for (int kind = 0; kind < 3; ++kind) {
-    GemvBatch b;
-    memset(&b, 0, sizeof(b));
+  // longest rows first: the tail of the dynamic schedule is made of short units
+  std::stable_sort(items, items + count, [](const Item& a, const Item& b) { return a.d.K > b.d.K; });
+  for (int kind = 0; kind < 6; ++kind) {
+    GemvBatch bt;
+    memset(&bt, 0, sizeof(bt));
     int64_t Ns[kMaxBatch];
-    auto flush = [&]() {
-      if (!b.count) return;
-      if (kind == 0) dispatch_fused<WCOMP_BYTESPLIT>(b, Ns, B, sms, s);
-      else if (kind == 1) dispatch_fused<WCOMP_K15>(b, Ns, B, sms, s);
-      else dispatch_generic(b, Ns, B, sms, s);
-      memset(&b, 0, sizeof(b));
+    auto flush = [&]() -> int {
+      if (!bt.count) return WCOMP_OK;
+      int st;
+      switch (kind) {
+        case 0: st = dispatch_vec<kBytesplit>(bt, Ns, B, dev, sms, s); break;
+        case 1: st = dispatch_vec<kK15>(bt, Ns, B, dev, sms, s); break;
+        case 2: st = dispatch_vec<kPlain>(bt, Ns, B, dev, sms, s); break;
+        case 3: st = dispatch_generic<kBytesplit>(bt, Ns, B, sms, s); break;
+        case 4: st = dispatch_generic<kK15>(bt, Ns, B, sms, s); break;
+        default: st = dispatch_generic<kPlain>(bt, Ns, B, sms, s); break;
+      }
+      memset(&bt, 0, sizeof(bt));
+      return st;
     };
     for (int i = 0; i < count; ++i) {
-      const wcomp_container* c = cs[i];
-      const bool fast = fast_ok(c, xs[i]);
-      const int k = fast ? c->L.scheme : 2;
-      if (k != kind) continue;
-      b.d[b.count] = make_desc(c);
-      b.x[b.count] = xs[i];
-      b.y[b.count] = ys[i];
-      Ns[b.count] = c->L.N;
-      if (++b.count == kMaxBatch) flush();
+      if (items[i].kind != kind) continue;
+      bt.d[bt.count] = items[i].d;
+      bt.x[bt.count] = items[i].x;
+      bt.y[bt.count] = items[i].y;
+      Ns[bt.count] = items[i].d.N;
+      if (++bt.count == kMaxBatch) {
+        const int st = flush();
+        if (st != WCOMP_OK) return st;
+      }
     }
-    flush();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return map_cuda(e);
+    const int st = flush();
+    if (st != WCOMP_OK) return st;
   }
   return WCOMP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; }
+
+int gemv_containers(const wcomp_container* const* cs, const uint16_t* const* xs, int B, float* const* ys, int count,
+                    cudaStream_t s) {
+  if (B < 1 || B > 16) return WCOMP_EINVAL;
+  std::vector<Item> items(count);
+  for (int i = 0; i < count; ++i) {
+    if (!cs[i] || !xs[i] || !ys[i]) return WCOMP_EINVAL;
+    if (cs[i]->L.N >= (int64_t(1) << 31)) return WCOMP_EUNSUPPORTED;
+    items[i].d = make_desc(cs[i]);
+    items[i].x = xs[i];
+    items[i].y = ys[i];
+    const bool vec = cs[i]->L.K % kGroup == 0 && aligned16(xs[i]) && aligned32(cs[i]->d_main);
+    items[i].kind = (vec ? 0 : 3) + cs[i]->L.scheme;
+  }
+  return run_items(items.data(), count, B, s);
+}
+
+int gemv_plain(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks, const uint16_t* const* xs, int B,
+               float* const* ys, int count, cudaStream_t s) {
+  if (B < 1 || B > 16) return WCOMP_EINVAL;
+  std::vector<Item> items(count);
+  for (int i = 0; i < count; ++i) {
+    if (!ws[i] || !xs[i] || !ys[i] || Ns[i] <= 0 || Ks[i] <= 0) return WCOMP_EINVAL;
+    if (Ns[i] >= (int64_t(1) << 31)) return WCOMP_EUNSUPPORTED;
+    TensorDesc d{};
+    d.raw = reinterpret_cast<const uint8_t*>(ws[i]);
+    d.N = Ns[i];
+    d.K = Ks[i];
+    d.n = uint64_t(Ns[i]) * uint64_t(Ks[i]);
+    d.scheme = kPlain;
+    items[i].d = d;
+    items[i].x = xs[i];
+    items[i].y = ys[i];
+    const bool vec = Ks[i] % kGroup == 0 && aligned16(xs[i]) && aligned32(ws[i]);
+    items[i].kind = vec ? kPlain : 3 + kPlain;
+  }
+  return run_items(items.data(), count, B, s);
 }
 
 }  // namespace
@@ -406,48 +530,23 @@ using namespace wc;
 
 extern "C" int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream) {
   if (!c || !d_x || !d_y) return WCOMP_EINVAL;
-  return launch_gemv(&c, &d_x, B, &d_y, 1, static_cast<cudaStream_t>(stream));
+  return gemv_containers(&c, &d_x, B, &d_y, 1, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int wcomp_gemv_batched(const wcomp_container* const* containers, const uint16_t* const* d_x, int B,
                                   float* const* d_y, int count, void* stream) {
   if (!containers || !d_x || !d_y || count <= 0) return WCOMP_EINVAL;
-  return launch_gemv(containers, d_x, B, d_y, count, static_cast<cudaStream_t>(stream));
+  return gemv_containers(containers, d_x, B, d_y, count, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int wcomp_gemv_bf16(const uint16_t* d_w, int64_t N, int64_t K, const uint16_t* d_x, int B, float* d_y,
                                void* stream) {
-  if (!d_w || !d_x || !d_y || N <= 0 || K <= 0 || B < 1 || B > 16) return WCOMP_EINVAL;
-  if (N >= (int64_t(1) << 31)) return WCOMP_EUNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int sms = sm_count(dev);
-  PlainArgs a{d_w, d_x, d_y, N, K};
-  const bool fast = K % kGroup == 0 && (reinterpret_cast<uintptr_t>(d_w) & 31) == 0 &&
-                    (reinterpret_cast<uintptr_t>(d_x) & 15) == 0;
-  const int BT = pow2_batch(B);
-  if (fast) {
-    const int R = BT >= 16 ? 1 : 2;
-    const uint32_t sets = uint32_t(cdiv(uint64_t(N), R));
-    const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(sets, kWarps), uint64_t(sms) * 8));
-    switch (BT) {
-      case 1: gemv_bf16_kernel<1, 2><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 2: gemv_bf16_kernel<2, 2><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 4: gemv_bf16_kernel<4, 2><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 8: gemv_bf16_kernel<8, 2><<<blocks, kThreads, 0, s>>>(a, B); break;
-      default: gemv_bf16_kernel<16, 1><<<blocks, kThreads, 0, s>>>(a, B); break;
-    }
-  } else {
-    const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(uint64_t(N), kWarps), uint64_t(sms) * 8));
-    switch (BT) {
-      case 1: gemv_bf16_generic_kernel<1><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 2: gemv_bf16_generic_kernel<2><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 4: gemv_bf16_generic_kernel<4><<<blocks, kThreads, 0, s>>>(a, B); break;
-      case 8: gemv_bf16_generic_kernel<8><<<blocks, kThreads, 0, s>>>(a, B); break;
-      default: gemv_bf16_generic_kernel<16><<<blocks, kThreads, 0, s>>>(a, B); break;
-    }
-  }
-  count_launches(1);
-  return map_cuda(cudaGetLastError());
+  if (!d_w || !d_x || !d_y || N <= 0 || K <= 0) return WCOMP_EINVAL;
+  return gemv_plain(&d_w, &N, &K, &d_x, B, &d_y, 1, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int wcomp_gemv_bf16_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,
+                                       const uint16_t* const* d_x, int B, float* const* d_y, int count, void* stream) {
+  if (!d_w || !N || !K || !d_x || !d_y || count <= 0) return WCOMP_EINVAL;
+  return gemv_plain(d_w, N, K, d_x, B, d_y, count, static_cast<cudaStream_t>(stream));
 }

@@ -67,6 +67,9 @@ def lib():
     L.wcomp_decode.argtypes = [P, P, P]
     L.wcomp_gemv.argtypes = [P, P, ctypes.c_int, P, P]
     L.wcomp_gemv_bf16.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int, P, P]
+    L.wcomp_gemv_bf16_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(P), ctypes.c_int,
+                                          ctypes.POINTER(P), ctypes.c_int, P]
     L.wcomp_decode_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P), ctypes.c_int, P]
     L.wcomp_gemv_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(P), ctypes.c_int, ctypes.POINTER(P),
                                      ctypes.c_int, P]
@@ -80,7 +83,8 @@ def lib():
     L.wcomp_version.argtypes = []
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
-    for name in ("wcomp_encode", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_decode_batched",
+    for name in ("wcomp_encode", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
+                 "wcomp_decode_batched",
                  "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_version"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -215,6 +219,30 @@ def gemv_bf16(w: torch.Tensor, x: torch.Tensor, y: Optional[torch.Tensor] = None
     _check(lib().wcomp_gemv_bf16(P(w.data_ptr()), N, K, P(x.data_ptr()), B, P(y.data_ptr()), P(_stream(stream))),
            "wcomp_gemv_bf16")
     return y
+
+
+def gemv_bf16_batched(ws: Sequence[torch.Tensor], xs: Sequence[torch.Tensor],
+                      ys: Optional[List[torch.Tensor]] = None, stream=None):
+    """Plain BF16 GEMV over several weight tensors in one launch."""
+    B = xs[0].shape[0] if xs[0].dim() == 2 else 1
+    Ns, Ks = [], []
+    for w, x in zip(ws, xs):
+        _bits16(w, "w")
+        _bits16(x, "x")
+        N, K = (w.shape[0], w.shape[1]) if w.dim() == 2 else (1, w.numel())
+        if x.numel() != B * K:
+            raise ValueError("x has the wrong size")
+        Ns.append(N)
+        Ks.append(K)
+    if ys is None:
+        ys = [torch.empty((B, N), dtype=torch.float32, device="cuda") for N in Ns]
+    n_arr = (ctypes.c_int64 * len(ws))(*Ns)
+    k_arr = (ctypes.c_int64 * len(ws))(*Ks)
+    _check(lib().wcomp_gemv_bf16_batched(_ptr_array([w.data_ptr() for w in ws]), n_arr, k_arr,
+                                         _ptr_array([x.data_ptr() for x in xs]), B,
+                                         _ptr_array([y.data_ptr() for y in ys]), len(ws), P(_stream(stream))),
+           "wcomp_gemv_bf16_batched")
+    return ys
 
 
 def _ptr_array(ptrs: Sequence[int]):

@@ -139,6 +139,16 @@ WCOMP_API int wcomp_gemv_bf16(const uint16_t* d_w, int64_t N, int64_t K, const u
                     float* d_y, void* stream);
 
 /*
+ * Batched plain BF16 GEMV: tensor i is W_i[N[i], K[i]] at d_w[i] with input
+ * d_x[i] (B x K[i]) and output d_y[i] (B x N[i]); host arrays of length count.
+ * The same launch structure as wcomp_gemv_batched, so the two compare like
+ * for like.
+ */
+WCOMP_API int wcomp_gemv_bf16_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,
+                                      const uint16_t* const* d_x, int B, float* const* d_y, int count,
+                                      void* stream);
+
+/*
  * Batched forms: one launch over `count` containers (any mix of schemes and
  * shapes).  Arrays are host arrays of length count; every d_outs[i] /
  * d_x[i] / d_y[i] is a device buffer sized for containers[i].  All

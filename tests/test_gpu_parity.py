@@ -162,6 +162,17 @@ def test_plain_bf16_gemv(W, B):
     check_gemv(W.gemv_bf16(dev(w2), dev(x2)), O.gemv(w2, x2))
 
 
+def test_plain_batched(W):
+    shapes = [(64, 1024), (33, 1000), (200, 2048), (5, 4096)]
+    ws = [synth.gen_weights_np(synth.WeightSpec(f"q{i}", N, K, "normal", 0.02, seed=800 + i))
+          for i, (N, K) in enumerate(shapes)]
+    for B in (1, 4, 16):
+        xs = [synth.gen_x_np(B, K, 900 + i) for i, (_, K) in enumerate(shapes)]
+        ys = W.gemv_bf16_batched([dev(w) for w in ws], [dev(x) for x in xs])
+        for w, x, y in zip(ws, xs, ys):
+            check_gemv(y, O.gemv(w, x))
+
+
 def test_batched_matches_single(W):
     specs = [synth.WeightSpec(f"b{i}", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=400 + i)
              for i, (N, K) in enumerate([(64, 1024), (200, 640), (33, 1000), (128, 2048), (1, 4096)])]
