@@ -293,10 +293,8 @@ class HotPath:
         for c in self.containers:
             c.free(self.stream)
         t0 = mark() if ev is not None else None
-        cs = []
-        for w in self.weights:
-            for scheme in (0, 1):
-                cs.append(W.encode(w, scheme, stream=self.stream))
+        cs = W.encode_batched([w for w in self.weights for _ in (0, 1)], [0, 1] * len(self.weights),
+                              stream=self.stream)
         self.containers = cs
         t1 = mark() if ev is not None else None
         W.decode_batched(cs, self.outs, stream=self.stream)
@@ -341,32 +339,39 @@ class HotPath:
         return d
 
 
-def time_scheme_split(hp, W, torch, B: int, reps: int = 5) -> dict:
-    """Fused GEMV time per scheme (all 7 tensors in one batched launch) and plain GEMV, median of reps."""
+def time_launches(fn, stream, reps: int = 10) -> float:
+    """Average device time (ms) of one call of fn, over reps back-to-back calls.
+
+    One untimed call first keeps the GPU busy while the timed calls are
+    enqueued, so host launch latency does not enter the measurement."""
+    import torch
+
+    fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def time_kernels(hp, W, torch) -> dict:
+    """Per-launch device time of each kernel kind of the step (ms)."""
     res = {}
-    by = {0: [c for c in hp.containers if c.scheme == 0], 1: [c for c in hp.containers if c.scheme == 1]}
-    ys = {s: [torch.empty((B, c.N), dtype=torch.float32, device="cuda") for c in by[s]] for s in by}
+    by = {s: [c for c in hp.containers if c.scheme == s] for s in (0, 1)}
+    outs = {s: [o for o, c in zip(hp.outs, hp.containers) if c.scheme == s] for s in (0, 1)}
     for s in (0, 1):
-        ts = []
-        for _ in range(reps + 1):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(hp.stream)
-            W.gemv_batched(by[s], hp.xs[B], ys[s], stream=hp.stream)
-            b.record(hp.stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b))
-        res[SCHEME_NAMES[s]] = statistics.median(ts[1:])
-    ts = []
-    for _ in range(reps + 1):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(hp.stream)
-        W.gemv_bf16_batched(hp.weights, hp.xs[B], hp.yp[B], stream=hp.stream)
-        b.record(hp.stream)
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
-    res["plain"] = statistics.median(ts[1:])
+        nm = SCHEME_NAMES[s]
+        res[f"decode_{nm}"] = time_launches(lambda: W.decode_batched(by[s], outs[s], stream=hp.stream), hp.stream)
+        for B in BATCHES:
+            ys = [torch.empty((B, c.N), dtype=torch.float32, device="cuda") for c in by[s]]
+            res[f"gemv_fused_{nm}_b{B}"] = time_launches(
+                lambda: W.gemv_batched(by[s], hp.xs[B], ys, stream=hp.stream), hp.stream)
+    for B in BATCHES:
+        res[f"gemv_plain_b{B}"] = time_launches(
+            lambda: W.gemv_bf16_batched(hp.weights, hp.xs[B], hp.yp[B], stream=hp.stream), hp.stream)
     return res
 
 
@@ -433,23 +438,31 @@ def run_ours(args):
         gbs = bytes_[k] / (ms / 1e3) / 1e9
         rows[k] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                    "frac_of_8TBps": round(gbs / 8000.0, 4), "bytes": bytes_[k]}
-    # fused vs plain, per scheme, at each batch
+    # per-launch kernel times (back-to-back launches, device clock)
+    kt = time_kernels(hp, W, torch)
+    kbytes = {}
+    for s_ in (0, 1):
+        nm = SCHEME_NAMES[s_]
+        infos = [i for i in hp.infos if i["scheme"] == s_]
+        kbytes[f"decode_{nm}"] = sum(decode_bytes(i) for i in infos)
+        for B in BATCHES:
+            kbytes[f"gemv_fused_{nm}_b{B}"] = sum(gemv_bytes(i, B) for i in infos)
+    for B in BATCHES:
+        kbytes[f"gemv_plain_b{B}"] = sum(plain_bytes(sp.N, sp.K, B) for sp in specs)
+    kernels = {k: {"ms": round(v, 4), "GB/s": round(kbytes[k] / (v / 1e3) / 1e9, 1),
+                   "frac_of_peak": round(kbytes[k] / (v / 1e3) / 1e9 / peak, 4), "bytes": kbytes[k]}
+               for k, v in kt.items()}
     ratio = {}
     for B in BATCHES:
-        t = time_scheme_split(hp, W, torch, B)
-        ratio[f"b{B}"] = {"fused_ms": {k: round(v, 4) for k, v in t.items() if k != "plain"},
-                          "plain_ms": round(t["plain"], 4),
-                          "fused_over_plain": {k: round(v / t["plain"], 4) for k, v in t.items() if k != "plain"}}
-        for s in (0, 1):
-            nm = SCHEME_NAMES[s]
-            gb = hp.per_scheme_bytes(B)[s] / (t[nm] / 1e3) / 1e9
-            ratio[f"b{B}"].setdefault("fused_GB/s", {})[nm] = round(gb, 1)
-    # dominant kernel among the row kinds = largest share of the step
-    dom = max(phase_ms, key=lambda k: phase_ms[k])
-    dom_gbs = bytes_[dom] / (phase_ms[dom] / 1e3) / 1e9
+        ratio[f"b{B}"] = {SCHEME_NAMES[s_]: round(kt[f"gemv_fused_{SCHEME_NAMES[s_]}_b{B}"] / kt[f"gemv_plain_b{B}"], 4)
+                          for s_ in (0, 1)}
+    # dominant kernel: largest share of the step among the kernels timed above
+    per_step = {k: v for k, v in kt.items()}
+    dom = max(per_step, key=lambda k: per_step[k])
+    dom_gbs = kbytes[dom] / (kt[dom] / 1e3) / 1e9
     traffic = load_traffic(dom)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(dom_gbs / peak, 4), "peak_source": peaks["source"],
+                "frac": round(dom_gbs / peak, 4), "peak_source": peaks["source"] + " (hbm_gbs, copy)",
                 "traffic": traffic}
 
     result = {
@@ -463,7 +476,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (386 MB BF16, ~580 MB containers), swept in order",
                    "parallelism": f"replicas x{world}"},
         "rows": rows,
-        "fused_vs_plain": ratio,
+        "kernels": kernels,
+        "fused_over_plain_time": ratio,
         "escape_rate": {SCHEME_NAMES[s]: round(sum(i["n_escapes"] for i in hp.infos if i["scheme"] == s) /
                                                sum(i["n"] for i in hp.infos if i["scheme"] == s), 6) for s in (0, 1)},
         "bpw": {SCHEME_NAMES[s]: {"entropy": round(sum(i["entropy_bpw"] * i["n"] for i in hp.infos if i["scheme"] == s) /

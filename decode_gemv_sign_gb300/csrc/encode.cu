@@ -1,14 +1,20 @@
 // Encoder: histogram -> top-15 table -> pack codes and raw bits -> tile scan
-// -> escape compaction -> row index.  All steps run on the GPU; the host reads
-// back the escape count once to size the escape stream.
+// -> escape compaction -> row index, for one tensor or a batch of tensors.
+// All steps run on the GPU; the host reads back the escape counts once per
+// batch to size the escape streams.
 //
 // Method: forgeeks page "Prueba de GLM-5.2 reduce la memoria BF16 en casi un
 // 25%", section "Cómo funciona la compresión" (frequent sign+exponent symbols
 // get 4-bit codes into a 15-entry table, rare symbols go to an exact escape
 // stream, the low byte / 7-bit mantissa is stored unchanged).
+//
+// Every kernel takes the whole batch as a parameter-space descriptor array
+// and finds its tensor from a prefix over blocks, tiles or rows, so a batch
+// costs about a dozen launches and one host synchronization.
 #include <string.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "wcomp_impl.cuh"
 
@@ -17,53 +23,112 @@ namespace {
 
 constexpr int kThreads = 256;  // pack / compact: one 8192-element tile per CTA
 
+struct Summary {
+  uint32_t E;
+  uint16_t table[16];
+  uint32_t pad[3];
+};
+
+struct EncDesc {
+  const uint16_t* w;
+  uint8_t* main;
+  uint8_t* esc;
+  Summary* summary;
+  uint64_t n;
+  int64_t N, K;
+  uint64_t E;
+  uint64_t off_codes, off_raw, off_a, off_b, off_c, off_tile, off_row, off_scratch, off_pos, off_val;
+  uint32_t n_tiles;
+  int scheme;
+  int aligned;
+};
+
+struct EncBatch {
+  EncDesc d[kMaxBatch];
+  uint32_t prefix[kMaxBatch + 1];  // blocks, tiles or rows, per launch
+  int count;
+};
+
+constexpr int kMaxZero = 8 * kMaxBatch;
+struct ZeroList {
+  uint8_t* p[kMaxZero];
+  uint32_t len[kMaxZero];
+  int count;
+};
+
+__device__ __forceinline__ int find_owner(const EncBatch& b, uint32_t x) {
+  int i = 0;
+  while (i + 1 < b.count && b.prefix[i + 1] <= x) ++i;
+  return i;
+}
+
+// Zero small byte ranges (section padding, histogram scratch); one CTA per range.
+__global__ void __launch_bounds__(256) zero_kernel(const __grid_constant__ ZeroList z) {
+  const int r = blockIdx.x;
+  if (r >= z.count) return;
+  uint8_t* p = z.p[r];
+  for (uint32_t i = threadIdx.x; i < z.len[r]; i += blockDim.x) p[i] = 0;
+}
+
 // ---------------------------------------------------------------------------
-// a1: per-tensor histogram.  Each lane owns a column of a [bins][32] counter
-// array in shared memory, so the 32 lanes of a warp never hit the same bank;
-// different warps meet only through shared-memory atomics.
+// a1: per-tensor histogram.  Counters live in shared memory as [bins][16]
+// words; lane l owns the low half of column l (l < 16) or the high half of
+// column l - 16, so the lanes of a warp touch 16 distinct banks and two lanes
+// share a word only as its two halves.  The host sizes the grid so that no
+// 16-bit half can exceed 65535 (at most 8191 elements per thread).
 // ---------------------------------------------------------------------------
 template <int SHIFT, int NB>
-__global__ void __launch_bounds__(256) hist_kernel(const uint16_t* __restrict__ w, uint64_t n, int aligned,
-                                                   uint32_t* __restrict__ hist) {
-  extern __shared__ uint32_t h[];  // [NB][32]
-  for (int i = threadIdx.x; i < NB * 32; i += blockDim.x) h[i] = 0;
+__global__ void __launch_bounds__(256) hist_kernel(const __grid_constant__ EncBatch bt) {
+  __shared__ uint32_t h[NB * 16];
+  for (int i = threadIdx.x; i < NB * 16; i += blockDim.x) h[i] = 0;
   __syncthreads();
+  const int t = find_owner(bt, blockIdx.x);
+  const EncDesc& d = bt.d[t];
+  const uint32_t blk = blockIdx.x - bt.prefix[t], nblk = bt.prefix[t + 1] - bt.prefix[t];
   const int lane = threadIdx.x & 31;
-  const uint64_t chunks = cdiv(n, 8);
-  for (uint64_t ch = blockIdx.x * uint64_t(blockDim.x) + threadIdx.x; ch < chunks;
-       ch += uint64_t(gridDim.x) * blockDim.x) {
+  const uint32_t col = lane & 15, inc = lane < 16 ? 1u : 65536u;
+  const uint64_t chunks = cdiv(d.n, 8);
+  for (uint64_t ch = uint64_t(blk) * blockDim.x + threadIdx.x; ch < chunks; ch += uint64_t(nblk) * blockDim.x) {
     const uint64_t base = ch * 8;
-    if (aligned && base + 8 <= n) {
-      uint4 v = ld_stream_v4(w + base);
-      uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    if (d.aligned && base + 8 <= d.n) {
+      const uint4 v = ld_stream_v4(d.w + base);
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        atomicAdd(&h[((wd[j] & 0xFFFF) >> SHIFT) * 32 + lane], 1u);
-        atomicAdd(&h[(wd[j] >> (16 + SHIFT)) * 32 + lane], 1u);
+        atomicAdd(&h[((wd[j] & 0xFFFF) >> SHIFT) * 16 + col], inc);
+        atomicAdd(&h[(wd[j] >> (16 + SHIFT)) * 16 + col], inc);
       }
     } else {
-      for (uint64_t i = base; i < n && i < base + 8; ++i) atomicAdd(&h[(uint32_t(w[i]) >> SHIFT) * 32 + lane], 1u);
+      for (uint64_t i = base; i < d.n && i < base + 8; ++i)
+        atomicAdd(&h[(uint32_t(d.w[i]) >> SHIFT) * 16 + col], inc);
     }
   }
   __syncthreads();
+  uint32_t* hist = reinterpret_cast<uint32_t*>(d.main + d.off_scratch + Scratch::hist);
   for (int b = threadIdx.x; b < NB; b += blockDim.x) {
     uint32_t s = 0;
-    for (int l = 0; l < 32; ++l) s += h[b * 32 + ((l + b) & 31)];
+    for (int l = 0; l < 16; ++l) {
+      const uint32_t v = h[b * 16 + ((l + b) & 15)];
+      s += (v & 0xFFFF) + (v >> 16);
+    }
     if (s) atomicAdd(&hist[b], s);
   }
 }
 
 // ---------------------------------------------------------------------------
 // a2: table of the 15 most frequent symbols, ordered by (count desc, symbol
-// asc), and the inverse map symbol -> code (15 = escape).  One CTA: every bin
-// computes its rank by comparing against all bins.
+// asc), and the inverse map symbol -> code (15 = escape).  One CTA per tensor:
+// every bin computes its rank by comparing against all bins.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(512) select_kernel(const uint32_t* __restrict__ hist, int nb,
-                                                     uint8_t* __restrict__ lut, uint16_t* __restrict__ table16) {
+__global__ void __launch_bounds__(512) select_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t cnt[kMaxBins];
+  const EncDesc& d = bt.d[blockIdx.x];
+  const int nb = d.scheme == WCOMP_BYTESPLIT ? 256 : 512;
+  const uint32_t* hist = reinterpret_cast<const uint32_t*>(d.main + d.off_scratch + Scratch::hist);
+  uint8_t* lut = d.main + d.off_scratch + Scratch::lut;
   const int i = threadIdx.x;
   if (i < nb) cnt[i] = hist[i];
-  if (i < 16) table16[i] = 0;
+  if (i < 16) d.summary->table[i] = 0;
   __syncthreads();
   if (i < nb) {
     const uint32_t ci = cnt[i];
@@ -73,7 +138,7 @@ __global__ void __launch_bounds__(512) select_kernel(const uint32_t* __restrict_
       rank += (cj > ci) || (cj == ci && j < i);
     }
     lut[i] = rank < kTableSize ? uint8_t(rank) : uint8_t(kEscape);
-    if (rank < kTableSize) table16[rank] = uint16_t(i);
+    if (rank < kTableSize) d.summary->table[rank] = uint16_t(i);
   }
 }
 
@@ -88,61 +153,57 @@ __device__ __forceinline__ uint32_t block_sum_256(uint32_t v, uint32_t* sm) {
   return t;  // valid in thread 0
 }
 
-// Exclusive prefix of v over the 256 threads of the block (and the block total).
-__device__ __forceinline__ uint32_t block_exclusive_256(uint32_t v, uint32_t* sm, uint32_t& total) {
+// Exclusive prefix of v over the 256 threads of the block.
+__device__ __forceinline__ uint32_t block_exclusive_256(uint32_t v, uint32_t* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
     if (lane >= o) inc += u;
   }
   if (lane == 31) sm[warp] = inc;
   __syncthreads();
   uint32_t before = 0;
-  total = 0;
-  for (int k = 0; k < kThreads / 32; ++k) {
-    const uint32_t s = sm[k];
-    if (k < warp) before += s;
-    total += s;
-  }
+  for (int k = 0; k < warp; ++k) before += sm[k];
   return before + inc - v;
 }
 
 // ---------------------------------------------------------------------------
-// a3: pack.  Thread j of tile t handles group g = 256 t + j (32 elements).
-// Writes the 16 code bytes, the raw bytes (byte-split) or the three mantissa
-// planes (K15), and the tile's escape count.
+// a3: pack.  Thread j of a tile handles group 256 t + j (32 elements): the 16
+// code bytes, the raw bytes (byte-split) or the three mantissa planes (K15),
+// and the tile's escape count.
 // ---------------------------------------------------------------------------
 template <int SCHEME>
-__global__ void __launch_bounds__(kThreads) pack_kernel(const uint16_t* __restrict__ w, uint64_t n, int aligned,
-                                                        const uint8_t* __restrict__ lut_g, uint8_t* __restrict__ codes,
-                                                        uint8_t* __restrict__ raw, uint8_t* __restrict__ pa,
-                                                        uint8_t* __restrict__ pb, uint8_t* __restrict__ pc,
-                                                        uint32_t* __restrict__ tile_counts) {
+__global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint8_t lut[kMaxBins];
   __shared__ uint32_t red[kThreads / 32];
   constexpr int NB = SCHEME == WCOMP_BYTESPLIT ? 256 : 512;
   constexpr int SHIFT = SCHEME == WCOMP_BYTESPLIT ? 8 : 7;
+  const int ti = find_owner(bt, blockIdx.x);
+  const EncDesc& d = bt.d[ti];
+  const uint32_t tile = blockIdx.x - bt.prefix[ti];
+  const uint8_t* lut_g = d.main + d.off_scratch + Scratch::lut;
   for (int i = threadIdx.x; i < NB; i += blockDim.x) lut[i] = lut_g[i];
   __syncthreads();
+  const uint64_t n = d.n;
   const uint64_t G = cdiv(n, kGroup);
-  const uint64_t g = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
+  const uint64_t g = uint64_t(tile) * kThreads + threadIdx.x;
   uint32_t esc = 0;
   if (g < G) {
     const uint64_t base = g * kGroup;
     uint32_t wv[16];
-    if (aligned && base + kGroup <= n) {
+    if (d.aligned && base + kGroup <= n) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint4 v = ld_stream_v4(w + base + 8 * k);
+        const uint4 v = ld_stream_v4(d.w + base + 8 * k);
         wv[4 * k + 0] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
       }
     } else {
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const uint64_t i0 = base + 2 * k;
-        uint32_t lo = i0 < n ? w[i0] : 0u, hi = i0 + 1 < n ? w[i0 + 1] : 0u;
+        const uint32_t lo = i0 < n ? d.w[i0] : 0u, hi = i0 + 1 < n ? d.w[i0 + 1] : 0u;
         wv[k] = lo | (hi << 16);
       }
     }
@@ -167,26 +228,31 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const uint16_t* __restri
         c |= ((m >> 6) & 0x1) << (8 * ln + q);
       }
     }
-    *reinterpret_cast<uint4*>(codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    uint8_t* m = d.main;
+    *reinterpret_cast<uint4*>(m + d.off_codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     if (SCHEME == WCOMP_BYTESPLIT) {
-      *reinterpret_cast<uint4*>(raw + 32 * g) = make_uint4(r[0], r[1], r[2], r[3]);
-      if (base + 16 < n) *reinterpret_cast<uint4*>(raw + 32 * g + 16) = make_uint4(r[4], r[5], r[6], r[7]);
+      *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(r[0], r[1], r[2], r[3]);
+      if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(r[4], r[5], r[6], r[7]);
     } else {
-      *reinterpret_cast<uint4*>(pa + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
-      *reinterpret_cast<uint2*>(pb + 8 * g) = make_uint2(b[0], b[1]);
-      *reinterpret_cast<uint32_t*>(pc + 4 * g) = c;
+      *reinterpret_cast<uint4*>(m + d.off_a + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<uint2*>(m + d.off_b + 8 * g) = make_uint2(b[0], b[1]);
+      *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;
     }
   }
   const uint32_t total = block_sum_256(esc, red);
-  if (threadIdx.x == 0) tile_counts[blockIdx.x] = total;
+  if (threadIdx.x == 0) reinterpret_cast<uint32_t*>(d.main + d.off_tile)[tile] = total;
 }
 
 // ---------------------------------------------------------------------------
 // Exclusive scan of the per-tile escape counts, in place; entry n_tiles
-// receives E.  One CTA, two passes, no inter-block waits.
+// receives E (also written to the tensor's summary).  One CTA per tensor, two
+// passes, no inter-block waits.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) scan_kernel(uint32_t* __restrict__ idx, uint32_t n_tiles) {
+__global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t part[1024];
+  const EncDesc& d = bt.d[blockIdx.x];
+  uint32_t* idx = reinterpret_cast<uint32_t*>(d.main + d.off_tile);
+  const uint32_t n_tiles = d.n_tiles;
   const uint32_t per = uint32_t(cdiv(n_tiles, 1024));
   const uint32_t lo = threadIdx.x * per;
   const uint32_t hi = min(lo + per, n_tiles);
@@ -195,7 +261,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(uint32_t* __restrict__ idx, 
   part[threadIdx.x] = s;
   __syncthreads();
   for (int o = 1; o < 1024; o <<= 1) {
-    uint32_t v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0u;
+    const uint32_t v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0u;
     __syncthreads();
     part[threadIdx.x] += v;
     __syncthreads();
@@ -206,26 +272,29 @@ __global__ void __launch_bounds__(1024) scan_kernel(uint32_t* __restrict__ idx, 
     idx[i] = run;
     run += v;
   }
-  if (threadIdx.x == 1023) idx[n_tiles] = part[1023];
+  if (threadIdx.x == 1023) {
+    idx[n_tiles] = part[1023];
+    d.summary->E = part[1023];
+  }
 }
 
 // ---------------------------------------------------------------------------
-// a4: escape compaction.  Thread j of tile t re-reads the 32 codes of group
-// 256 t + j, ranks its escapes inside the tile with a block scan and writes
+// a4: escape compaction.  Thread j of a tile re-reads the 32 codes of its
+// group, ranks its escapes inside the tile with a block scan and writes
 // (position, value) pairs in ascending position order.
 // ---------------------------------------------------------------------------
 template <int SCHEME>
-__global__ void __launch_bounds__(kThreads) compact_kernel(const uint16_t* __restrict__ w, uint64_t n,
-                                                           const uint8_t* __restrict__ codes,
-                                                           const uint32_t* __restrict__ tile_index,
-                                                           uint32_t* __restrict__ pos, uint8_t* __restrict__ val) {
+__global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t sm[kThreads / 32];
-  const uint32_t t = blockIdx.x;
+  const int ti = find_owner(bt, blockIdx.x);
+  const EncDesc& d = bt.d[ti];
+  const uint32_t t = blockIdx.x - bt.prefix[ti];
+  const uint32_t* tile_index = reinterpret_cast<const uint32_t*>(d.main + d.off_tile);
   if (tile_index[t + 1] == tile_index[t]) return;  // uniform: no escapes in this tile
-  const uint64_t G = cdiv(n, kGroup);
+  const uint64_t G = cdiv(d.n, kGroup);
   const uint64_t g = uint64_t(t) * kThreads + threadIdx.x;
   uint4 c4 = make_uint4(0, 0, 0, 0);
-  if (g < G) c4 = *reinterpret_cast<const uint4*>(codes + 16 * g);
+  if (g < G) c4 = *reinterpret_cast<const uint4*>(d.main + d.off_codes + 16 * g);
   const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
   uint32_t cnt = 0;
 #pragma unroll
@@ -233,14 +302,15 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const uint16_t* __res
     const uint32_t x = cw[i] & (cw[i] >> 1) & (cw[i] >> 2) & (cw[i] >> 3) & 0x11111111u;
     cnt += __popc(x);
   }
-  uint32_t total;
-  uint32_t o = tile_index[t] + block_exclusive_256(cnt, sm, total);
+  uint32_t o = tile_index[t] + block_exclusive_256(cnt, sm);
   if (!cnt) return;
+  uint32_t* pos = reinterpret_cast<uint32_t*>(d.esc + d.off_pos);
+  uint8_t* val = d.esc + d.off_val;
   const uint64_t base = g * kGroup;
   for (int e = 0; e < kGroup; ++e) {
     if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape) {
       const uint32_t p = uint32_t(base + e);
-      const uint32_t v = w[p];
+      const uint32_t v = d.w[p];
       pos[o] = p;
       if (SCHEME == WCOMP_BYTESPLIT)
         val[o] = uint8_t(v >> 8);
@@ -251,24 +321,231 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const uint16_t* __res
   }
 }
 
-// Row index: entry r = number of escapes below r * K (lower bound search).
-__global__ void row_index_kernel(const uint32_t* __restrict__ pos, uint64_t E, int64_t N, int64_t K,
-                                 uint32_t* __restrict__ row_index) {
-  const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (r > N) return;
-  const uint64_t bound = uint64_t(r) * uint64_t(K);
-  uint64_t lo = 0, hi = E;
+// Row index: entry r = number of escapes below r * K (lower-bound search).
+__global__ void __launch_bounds__(256) row_index_kernel(const __grid_constant__ EncBatch bt) {
+  const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= bt.prefix[bt.count]) return;
+  const int ti = find_owner(bt, x);
+  const EncDesc& d = bt.d[ti];
+  const int64_t r = int64_t(x - bt.prefix[ti]);
+  const uint64_t bound = uint64_t(r) * uint64_t(d.K);
+  const uint32_t* pos = reinterpret_cast<const uint32_t*>(d.esc + d.off_pos);
+  uint64_t lo = 0, hi = d.E;
   while (lo < hi) {
     const uint64_t mid = (lo + hi) >> 1;
     if (pos[mid] < bound) lo = mid + 1; else hi = mid;
   }
-  row_index[r] = uint32_t(lo);
+  reinterpret_cast<uint32_t*>(d.main + d.off_row)[r] = uint32_t(lo);
 }
 
-cudaError_t zero_pad(uint8_t* base, uint64_t off, uint64_t sz, cudaStream_t s) {
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+struct Job {
+  wcomp_container* c;
+  EncDesc d;
+};
+
+void add_pad(ZeroList& z, uint8_t* base, uint64_t off, uint64_t sz) {
   const uint64_t p = padsec(sz);
-  if (p == sz) return cudaSuccess;
-  return cudaMemsetAsync(base + off + sz, 0, p - sz, s);
+  if (p == sz) return;
+  z.p[z.count] = base + off + sz;
+  z.len[z.count] = uint32_t(p - sz);
+  ++z.count;
+}
+
+template <typename F>
+cudaError_t for_chunks(std::vector<Job>& jobs, int scheme_filter, F&& launch) {
+  std::vector<int> idx;
+  for (int i = 0; i < int(jobs.size()); ++i)
+    if (scheme_filter < 0 || jobs[i].d.scheme == scheme_filter) idx.push_back(i);
+  for (size_t s = 0; s < idx.size(); s += kMaxBatch) {
+    EncBatch b;
+    memset(&b, 0, sizeof(b));
+    b.count = int(std::min<size_t>(kMaxBatch, idx.size() - s));
+    for (int j = 0; j < b.count; ++j) b.d[j] = jobs[idx[s + j]].d;
+    launch(b);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_zero(ZeroList& z, cudaStream_t s) {
+  if (!z.count) return cudaSuccess;
+  zero_kernel<<<z.count, 256, 0, s>>>(z);
+  count_launches(1);
+  z.count = 0;
+  return cudaGetLastError();
+}
+
+int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks, const int* schemes, int count,
+                cudaStream_t s, wcomp_container** out) {
+  for (int i = 0; i < count; ++i) out[i] = nullptr;
+  for (int i = 0; i < count; ++i) {
+    if (!ws[i] || Ns[i] <= 0 || Ks[i] <= 0) return WCOMP_EINVAL;
+    if (schemes[i] != WCOMP_BYTESPLIT && schemes[i] != WCOMP_K15) return WCOMP_EINVAL;
+    if (Ns[i] >= (int64_t(1) << 32) || Ks[i] >= (int64_t(1) << 32) ||
+        uint64_t(Ns[i]) * uint64_t(Ks[i]) >= (uint64_t(1) << 32))
+      return WCOMP_EUNSUPPORTED;
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int sms = sm_count(dev);
+  std::vector<Job> jobs(count);
+  for (auto& j : jobs) j.c = nullptr;
+  Summary* d_sum = nullptr;
+  auto fail = [&](cudaError_t err) -> int {
+    for (auto& j : jobs)
+      if (j.c) wcomp_free(j.c, s);
+    if (d_sum) cudaFreeAsync(d_sum, s);
+    return map_cuda(err);
+  };
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_sum), sizeof(Summary) * count, s);
+  if (e != cudaSuccess) return map_cuda(e);
+  ZeroList z;
+  memset(&z, 0, sizeof(z));
+  for (int i = 0; i < count; ++i) {
+    wcomp_container* c = new (std::nothrow) wcomp_container();
+    if (!c) return fail(cudaErrorMemoryAllocation);
+    jobs[i].c = c;
+    c->device = dev;
+    Layout& L = c->L;
+    L.compute(schemes[i], Ns[i], Ks[i], 0);
+    e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
+    if (e != cudaSuccess) return fail(e);
+    EncDesc& d = jobs[i].d;
+    memset(&d, 0, sizeof(d));
+    d.w = ws[i];
+    d.main = c->d_main;
+    d.summary = d_sum + i;
+    d.n = L.n;
+    d.N = L.N;
+    d.K = L.K;
+    d.off_codes = L.off_codes; d.off_raw = L.off_raw; d.off_a = L.off_a; d.off_b = L.off_b; d.off_c = L.off_c;
+    d.off_tile = L.off_tile; d.off_row = L.off_row; d.off_scratch = L.off_scratch;
+    d.n_tiles = uint32_t(L.n_tiles);
+    d.scheme = schemes[i];
+    d.aligned = (reinterpret_cast<uintptr_t>(ws[i]) & 15) == 0;
+    z.p[z.count] = c->d_main + L.off_scratch + Scratch::hist;
+    z.len[z.count] = kMaxBins * sizeof(uint32_t);
+    ++z.count;
+    add_pad(z, c->d_main, L.off_b, L.sz_b);
+    add_pad(z, c->d_main, L.off_c, L.sz_c);
+    add_pad(z, c->d_main, L.off_tile, L.sz_tile);
+    add_pad(z, c->d_main, L.off_row, L.sz_row);
+    if (z.count + 5 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+  }
+  if ((e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+
+  // a1: histogram blocks in proportion to size, at most 8191 elements per thread
+  uint64_t total_n = 0;
+  for (auto& j : jobs) total_n += j.d.n;
+  auto hist_launch = [&](int scheme) {
+    return for_chunks(jobs, scheme, [&](EncBatch& b) {
+      uint32_t blocks = 0;
+      for (int j = 0; j < b.count; ++j) {
+        b.prefix[j] = blocks;
+        const uint64_t want = std::max<uint64_t>(1, (uint64_t(sms) * 6 * b.d[j].n + total_n - 1) / total_n);
+        const uint64_t need = cdiv(b.d[j].n, uint64_t(8191) * 256);
+        blocks += uint32_t(std::min<uint64_t>(std::max(want, need), cdiv(b.d[j].n, 8 * 256)));
+      }
+      b.prefix[b.count] = blocks;
+      if (scheme == WCOMP_BYTESPLIT)
+        hist_kernel<8, 256><<<blocks, 256, 0, s>>>(b);
+      else
+        hist_kernel<7, 512><<<blocks, 256, 0, s>>>(b);
+      count_launches(1);
+    });
+  };
+  auto tiles_prefix = [](EncBatch& b) {
+    uint32_t t = 0;
+    for (int j = 0; j < b.count; ++j) {
+      b.prefix[j] = t;
+      t += b.d[j].n_tiles;
+    }
+    b.prefix[b.count] = t;
+    return t;
+  };
+  if ((e = hist_launch(WCOMP_BYTESPLIT)) != cudaSuccess) return fail(e);
+  if ((e = hist_launch(WCOMP_K15)) != cudaSuccess) return fail(e);
+  // a2: tables
+  e = for_chunks(jobs, -1, [&](EncBatch& b) {
+    select_kernel<<<b.count, 512, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  // a3: pack, then the tile scan
+  e = for_chunks(jobs, WCOMP_BYTESPLIT, [&](EncBatch& b) {
+    pack_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  e = for_chunks(jobs, WCOMP_K15, [&](EncBatch& b) {
+    pack_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  e = for_chunks(jobs, -1, [&](EncBatch& b) {
+    scan_kernel<<<b.count, 1024, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+
+  // the one synchronization: escape counts and tables
+  std::vector<Summary> hs(count);
+  e = cudaMemcpyAsync(hs.data(), d_sum, sizeof(Summary) * count, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(e);
+  cudaFreeAsync(d_sum, s);
+  d_sum = nullptr;
+
+  for (int i = 0; i < count; ++i) {
+    wcomp_container* c = jobs[i].c;
+    memcpy(c->table, hs[i].table, sizeof(c->table));
+    Layout& L = c->L;
+    L.compute(L.scheme, L.N, L.K, hs[i].E);
+    EncDesc& d = jobs[i].d;
+    d.E = L.E;
+    d.off_pos = L.off_pos;
+    d.off_val = L.off_val;
+    if (L.E) {
+      e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+      if (e != cudaSuccess) return fail(e);
+      d.esc = c->d_esc;
+      add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
+      add_pad(z, c->d_esc, L.off_val, L.sz_val);
+      if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+    }
+  }
+  if ((e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+  // a4: compaction for tensors with escapes; row indexes for all
+  std::vector<Job> with_esc;
+  for (auto& j : jobs)
+    if (j.d.E) with_esc.push_back(j);
+  e = for_chunks(with_esc, WCOMP_BYTESPLIT, [&](EncBatch& b) {
+    compact_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  e = for_chunks(with_esc, WCOMP_K15, [&](EncBatch& b) {
+    compact_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  e = for_chunks(jobs, -1, [&](EncBatch& b) {
+    uint32_t rows = 0;
+    for (int j = 0; j < b.count; ++j) {
+      b.prefix[j] = rows;
+      rows += uint32_t(b.d[j].N + 1);
+    }
+    b.prefix[b.count] = rows;
+    row_index_kernel<<<unsigned(cdiv(rows, 256)), 256, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail(e);
+  for (int i = 0; i < count; ++i) out[i] = jobs[i].c;
+  return WCOMP_OK;
 }
 
 }  // namespace
@@ -281,101 +558,11 @@ extern "C" int wcomp_encode(const uint16_t* d_w, int64_t N, int64_t K, int schem
   if (!out) return WCOMP_EINVAL;
   *out = nullptr;
   if (!d_w || N <= 0 || K <= 0) return WCOMP_EINVAL;
-  if (scheme != WCOMP_BYTESPLIT && scheme != WCOMP_K15) return WCOMP_EINVAL;
-  if (N >= (int64_t(1) << 32) || K >= (int64_t(1) << 32) || uint64_t(N) * uint64_t(K) >= (uint64_t(1) << 32))
-    return WCOMP_EUNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  wcomp_container* c = new (std::nothrow) wcomp_container();
-  if (!c) return WCOMP_ENOMEM;
-  cudaGetDevice(&c->device);
-  Layout& L = c->L;
-  L.compute(scheme, N, K, 0);
-  const int aligned = (reinterpret_cast<uintptr_t>(d_w) & 15) == 0;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
-  if (e != cudaSuccess) {
-    delete c;
-    return map_cuda(e);
-  }
-  uint8_t* m = c->d_main;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(m + L.off_scratch + Scratch::hist);
-  uint8_t* lut = m + L.off_scratch + Scratch::lut;
-  uint16_t* table16 = reinterpret_cast<uint16_t*>(m + L.off_scratch + Scratch::table);
-  uint32_t* tile_idx = reinterpret_cast<uint32_t*>(m + L.off_tile);
-  uint32_t* row_idx = reinterpret_cast<uint32_t*>(m + L.off_row);
-  const int nb = scheme == WCOMP_BYTESPLIT ? 256 : 512;
+  return encode_many(&d_w, &N, &K, &scheme, 1, static_cast<cudaStream_t>(stream), out);
+}
 
-  e = cudaMemsetAsync(hist, 0, kMaxBins * sizeof(uint32_t), s);
-  if (e == cudaSuccess) e = zero_pad(m, L.off_b, L.sz_b, s);
-  if (e == cudaSuccess) e = zero_pad(m, L.off_c, L.sz_c, s);
-  if (e == cudaSuccess) e = zero_pad(m, L.off_tile, L.sz_tile, s);
-  if (e == cudaSuccess) e = zero_pad(m, L.off_row, L.sz_row, s);
-
-  const int sms = sm_count(c->device);
-  if (e == cudaSuccess) {
-    const uint64_t chunks = cdiv(L.n, 8);
-    const int grid = int(std::min<uint64_t>(cdiv(chunks, 256), uint64_t(sms) * 4));
-    if (scheme == WCOMP_BYTESPLIT) {
-      const size_t smem = 256 * 32 * sizeof(uint32_t);
-      hist_kernel<8, 256><<<grid, 256, smem, s>>>(d_w, L.n, aligned, hist);
-    } else {
-      const size_t smem = 512 * 32 * sizeof(uint32_t);
-      static bool attr = false;
-      if (!attr) {
-        cudaFuncSetAttribute(hist_kernel<7, 512>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        attr = true;
-      }
-      hist_kernel<7, 512><<<grid, 256, smem, s>>>(d_w, L.n, aligned, hist);
-    }
-    select_kernel<<<1, 512, 0, s>>>(hist, nb, lut, table16);
-    const unsigned tiles = unsigned(L.n_tiles);
-    if (scheme == WCOMP_BYTESPLIT)
-      pack_kernel<WCOMP_BYTESPLIT><<<tiles, kThreads, 0, s>>>(d_w, L.n, aligned, lut, m + L.off_codes,
-                                                              m + L.off_raw, nullptr, nullptr, nullptr, tile_idx);
-    else
-      pack_kernel<WCOMP_K15><<<tiles, kThreads, 0, s>>>(d_w, L.n, aligned, lut, m + L.off_codes, nullptr,
-                                                        m + L.off_a, m + L.off_b, m + L.off_c, tile_idx);
-    scan_kernel<<<1, 1024, 0, s>>>(tile_idx, tiles);
-    count_launches(4);  // histogram, select, pack, scan
-    e = cudaGetLastError();
-  }
-  struct {
-    uint32_t E;
-    uint16_t table[16];
-  } hostinfo;
-  if (e == cudaSuccess) e = cudaMemcpyAsync(&hostinfo.E, tile_idx + L.n_tiles, 4, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(hostinfo.table, table16, 32, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) {
-    wcomp_free(c, stream);
-    return map_cuda(e);
-  }
-  memcpy(c->table, hostinfo.table, sizeof(c->table));
-  L.compute(scheme, N, K, hostinfo.E);
-  if (L.E) {
-    e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
-    uint8_t* x = c->d_esc;
-    if (e == cudaSuccess) e = zero_pad(x, L.off_pos, L.sz_pos, s);
-    if (e == cudaSuccess) e = zero_pad(x, L.off_val, L.sz_val, s);
-    if (e == cudaSuccess) {
-      uint32_t* pos = reinterpret_cast<uint32_t*>(x + L.off_pos);
-      uint8_t* val = x + L.off_val;
-      if (scheme == WCOMP_BYTESPLIT)
-        compact_kernel<WCOMP_BYTESPLIT><<<unsigned(L.n_tiles), kThreads, 0, s>>>(d_w, L.n, m + L.off_codes,
-                                                                                tile_idx, pos, val);
-      else
-        compact_kernel<WCOMP_K15><<<unsigned(L.n_tiles), kThreads, 0, s>>>(d_w, L.n, m + L.off_codes, tile_idx,
-                                                                          pos, val);
-      row_index_kernel<<<unsigned(cdiv(uint64_t(N) + 1, 256)), 256, 0, s>>>(pos, L.E, N, K, row_idx);
-      count_launches(2);  // compact, row index
-      e = cudaGetLastError();
-    }
-  } else {
-    e = cudaMemsetAsync(row_idx, 0, 4 * (uint64_t(N) + 1), s);
-  }
-  if (e != cudaSuccess) {
-    wcomp_free(c, stream);
-    return map_cuda(e);
-  }
-  *out = c;
-  return WCOMP_OK;
+extern "C" int wcomp_encode_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,
+                                    const int* schemes, int count, void* stream, wcomp_container** out) {
+  if (!d_w || !N || !K || !schemes || !out || count <= 0) return WCOMP_EINVAL;
+  return encode_many(d_w, N, K, schemes, count, static_cast<cudaStream_t>(stream), out);
 }

@@ -18,7 +18,7 @@
 // loads in flight while it computes the current one (register double
 // buffering), loads each stream with vector loads that bypass L1, rebuilds
 // BF16 pairs with prmt lookups, widens them to fp32 with a shift / mask and
-// accumulates with packed fp32x2 FMAs.  x is read through L1, where it stays
+// accumulates in fp32 (mixed-precision or packed fp32x2 FMAs, see below).  x is read through L1, where it stays
 // (every warp of the SM reads the same x).
 //
 // Escapes.  An escaped weight decodes to the placeholder (symbol 0, so
@@ -45,19 +45,25 @@ constexpr int kSlots = 1024;  // work-counter slots per device (one per launch, 
 
 enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
-struct F2 {
-  float x, y;
-};
+// FMA forms.  MODE 0 widens weights and x to fp32 and issues packed fp32x2
+// FMAs (x is widened once per unit of R rows).  MODE 1 feeds the BF16 halves
+// of the pair words straight into mixed-precision FMAs (bf16 x bf16 + fp32);
+// the product of two BF16 values is exact in fp32, so both forms round the
+// same sums.  MODE 1 saves the widening work and wins for small batches.
+#ifndef WCOMP_GEMV_MIXED_MAX_B
+#define WCOMP_GEMV_MIXED_MAX_B 2
+#endif
 
-__device__ __forceinline__ void fma2(F2& acc, uint32_t w_pair, float x0, float x1) {
-  // acc.{x,y} += {w_lo, w_hi} * {x0, x1} as one packed fp32x2 FMA
-  const float w0 = bf16_lo(w_pair), w1 = bf16_hi(w_pair);
-  uint64_t a, b, c, d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(w0), "f"(w1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(acc.x), "f"(acc.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(d));
+__device__ __forceinline__ void fma_wide(float2& acc, uint32_t w_pair, float x0, float x1) {
+  acc = __ffma2_rn(make_float2(bf16_lo(w_pair), bf16_hi(w_pair)), make_float2(x0, x1), acc);
+}
+
+__device__ __forceinline__ void fma_mixed(float2& acc, uint32_t w_pair, uint32_t x_pair) {
+  unsigned short w0, w1, x0, x1;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(w0), "=h"(w1) : "r"(w_pair));
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(x0), "=h"(x1) : "r"(x_pair));
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc.x) : "h"(w0), "h"(x0));
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc.y) : "h"(w1), "h"(x1));
 }
 
 __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
@@ -140,24 +146,31 @@ __device__ __forceinline__ void pairs8(const RegTable& t, const GroupBuf& b, uin
   w[3] = prmt(l1, h1, 0x7362);
 }
 
-template <int SRC, int BT, int R>
+template <int SRC, int BT, int R, int MODE>
 __device__ __forceinline__ void compute_group(const TensorDesc& d, const uint16_t* __restrict__ xg, int64_t K, int B,
-                                              const GroupBuf (&buf)[R], const bool (&live)[R], F2 (&acc)[R][BT]) {
+                                              const GroupBuf (&buf)[R], const bool (&live)[R],
+                                              float2 (&acc)[R][BT]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float xf[BT][8];
+    uint32_t xw[BT][4];
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
       if (b < B) {
         const uint4 v = ld_x_v4(xg + int64_t(b) * K + 8 * i);
-        xf[b][0] = bf16_lo(v.x); xf[b][1] = bf16_hi(v.x);
-        xf[b][2] = bf16_lo(v.y); xf[b][3] = bf16_hi(v.y);
-        xf[b][4] = bf16_lo(v.z); xf[b][5] = bf16_hi(v.z);
-        xf[b][6] = bf16_lo(v.w); xf[b][7] = bf16_hi(v.w);
+        xw[b][0] = v.x; xw[b][1] = v.y; xw[b][2] = v.z; xw[b][3] = v.w;
       } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xf[b][k] = 0.f;
+        xw[b][0] = xw[b][1] = xw[b][2] = xw[b][3] = 0u;
       }
+    }
+    float xf[MODE == 0 ? BT : 1][8];
+    if (MODE == 0) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          xf[MODE == 0 ? b : 0][2 * q] = bf16_lo(xw[b][q]);
+          xf[MODE == 0 ? b : 0][2 * q + 1] = bf16_hi(xw[b][q]);
+        }
     }
 #pragma unroll
     for (int j = 0; j < R; ++j) {
@@ -169,10 +182,13 @@ __device__ __forceinline__ void compute_group(const TensorDesc& d, const uint16_
       else pairs8<SRC, 3>(d.t, buf[j], w);
 #pragma unroll
       for (int b = 0; b < BT; ++b) {
-        fma2(acc[j][b], w[0], xf[b][0], xf[b][1]);
-        fma2(acc[j][b], w[1], xf[b][2], xf[b][3]);
-        fma2(acc[j][b], w[2], xf[b][4], xf[b][5]);
-        fma2(acc[j][b], w[3], xf[b][6], xf[b][7]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (MODE == 0)
+            fma_wide(acc[j][b], w[q], xf[MODE == 0 ? b : 0][2 * q], xf[MODE == 0 ? b : 0][2 * q + 1]);
+          else
+            fma_mixed(acc[j][b], w[q], xw[b][q]);
+        }
       }
     }
   }
@@ -222,7 +238,7 @@ __device__ __forceinline__ uint32_t grab(uint32_t* slot, int lane) {
 // ---------------------------------------------------------------------------
 // The kernel (vector path: K % 32 == 0, aligned streams and x).
 // ---------------------------------------------------------------------------
-template <int SRC, int BT, int R, int MINB>
+template <int SRC, int BT, int R, int MINB, int MODE>
 __global__ void __launch_bounds__(kThreads, MINB)
     gemv_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
   const int lane = threadIdx.x & 31;
@@ -238,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     bool live[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
-    F2 acc[R][BT];
+    float2 acc[R][BT];
 #pragma unroll
     for (int j = 0; j < R; ++j)
 #pragma unroll
-      for (int b = 0; b < BT; ++b) acc[j][b] = F2{0.f, 0.f};
+      for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
 
     GroupBuf b0[R], b1[R];
     uint64_t gk = lane;
@@ -269,14 +285,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int j = 0; j < R; ++j)
           if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 32, b1[j]);
       }
-      compute_group<SRC, BT, R>(d, x + gk * kGroup, K, B, b0, live, acc);
+      compute_group<SRC, BT, R, MODE>(d, x + gk * kGroup, K, B, b0, live, acc);
       if (!more) break;
       if (gk + 64 < KG) {
 #pragma unroll
         for (int j = 0; j < R; ++j)
           if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 64, b0[j]);
       }
-      compute_group<SRC, BT, R>(d, x + (gk + 32) * kGroup, K, B, b1, live, acc);
+      compute_group<SRC, BT, R, MODE>(d, x + (gk + 32) * kGroup, K, B, b1, live, acc);
     }
 
     float s[R][BT];
@@ -376,7 +392,7 @@ int counter_slot(int dev, uint32_t** slot) {
   return WCOMP_OK;
 }
 
-template <int SRC, int BT, int R, int MINB>
+template <int SRC, int BT, int R, int MINB, int MODE = (BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0)>
 int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
   uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
@@ -390,14 +406,14 @@ int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   static int per_sm_cache = 0;
   if (!per_sm_cache) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE>, kThreads, 0) !=
             cudaSuccess ||
         per_sm <= 0)
       per_sm = 1;
     per_sm_cache = per_sm;
   }
   const int blocks = per_sm_cache * sms;
-  gemv_kernel<SRC, BT, R, MINB><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
+  gemv_kernel<SRC, BT, R, MINB, MODE><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }

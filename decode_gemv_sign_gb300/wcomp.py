@@ -64,6 +64,9 @@ def lib():
                            "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
     L = ctypes.CDLL(LIB_PATH)
     L.wcomp_encode.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, ctypes.POINTER(P)]
+    L.wcomp_encode_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
+                                       P, ctypes.POINTER(P)]
     L.wcomp_decode.argtypes = [P, P, P]
     L.wcomp_gemv.argtypes = [P, P, ctypes.c_int, P, P]
     L.wcomp_gemv_bf16.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int, P, P]
@@ -83,7 +86,7 @@ def lib():
     L.wcomp_version.argtypes = []
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
-    for name in ("wcomp_encode", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
+    for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
                  "wcomp_decode_batched",
                  "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -177,6 +180,28 @@ def encode(w: torch.Tensor, scheme, stream=None) -> Container:
     _check(lib().wcomp_encode(P(w.data_ptr()), N, K, SCHEMES[scheme], P(_stream(stream)), ctypes.byref(h)),
            "wcomp_encode")
     return Container(h.value)
+
+
+def encode_batched(ws: Sequence[torch.Tensor], schemes, stream=None) -> List[Container]:
+    """Encode several tensors in one batched pass (one host synchronization).
+
+    ``schemes`` is one scheme for all tensors or a sequence with one per tensor.
+    """
+    n = len(ws)
+    if isinstance(schemes, (str, int)):
+        schemes = [schemes] * n
+    Ns, Ks = [], []
+    for w in ws:
+        _bits16(w, "w")
+        if w.dim() not in (1, 2):
+            raise ValueError("w must be 1-D or 2-D")
+        Ns.append(w.shape[0] if w.dim() == 2 else 1)
+        Ks.append(w.shape[1] if w.dim() == 2 else w.numel())
+    outs = (P * n)()
+    _check(lib().wcomp_encode_batched(_ptr_array([w.data_ptr() for w in ws]), (ctypes.c_int64 * n)(*Ns),
+                                      (ctypes.c_int64 * n)(*Ks), (ctypes.c_int * n)(*[SCHEMES[x] for x in schemes]),
+                                      n, P(_stream(stream)), outs), "wcomp_encode_batched")
+    return [Container(outs[i]) for i in range(n)]
 
 
 def decode(c: Container, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

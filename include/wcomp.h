@@ -106,6 +106,15 @@ WCOMP_API int wcomp_encode(const uint16_t* d_w, int64_t N, int64_t K, int scheme
                  wcomp_container** out);
 
 /*
+ * Encode `count` tensors in one pass: tensor i is W_i[N[i], K[i]] at d_w[i],
+ * coded with schemes[i]; out[i] receives its container.  The same steps as
+ * wcomp_encode run as batched launches over all tensors, with one stream
+ * synchronization for the whole batch.  On failure every out[i] is NULL.
+ */
+WCOMP_API int wcomp_encode_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,
+                                   const int* schemes, int count, void* stream, wcomp_container** out);
+
+/*
  * Decode a container to exact BF16 bits.
  *   d_out   device, uint16[N*K]; the caller's buffer.
  * The code stream is expanded through the 15-entry table, joined with the raw

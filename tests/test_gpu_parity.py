@@ -191,6 +191,23 @@ def test_batched_matches_single(W):
         c.free()
 
 
+def test_encode_batched_matches_single(W):
+    specs = [synth.WeightSpec(f"e{i}", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=1000 + i)
+             for i, (N, K) in enumerate([(64, 1024), (1, 31), (33, 1000), (128, 2048), (3, 40000), (7, 301)])]
+    ws = [synth.gen_weights_np(s) for s in specs]
+    schemes = [i % 2 for i in range(len(ws))]
+    cs = W.encode_batched([dev(w) for w in ws], schemes)
+    for w, c, sc in zip(ws, cs, schemes):
+        assert W.serialize(c) == O.serialize(O.encode(w, sc))
+    # more tensors than one launch carries, mixed schemes and shapes
+    ws2 = [synth.gen_weights_np(synth.WeightSpec(f"f{i}", 8 + i, 256 + 32 * (i % 5), "normal", 0.02, 0.02,
+                                                 "normal", 1.0, seed=1100 + i)) for i in range(75)]
+    cs2 = W.encode_batched([dev(w) for w in ws2], [(i // 3) % 2 for i in range(75)])
+    for i, (w, c) in enumerate(zip(ws2, cs2)):
+        assert W.serialize(c) == O.serialize(O.encode(w, (i // 3) % 2))
+        assert np.array_equal(host(W.decode(c)).reshape(w.shape), w)
+
+
 def test_many_tensors_batch_over_limit(W):
     # more containers than one launch carries
     ws = [synth.gen_weights_np(synth.WeightSpec(f"m{i}", 16, 512, "normal", 0.02, 0.01, "normal", 1.0, seed=600 + i))
