@@ -75,6 +75,7 @@ extern "C" const char* wcomp_strerror(int s) {
     case WCOMP_ECORRUPT: return "corrupt container";
     case WCOMP_ECUDA: return "CUDA error";
     case WCOMP_EUNSUPPORTED: return "unsupported size";
+    case WCOMP_ETIMEOUT: return "a device wait timed out";
     default: return "unknown status";
   }
 }

@@ -13,13 +13,13 @@
 // tensor; a launch covers the units of every tensor in the batch.  The grid is
 // persistent (as many CTAs as fit on the GPU at once) and every warp grabs
 // units from a global counter, one at a time, so the GPU drains evenly even
-// when the tensors differ in shape.  Inside a unit the warp walks the rows:
-// lane l takes the 32-element groups l, l+32, ..., keeps the next group's
-// loads in flight while it computes the current one (register double
-// buffering), loads each stream with vector loads that bypass L1, rebuilds
-// BF16 pairs with prmt lookups, widens them to fp32 with a shift / mask and
-// accumulates in fp32 (mixed-precision or packed fp32x2 FMAs, see below).  x is read through L1, where it stays
-// (every warp of the SM reads the same x).
+// when the tensors differ in shape.  Inside a unit the warp walks the rows in
+// 1024-element chunks (lane mapping below), keeps the next chunk's loads in
+// flight while it computes the current one (register double buffering),
+// loads the streams with coalesced loads that bypass L1, rebuilds BF16 pairs
+// with prmt lookups and accumulates in fp32 (mixed-precision or packed
+// fp32x2 FMAs, see below).  x is read through L1, where it stays (every warp
+// of the SM reads the same x).
 //
 // Escapes.  An escaped weight decodes to the placeholder (symbol 0, so
 // |w| < 2^-125).  Each lane adds x * (w_true - w_placeholder) for a share of
@@ -51,7 +51,7 @@ enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 // the product of two BF16 values is exact in fp32, so both forms round the
 // same sums.  MODE 1 saves the widening work and wins for small batches.
 #ifndef WCOMP_GEMV_MIXED_MAX_B
-#define WCOMP_GEMV_MIXED_MAX_B 2
+#define WCOMP_GEMV_MIXED_MAX_B 4
 #endif
 
 __device__ __forceinline__ void fma_wide(float2& acc, uint32_t w_pair, float x0, float x1) {
@@ -82,44 +82,53 @@ __device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// Weight sources: one 32-element group of one row.
+// Lane mapping.  A row is walked in chunks of 1024 elements.  Inside a chunk,
+// lane l owns the four 8-element slices starting at 256 i + 8 l (i = 0..3):
+// for every slice the 32 lanes cover 256 consecutive elements, so each load
+// of codes (4 bytes), raw bytes (8), mantissa-plane words, plain BF16 (16)
+// and x (16) is one contiguous, fully coalesced request per warp.
 // ---------------------------------------------------------------------------
-struct GroupBuf {
+constexpr int kChunk = 1024;
+constexpr int kSlice = 256;
+
+// One row's share of a chunk for one lane.
+//   byte-split: v[i] code word of slice i, v[4+2i], v[5+2i] its raw bytes
+//   K15:        v[i] code word, v[4+i] plane A word, v[8+i] plane B word,
+//               v[12+i] plane C word (shared by the 4 lanes of a 32-element group)
+//   plain:      v[4i .. 4i+3] the slice's 8 BF16 values
+struct ChunkBuf {
   uint32_t v[16];
 };
 
-template <int SRC>
-__device__ __forceinline__ void load_buf(const TensorDesc& d, uint64_t g, GroupBuf& b) {
-  if (SRC == kBytesplit) {
-    const uint4 c = ld_stream_v4(d.codes + 16 * g);
-    b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
-    uint32_t r[8];
-    ld_stream_v8(d.raw + 32 * g, r);
+template <int SRC, bool FULL>
+__device__ __forceinline__ void load_chunk(const TensorDesc& d, uint64_t e_base, uint32_t vmask, int lane,
+                                           ChunkBuf& b) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b.v[4 + i] = r[i];
-  } else if (SRC == kK15) {
-    const uint4 c = ld_stream_v4(d.codes + 16 * g);
-    const uint4 a = ld_stream_v4(d.pa + 16 * g);
-    const uint2 pb = ld_stream_v2(d.pb + 8 * g);
-    b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
-    b.v[4] = a.x; b.v[5] = a.y; b.v[6] = a.z; b.v[7] = a.w;
-    b.v[8] = pb.x; b.v[9] = pb.y;
-    b.v[10] = ld_stream_u32(d.pc + 4 * g);
-  } else {
-    uint32_t r[8];
-    const uint8_t* w = d.raw + 64 * g;
-    ld_stream_v8(w, r);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) b.v[i] = r[i];
-    ld_stream_v8(w + 32, r);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) b.v[8 + i] = r[i];
+  for (int i = 0; i < 4; ++i) {
+    if (!FULL && !((vmask >> i) & 1)) continue;
+    const uint64_t e = e_base + kSlice * i + 8 * lane;
+    if (SRC == kBytesplit) {
+      b.v[i] = ld_stream_u32(d.codes + (e >> 1));
+      const uint2 r = ld_stream_v2(d.raw + e);
+      b.v[4 + 2 * i] = r.x;
+      b.v[5 + 2 * i] = r.y;
+    } else if (SRC == kK15) {
+      const uint64_t g = e >> 5;
+      const uint32_t q2 = lane & 3;  // which 8 elements of the 32-element group
+      b.v[i] = ld_stream_u32(d.codes + (e >> 1));
+      b.v[4 + i] = ld_stream_u32(d.pa + 16 * g + 4 * q2);
+      b.v[8 + i] = ld_stream_u32(d.pb + 8 * g + 4 * (q2 >> 1));
+      b.v[12 + i] = ld_stream_u32(d.pc + 4 * g);
+    } else {
+      const uint4 w = ld_stream_v4(d.raw + 2 * e);
+      b.v[4 * i + 0] = w.x; b.v[4 * i + 1] = w.y; b.v[4 * i + 2] = w.z; b.v[4 * i + 3] = w.w;
+    }
   }
 }
 
-// BF16 pairs of code word I (elements 8I .. 8I+7) of a loaded group.
+// BF16 pairs (elements 2q, 2q+1 of the slice in w[q]) of slice I.
 template <int SRC, int I>
-__device__ __forceinline__ void pairs8(const RegTable& t, const GroupBuf& b, uint32_t (&w)[4]) {
+__device__ __forceinline__ void slice_pairs(const RegTable& t, const ChunkBuf& b, int lane, uint32_t (&w)[4]) {
   if (SRC == kPlain) {
     w[0] = b.v[4 * I + 0]; w[1] = b.v[4 * I + 1]; w[2] = b.v[4 * I + 2]; w[3] = b.v[4 * I + 3];
     return;
@@ -133,12 +142,14 @@ __device__ __forceinline__ void pairs8(const RegTable& t, const GroupBuf& b, uin
     l0 = b.v[4 + 2 * I];
     l1 = b.v[5 + 2 * I];
   } else {
-    const uint32_t a[4] = {b.v[4], b.v[5], b.v[6], b.v[7]};
-    const uint32_t pb[2] = {b.v[8], b.v[9]};
+    // quads q0 = 2 (lane & 3) and q0 + 1 of the 32-element group
+    const uint32_t A = b.v[4 + I], Bw = b.v[8 + I], C = b.v[12 + I];
+    const uint32_t q0 = 2 * (lane & 3), sb0 = 4 * (lane & 1);
     uint32_t e0, e1;
     lookup8(t.e0, m7, m, e0, e1);
-    l0 = k15_mant<2 * I>(a, pb, b.v[10]) | e0;
-    l1 = k15_mant<2 * I + 1>(a, pb, b.v[10]) | e1;
+    l0 = (A & 0x0F0F0F0Fu) | (((Bw >> sb0) << 4) & 0x30303030u) | (((C >> q0) << 6) & 0x40404040u) | e0;
+    l1 = ((A >> 4) & 0x0F0F0F0Fu) | (((Bw >> (sb0 + 2)) << 4) & 0x30303030u) |
+         (((C >> (q0 + 1)) << 6) & 0x40404040u) | e1;
   }
   w[0] = prmt(l0, h0, 0x5140);
   w[1] = prmt(l0, h0, 0x7362);
@@ -146,17 +157,18 @@ __device__ __forceinline__ void pairs8(const RegTable& t, const GroupBuf& b, uin
   w[3] = prmt(l1, h1, 0x7362);
 }
 
-template <int SRC, int BT, int R, int MODE>
-__device__ __forceinline__ void compute_group(const TensorDesc& d, const uint16_t* __restrict__ xg, int64_t K, int B,
-                                              const GroupBuf (&buf)[R], const bool (&live)[R],
-                                              float2 (&acc)[R][BT]) {
+template <int SRC, int BT, int R, int MODE, bool FULL>
+__device__ __forceinline__ void compute_chunk(const TensorDesc& d, const uint16_t* __restrict__ xc, int64_t K, int B,
+                                              const ChunkBuf (&buf)[R], const bool (&live)[R], uint32_t vmask,
+                                              int lane, float2 (&acc)[R][BT]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
+    if (!FULL && !((vmask >> i) & 1)) continue;
     uint32_t xw[BT][4];
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
       if (b < B) {
-        const uint4 v = ld_x_v4(xg + int64_t(b) * K + 8 * i);
+        const uint4 v = ld_x_v4(xc + int64_t(b) * K + kSlice * i + 8 * lane);
         xw[b][0] = v.x; xw[b][1] = v.y; xw[b][2] = v.z; xw[b][3] = v.w;
       } else {
         xw[b][0] = xw[b][1] = xw[b][2] = xw[b][3] = 0u;
@@ -176,10 +188,10 @@ __device__ __forceinline__ void compute_group(const TensorDesc& d, const uint16_
     for (int j = 0; j < R; ++j) {
       if (!live[j]) continue;
       uint32_t w[4];
-      if (i == 0) pairs8<SRC, 0>(d.t, buf[j], w);
-      else if (i == 1) pairs8<SRC, 1>(d.t, buf[j], w);
-      else if (i == 2) pairs8<SRC, 2>(d.t, buf[j], w);
-      else pairs8<SRC, 3>(d.t, buf[j], w);
+      if (i == 0) slice_pairs<SRC, 0>(d.t, buf[j], lane, w);
+      else if (i == 1) slice_pairs<SRC, 1>(d.t, buf[j], lane, w);
+      else if (i == 2) slice_pairs<SRC, 2>(d.t, buf[j], lane, w);
+      else slice_pairs<SRC, 3>(d.t, buf[j], lane, w);
 #pragma unroll
       for (int b = 0; b < BT; ++b) {
 #pragma unroll
@@ -250,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const uint16_t* __restrict__ x = p.x[ti];
     const int64_t r0 = int64_t(u - p.set_prefix[ti]) * R;
     const int64_t K = d.K;
-    const uint64_t KG = uint64_t(K) / kGroup;
     bool live[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
@@ -260,13 +271,33 @@ __global__ void __launch_bounds__(kThreads, MINB)
 #pragma unroll
       for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
 
-    GroupBuf b0[R], b1[R];
-    uint64_t gk = lane;
-    if (gk < KG) {
+    // valid slices of the last (partial) chunk: slice i of this lane ends by K
+    const uint32_t nchunks = uint32_t(cdiv(uint64_t(K), kChunk));
+    const uint32_t krem = uint32_t(K - int64_t(nchunks - 1) * kChunk);
+    uint32_t vlast = 0;
 #pragma unroll
-      for (int j = 0; j < R; ++j)
-        if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk, b0[j]);
-    }
+    for (int i = 0; i < 4; ++i) vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
+    const bool last_full = krem == kChunk;
+
+    ChunkBuf b0[R], b1[R];
+    auto load = [&](uint32_t c, ChunkBuf (&bb)[R]) {
+      const bool full = c + 1 < nchunks || last_full;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (!live[j]) continue;
+        const uint64_t eb = uint64_t(r0 + j) * uint64_t(K) + uint64_t(c) * kChunk;
+        if (full) load_chunk<SRC, true>(d, eb, 0xF, lane, bb[j]);
+        else load_chunk<SRC, false>(d, eb, vlast, lane, bb[j]);
+      }
+    };
+    auto compute = [&](uint32_t c, const ChunkBuf (&bb)[R]) {
+      const uint16_t* xc = x + uint64_t(c) * kChunk;
+      if (c + 1 < nchunks || last_full)
+        compute_chunk<SRC, BT, R, MODE, true>(d, xc, K, B, bb, live, 0xF, lane, acc);
+      else
+        compute_chunk<SRC, BT, R, MODE, false>(d, xc, K, B, bb, live, vlast, lane, acc);
+    };
+    load(0, b0);
     // escape slice of the unit: index now, first entries right after
     uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
     if (SRC != kPlain) {
@@ -278,21 +309,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         v0 = load_esc_val(d, e_lo + lane);
       }
     }
-    for (; gk < KG; gk += 64) {
-      const bool more = gk + 32 < KG;
-      if (more) {
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-          if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 32, b1[j]);
-      }
-      compute_group<SRC, BT, R, MODE>(d, x + gk * kGroup, K, B, b0, live, acc);
+    for (uint32_t c = 0; c < nchunks; c += 2) {
+      const bool more = c + 1 < nchunks;
+      if (more) load(c + 1, b1);
+      compute(c, b0);
       if (!more) break;
-      if (gk + 64 < KG) {
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-          if (live[j]) load_buf<SRC>(d, uint64_t(r0 + j) * KG + gk + 64, b0[j]);
-      }
-      compute_group<SRC, BT, R, MODE>(d, x + (gk + 32) * kGroup, K, B, b1, live, acc);
+      if (c + 2 < nchunks) load(c + 2, b0);
+      compute(c + 1, b1);
     }
 
     float s[R][BT];
@@ -318,6 +341,313 @@ __global__ void __launch_bounds__(kThreads, MINB)
     for (int j = 0; j < R; ++j)
       if (live[j]) warp_reduce_store<BT>(s[j], B, p.y[ti], d.N, r0 + j, lane);
     u = u_next;
+  }
+  // The last warp to finish returns the counter slot to zero for the next launch.
+  if (lane == 0) {
+    __threadfence();
+    const uint32_t total_warps = gridDim.x * kWarps;
+    if (atomicAdd(slot + 1, 1u) == total_warps - 1) {
+      atomicExch(slot, 0u);
+      atomicExch(slot + 1, 0u);
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The staged kernel: the same work decomposition, with the weight streams
+// brought into shared memory by bulk asynchronous copies (TMA, 1-D form).
+//
+// Every warp owns a ring of S stages.  One stage holds one 1024-element chunk
+// of each of the unit's R rows; lane 0 keeps S chunks in flight (it grabs the
+// next unit as soon as the current one is fully requested, so the ring runs
+// across unit boundaries) and every lane waits on the stage's mbarrier before
+// reading its slices out of shared memory.  Bytes in flight per SM no longer
+// cost registers, so far more of them are outstanding than with register
+// double buffering.  Waits are bounded: a stage that never completes sets the
+// device error word and the warp stops after draining its own copies.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls of try_wait before giving up (well over a second)
+
+template <int SRC>
+struct Geom {
+  // shared-memory bytes for one row's chunk: codes | raw   (byte-split)
+  //                                          codes | A | B window | C window   (K15)
+  //                                          BF16 values   (plain)
+  static constexpr uint32_t kB = 1024;                     // K15 plane B window offset
+  static constexpr uint32_t kC = 1024 + 256 + 16;          // K15 plane C window offset
+  static constexpr uint32_t row_bytes = SRC == kBytesplit ? 1536 : SRC == kK15 ? (kC + 128 + 16) : 2048;
+};
+
+// Words of slice i of one row, read from a stage.
+struct SliceWords {
+  uint32_t cw, r0, r1, A, Bw, C;
+  uint4 pw;
+};
+
+template <int SRC>
+__device__ __forceinline__ SliceWords read_slice(const uint8_t* rowbuf, int i, int lane, uint32_t dB, uint32_t dC) {
+  SliceWords w;
+  if (SRC == kPlain) {
+    w.pw = *reinterpret_cast<const uint4*>(rowbuf + 512 * i + 16 * lane);
+    return w;
+  }
+  w.cw = *reinterpret_cast<const uint32_t*>(rowbuf + 128 * i + 4 * lane);
+  if (SRC == kBytesplit) {
+    const uint2 r = *reinterpret_cast<const uint2*>(rowbuf + 512 + 256 * i + 8 * lane);
+    w.r0 = r.x;
+    w.r1 = r.y;
+  } else {
+    w.A = *reinterpret_cast<const uint32_t*>(rowbuf + 512 + 128 * i + 4 * lane);
+    w.Bw = *reinterpret_cast<const uint32_t*>(rowbuf + Geom<kK15>::kB + dB + 64 * i + 8 * (lane >> 2) +
+                                              4 * ((lane >> 1) & 1));
+    w.C = *reinterpret_cast<const uint32_t*>(rowbuf + Geom<kK15>::kC + dC + 32 * i + 4 * (lane >> 2));
+  }
+  return w;
+}
+
+template <int SRC>
+__device__ __forceinline__ void words_to_pairs(const RegTable& t, const SliceWords& sw, int lane, uint32_t (&w)[4]) {
+  if (SRC == kPlain) {
+    w[0] = sw.pw.x; w[1] = sw.pw.y; w[2] = sw.pw.z; w[3] = sw.pw.w;
+    return;
+  }
+  const QuadMasks m = code_masks(sw.cw);
+  const uint32_t m7 = sw.cw & 0x77777777u;
+  uint32_t h0, h1, l0, l1;
+  lookup8(t.hi, m7, m, h0, h1);
+  if (SRC == kBytesplit) {
+    l0 = sw.r0;
+    l1 = sw.r1;
+  } else {
+    const uint32_t q0 = 2 * (lane & 3), sb0 = 4 * (lane & 1);
+    uint32_t e0, e1;
+    lookup8(t.e0, m7, m, e0, e1);
+    l0 = (sw.A & 0x0F0F0F0Fu) | (((sw.Bw >> sb0) << 4) & 0x30303030u) | (((sw.C >> q0) << 6) & 0x40404040u) | e0;
+    l1 = ((sw.A >> 4) & 0x0F0F0F0Fu) | (((sw.Bw >> (sb0 + 2)) << 4) & 0x30303030u) |
+         (((sw.C >> (q0 + 1)) << 6) & 0x40404040u) | e1;
+  }
+  w[0] = prmt(l0, h0, 0x5140);
+  w[1] = prmt(l0, h0, 0x7362);
+  w[2] = prmt(l1, h1, 0x5140);
+  w[3] = prmt(l1, h1, 0x7362);
+}
+
+// Issue the bulk copies of chunk c of unit u's rows into one stage.
+template <int SRC, int R>
+__device__ __forceinline__ void issue_chunk(const GemvBatch& p, uint32_t u, uint32_t c, uint8_t* stage,
+                                            uint64_t* bar) {
+  const int ti = owner(p.set_prefix, p.count, u);
+  const TensorDesc& d = p.d[ti];
+  const int64_t r0 = int64_t(u - p.set_prefix[ti]) * R;
+  const uint64_t K = uint64_t(d.K);
+  const uint64_t k0 = uint64_t(c) * kChunk;
+  const uint32_t len = uint32_t(K - k0 < uint64_t(kChunk) ? K - k0 : uint64_t(kChunk));
+  uint32_t bytes = 0;
+  uint32_t sz[R][4];
+  const uint8_t* src[R][4];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sz[j][q] = 0;
+    if (r0 + j >= d.N) continue;
+    const uint64_t e0 = uint64_t(r0 + j) * K + k0;
+    if (SRC == kBytesplit) {
+      src[j][0] = d.codes + e0 / 2; sz[j][0] = len / 2;
+      src[j][1] = d.raw + e0; sz[j][1] = len;
+    } else if (SRC == kK15) {
+      src[j][0] = d.codes + e0 / 2; sz[j][0] = len / 2;
+      src[j][1] = d.pa + e0 / 2; sz[j][1] = len / 2;
+      const uint64_t bs = (e0 / 4) & ~uint64_t(15), be = ((e0 + len) / 4 + 15) & ~uint64_t(15);
+      src[j][2] = d.pb + bs; sz[j][2] = uint32_t(be - bs);
+      const uint64_t cs = (e0 / 8) & ~uint64_t(15), ce = ((e0 + len) / 8 + 15) & ~uint64_t(15);
+      src[j][3] = d.pc + cs; sz[j][3] = uint32_t(ce - cs);
+    } else {
+      src[j][0] = d.raw + 2 * e0; sz[j][0] = 2 * len;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bytes += sz[j][q];
+  }
+  fence_proxy_async();  // earlier generic reads of this stage come before the new async writes
+  mbar_expect_tx(bar, bytes);
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    uint8_t* rb = stage + j * Geom<SRC>::row_bytes;
+    const uint32_t dst_off[4] = {0u, SRC == kBytesplit || SRC == kK15 ? 512u : 0u, Geom<kK15>::kB, Geom<kK15>::kC};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (sz[j][q]) bulk_load(rb + dst_off[q], src[j][q], sz[j][q], bar);
+  }
+}
+
+template <int SRC, int BT, int R, int MODE, int S, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    gemv_tma_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot,
+                    uint32_t* __restrict__ err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr uint32_t kStage = (R * Geom<SRC>::row_bytes + 127) & ~127u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t* ring = smem + uint32_t(warp) * (S * kStage + S * 8 + 2 * S * 4);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * kStage);
+  uint32_t* uq = reinterpret_cast<uint32_t*>(ring + S * kStage + S * 8);
+  if (lane == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // producer state (warp-uniform): next unit / chunk to request
+  uint32_t pu = grab(slot, lane), pc = 0, pseq = 0;
+  uint32_t issued = 0, consumed = 0;
+  auto chunks_of = [&](uint32_t u) -> uint32_t {
+    const int ti = owner(p.set_prefix, p.count, u);
+    return uint32_t(cdiv(uint64_t(p.d[ti].K), kChunk));
+  };
+  uint32_t pn = pu < total_units ? chunks_of(pu) : 0;
+  // consumer state
+  uint32_t cseq = 0, cu = 0, cc = 0, cn = 0;
+  int ti = 0;
+  int64_t r0 = 0;
+  bool live[R];
+  float2 acc[R][BT];
+  uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
+  bool failed = false;
+
+  while (true) {
+    // keep S chunks requested
+    while (pu < total_units && issued - consumed < uint32_t(S)) {
+      if (pc == 0) {
+        if (lane == 0) uq[pseq % (2 * S)] = pu;
+        ++pseq;
+      }
+      if (lane == 0) issue_chunk<SRC, R>(p, pu, pc, ring + (issued % S) * kStage, &bars[issued % S]);
+      ++issued;
+      if (++pc == pn) {
+        pu = grab(slot, lane);
+        pc = 0;
+        pn = pu < total_units ? chunks_of(pu) : 0;
+      }
+    }
+    __syncwarp();
+    if (consumed == issued) break;
+    if (cc == 0) {  // start a unit
+      cu = uq[cseq % (2 * S)];
+      ++cseq;
+      ti = owner(p.set_prefix, p.count, cu);
+      const TensorDesc& d = p.d[ti];
+      r0 = int64_t(cu - p.set_prefix[ti]) * R;
+      cn = uint32_t(cdiv(uint64_t(d.K), kChunk));
+#pragma unroll
+      for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
+      if (SRC != kPlain) {
+        const int64_t r_end = r0 + R < d.N ? r0 + R : d.N;
+        e_lo = d.row_index[r0];
+        e_hi = d.row_index[r_end];
+        if (e_lo + lane < e_hi) {
+          p0 = d.esc_pos[e_lo + lane];
+          v0 = load_esc_val(d, e_lo + lane);
+        }
+      }
+    }
+    const TensorDesc& d = p.d[ti];
+    const int64_t K = d.K;
+    const uint32_t st = consumed % S;
+    if (!mbar_wait(&bars[st], (consumed / S) & 1, kWaitLimit)) {
+      failed = true;
+      break;
+    }
+    // compute chunk cc of the current unit
+    {
+      const uint64_t k0 = uint64_t(cc) * kChunk;
+      const uint32_t len = uint32_t(uint64_t(K) - k0 < uint64_t(kChunk) ? uint64_t(K) - k0 : uint64_t(kChunk));
+      const uint16_t* xc = p.x[ti] + k0;
+      const uint8_t* sbuf = ring + st * kStage;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool valid = kSlice * i + 8 * lane + 8 <= int(len);
+        if (len == kChunk || valid) {
+          uint32_t xw[BT][4];
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            if (b < B) {
+              const uint4 v = ld_x_v4(xc + int64_t(b) * K + kSlice * i + 8 * lane);
+              xw[b][0] = v.x; xw[b][1] = v.y; xw[b][2] = v.z; xw[b][3] = v.w;
+            } else {
+              xw[b][0] = xw[b][1] = xw[b][2] = xw[b][3] = 0u;
+            }
+          }
+          float xf[MODE == 0 ? BT : 1][8];
+          if (MODE == 0) {
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                xf[MODE == 0 ? b : 0][2 * q] = bf16_lo(xw[b][q]);
+                xf[MODE == 0 ? b : 0][2 * q + 1] = bf16_hi(xw[b][q]);
+              }
+          }
+#pragma unroll
+          for (int j = 0; j < R; ++j) {
+            if (!live[j]) continue;
+            uint32_t dB = 0, dC = 0;
+            if (SRC == kK15) {
+              const uint64_t e0 = uint64_t(r0 + j) * uint64_t(K) + k0;
+              dB = uint32_t((e0 / 4) & 15);
+              dC = uint32_t((e0 / 8) & 15);
+            }
+            const SliceWords sw = read_slice<SRC>(sbuf + j * Geom<SRC>::row_bytes, i, lane, dB, dC);
+            uint32_t w[4];
+            words_to_pairs<SRC>(d.t, sw, lane, w);
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (MODE == 0)
+                  fma_wide(acc[j][b], w[q], xf[MODE == 0 ? b : 0][2 * q], xf[MODE == 0 ? b : 0][2 * q + 1]);
+                else
+                  fma_mixed(acc[j][b], w[q], xw[b][q]);
+              }
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with the stage before lane 0 refills it
+    ++consumed;
+    if (++cc == cn) {  // unit complete: escapes, reduction, store
+      cc = 0;
+      float s[R][BT];
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) s[j][b] = acc[j][b].x + acc[j][b].y;
+      if (SRC != kPlain) {
+        const uint16_t* __restrict__ x = p.x[ti];
+        for (uint32_t e = e_lo + lane; e < e_hi; e += 32) {
+          uint32_t pos = p0, val = v0;
+          if (e != e_lo + lane) {
+            pos = d.esc_pos[e];
+            val = load_esc_val(d, e);
+          }
+          const int64_t j = int64_t(pos / uint64_t(K)) - r0;
+#pragma unroll
+          for (int jj = 0; jj < R; ++jj)
+            if (jj == j) add_escape<BT>(d, x, B, uint64_t(r0 + jj) * uint64_t(K), pos, val, s[jj]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        if (live[j]) warp_reduce_store<BT>(s[j], B, p.y[ti], d.N, r0 + j, lane);
+    }
+  }
+  if (failed) {
+    // record the failure and let this warp's own copies land before exiting
+    if (lane == 0) atomicOr(err, 1u);
+    for (uint32_t k = consumed + 1; k < issued; ++k) mbar_wait(&bars[k % S], (k / S) & 1, kWaitLimit);
+    __syncwarp();
   }
   // The last warp to finish returns the counter slot to zero for the next launch.
   if (lane == 0) {
@@ -376,19 +706,28 @@ std::mutex g_scratch_mu;
 uint32_t* g_scratch[64] = {nullptr};
 std::atomic<uint32_t> g_slot_rr{0};
 
-int counter_slot(int dev, uint32_t** slot) {
+// The word after the slots is the device error word (bit 0: a staged copy
+// never completed).
+int scratch(int dev, uint32_t** base) {
   if (dev < 0 || dev >= 64) return WCOMP_EUNSUPPORTED;
-  {
-    std::lock_guard<std::mutex> g(g_scratch_mu);
-    if (!g_scratch[dev]) {
-      uint32_t* p = nullptr;
-      cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p), kSlots * 2 * sizeof(uint32_t));
-      if (e == cudaSuccess) e = cudaMemset(p, 0, kSlots * 2 * sizeof(uint32_t));
-      if (e != cudaSuccess) return map_cuda(e);
-      g_scratch[dev] = p;
-    }
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (!g_scratch[dev]) {
+    uint32_t* p = nullptr;
+    const size_t bytes = (kSlots * 2 + 32) * sizeof(uint32_t);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&p), bytes);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, bytes);
+    if (e != cudaSuccess) return map_cuda(e);
+    g_scratch[dev] = p;
   }
-  *slot = g_scratch[dev] + 2 * (g_slot_rr.fetch_add(1, std::memory_order_relaxed) % kSlots);
+  *base = g_scratch[dev];
+  return WCOMP_OK;
+}
+
+int counter_slot(int dev, uint32_t** slot) {
+  uint32_t* base = nullptr;
+  const int st = scratch(dev, &base);
+  if (st != WCOMP_OK) return st;
+  *slot = base + 2 * (g_slot_rr.fetch_add(1, std::memory_order_relaxed) % kSlots);
   return WCOMP_OK;
 }
 
@@ -418,14 +757,79 @@ int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   return map_cuda(cudaGetLastError());
 }
 
+#ifndef WCOMP_GEMV_TMA
+#define WCOMP_GEMV_TMA 1
+#endif
+
+constexpr uint32_t kStageBudget = 8800;  // shared-memory bytes of staged chunks per warp
+
+template <int SRC, int R>
+constexpr int stages() {
+  constexpr uint32_t st = (R * Geom<SRC>::row_bytes + 127) & ~127u;
+  return kStageBudget / st < 2 ? 2 : int(kStageBudget / st);
+}
+
+template <int SRC, int BT, int R, int MINB, int MODE = (BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0)>
+int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  constexpr int S = stages<SRC, R>();
+  constexpr uint32_t kStage = (R * Geom<SRC>::row_bytes + 127) & ~127u;
+  constexpr size_t smem = size_t(kWarps) * (S * kStage + S * 8 + 2 * S * 4);
+  uint32_t units = 0;
+  for (int j = 0; j < b.count; ++j) {
+    b.set_prefix[j] = units;
+    units += uint32_t(cdiv(uint64_t(Ns[j]), R));
+  }
+  b.set_prefix[b.count] = units;
+  uint32_t* base = nullptr;
+  int st = scratch(dev, &base);
+  if (st != WCOMP_OK) return st;
+  uint32_t* slot = nullptr;
+  if ((st = counter_slot(dev, &slot)) != WCOMP_OK) return st;
+  auto kern = gemv_tma_kernel<SRC, BT, R, MODE, S, MINB>;
+  static int per_sm_cache = 0;
+  if (!per_sm_cache) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm <= 0)
+      per_sm = 1;
+    per_sm_cache = per_sm;
+  }
+  kern<<<per_sm_cache * sms, kThreads, smem, s>>>(b, units, B, slot, base + 2 * kSlots);
+  count_launches(1);
+  return map_cuda(cudaGetLastError());
+}
+
+// Rows per unit and CTAs per SM for each batch size (build-time tunables).
+#ifndef WCOMP_GEMV_R2
+#define WCOMP_GEMV_R2 1
+#endif
+#ifndef WCOMP_GEMV_R4
+#define WCOMP_GEMV_R4 2
+#endif
+#ifndef WCOMP_GEMV_R8
+#define WCOMP_GEMV_R8 2
+#endif
+#ifndef WCOMP_GEMV_R16
+#define WCOMP_GEMV_R16 1
+#endif
+
 template <int SRC>
 int dispatch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  if (WCOMP_GEMV_TMA) {
+    switch (pow2_batch(B)) {
+      case 1: return launch_tma<SRC, 1, 1, 3>(b, Ns, B, dev, sms, s);
+      case 2: return launch_tma<SRC, 2, WCOMP_GEMV_R2, 3>(b, Ns, B, dev, sms, s);
+      case 4: return launch_tma<SRC, 4, WCOMP_GEMV_R4, SRC == kK15 ? 2 : 3>(b, Ns, B, dev, sms, s);
+      case 8: return launch_tma<SRC, 8, WCOMP_GEMV_R8, 1>(b, Ns, B, dev, sms, s);
+      default: return launch_tma<SRC, 16, WCOMP_GEMV_R16, 1>(b, Ns, B, dev, sms, s);
+    }
+  }
   switch (pow2_batch(B)) {
     case 1: return launch_vec<SRC, 1, 1, 3>(b, Ns, B, dev, sms, s);
-    case 2: return launch_vec<SRC, 2, 1, 3>(b, Ns, B, dev, sms, s);
-    case 4: return launch_vec<SRC, 4, 2, 2>(b, Ns, B, dev, sms, s);
-    case 8: return launch_vec<SRC, 8, 1, 2>(b, Ns, B, dev, sms, s);
-    default: return launch_vec<SRC, 16, 1, 1>(b, Ns, B, dev, sms, s);
+    case 2: return launch_vec<SRC, 2, WCOMP_GEMV_R2, 3>(b, Ns, B, dev, sms, s);
+    case 4: return launch_vec<SRC, 4, WCOMP_GEMV_R4, 2>(b, Ns, B, dev, sms, s);
+    case 8: return launch_vec<SRC, 8, WCOMP_GEMV_R8, 1>(b, Ns, B, dev, sms, s);
+    default: return launch_vec<SRC, 16, WCOMP_GEMV_R16, 1>(b, Ns, B, dev, sms, s);
   }
 }
 
@@ -543,6 +947,25 @@ int gemv_plain(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks, 
 }  // namespace wc
 
 using namespace wc;
+
+extern "C" int wcomp_device_check(void* stream) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  uint32_t* base = nullptr;
+  int st = scratch(dev, &base);
+  if (st != WCOMP_OK) return st;
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, base + 2 * kSlots, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return map_cuda(e);
+  if (word) {
+    cudaMemsetAsync(base + 2 * kSlots, 0, sizeof(uint32_t), s);
+    cudaStreamSynchronize(s);
+    return WCOMP_ETIMEOUT;
+  }
+  return WCOMP_OK;
+}
 
 extern "C" int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream) {
   if (!c || !d_x || !d_y) return WCOMP_EINVAL;

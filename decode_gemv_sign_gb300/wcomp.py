@@ -20,7 +20,7 @@ BYTESPLIT = 0
 K15 = 1
 SCHEMES = {"bytesplit": BYTESPLIT, "byte-split": BYTESPLIT, "k15": K15, BYTESPLIT: BYTESPLIT, K15: K15}
 
-OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED = 0, -1, -2, -3, -4, -5
+OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
 
 class WcompError(RuntimeError):
@@ -84,6 +84,8 @@ def lib():
     L.wcomp_strerror.argtypes = [ctypes.c_int]
     L.wcomp_strerror.restype = ctypes.c_char_p
     L.wcomp_version.argtypes = []
+    L.wcomp_device_check.argtypes = [P]
+    L.wcomp_device_check.restype = ctypes.c_int
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
     for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
@@ -321,6 +323,11 @@ def deserialize(data: bytes, stream=None) -> Container:
 
 def version() -> int:
     return lib().wcomp_version()
+
+
+def device_check(stream=None) -> None:
+    """Raise if a kernel on this device reported a timed-out wait (clears the report)."""
+    _check(lib().wcomp_device_check(P(_stream(stream))), "wcomp_device_check")
 
 
 def launch_count() -> int:

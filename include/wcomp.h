@@ -65,7 +65,8 @@ typedef enum {
   WCOMP_ENOMEM = -2,        /* device or host allocation failed */
   WCOMP_ECORRUPT = -3,      /* serialized container failed validation */
   WCOMP_ECUDA = -4,         /* a CUDA runtime call failed */
-  WCOMP_EUNSUPPORTED = -5   /* size outside the supported range */
+  WCOMP_EUNSUPPORTED = -5,  /* size outside the supported range */
+  WCOMP_ETIMEOUT = -6       /* a kernel's bounded wait on its own copies ran out */
 } wcomp_status;
 
 typedef struct wcomp_container wcomp_container;
@@ -168,6 +169,13 @@ WCOMP_API int wcomp_decode_batched(const wcomp_container* const* containers, uin
                          int count, void* stream);
 WCOMP_API int wcomp_gemv_batched(const wcomp_container* const* containers, const uint16_t* const* d_x,
                        int B, float* const* d_y, int count, void* stream);
+
+/*
+ * Report and clear the device error word of the current device: kernels
+ * whose bounded waits run out record it there and stop early instead of
+ * hanging.  Synchronizes `stream`.  Returns WCOMP_OK or WCOMP_ETIMEOUT.
+ */
+WCOMP_API int wcomp_device_check(void* stream);
 
 /* Describe a container (host-side, no device work). */
 WCOMP_API int wcomp_info(const wcomp_container* c, wcomp_info_t* info);
