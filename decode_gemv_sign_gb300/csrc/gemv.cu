@@ -45,6 +45,24 @@ constexpr int kSlots = 1024;  // work-counter slots per device (one per launch, 
 
 enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
+// Build-time choices: the staged (TMA) kernel or the register double-buffered
+// kernel, and the proxy fence before a stage is refilled.
+#ifndef WCOMP_GEMV_TMA
+#define WCOMP_GEMV_TMA 0
+#endif
+#ifndef WCOMP_GEMV_MODE1
+#define WCOMP_GEMV_MODE1 1
+#endif
+#ifndef WCOMP_GEMV_MINB1
+#define WCOMP_GEMV_MINB1 4
+#endif
+#ifndef WCOMP_GEMV_MINB1_K15
+#define WCOMP_GEMV_MINB1_K15 3
+#endif
+#ifndef WCOMP_GEMV_PROXY_FENCE
+#define WCOMP_GEMV_PROXY_FENCE 1
+#endif
+
 // FMA forms.  MODE 0 widens weights and x to fp32 and issues packed fp32x2
 // FMAs (x is widened once per unit of R rows).  MODE 1 feeds the BF16 halves
 // of the pair words straight into mixed-precision FMAs (bf16 x bf16 + fp32);
@@ -100,8 +118,13 @@ struct ChunkBuf {
   uint32_t v[16];
 };
 
+// Stream base pointers of one tensor, held in registers for a unit.
+struct Streams {
+  const uint8_t *codes, *raw, *pa, *pb, *pc;
+};
+
 template <int SRC, bool FULL>
-__device__ __forceinline__ void load_chunk(const TensorDesc& d, uint64_t e_base, uint32_t vmask, int lane,
+__device__ __forceinline__ void load_chunk(const Streams& d, uint64_t e_base, uint32_t vmask, int lane,
                                            ChunkBuf& b) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -158,7 +181,7 @@ __device__ __forceinline__ void slice_pairs(const RegTable& t, const ChunkBuf& b
 }
 
 template <int SRC, int BT, int R, int MODE, bool FULL>
-__device__ __forceinline__ void compute_chunk(const TensorDesc& d, const uint16_t* __restrict__ xc, int64_t K, int B,
+__device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t* __restrict__ xc, int64_t K, int B,
                                               const ChunkBuf (&buf)[R], const bool (&live)[R], uint32_t vmask,
                                               int lane, float2 (&acc)[R][BT]) {
 #pragma unroll
@@ -188,10 +211,10 @@ __device__ __forceinline__ void compute_chunk(const TensorDesc& d, const uint16_
     for (int j = 0; j < R; ++j) {
       if (!live[j]) continue;
       uint32_t w[4];
-      if (i == 0) slice_pairs<SRC, 0>(d.t, buf[j], lane, w);
-      else if (i == 1) slice_pairs<SRC, 1>(d.t, buf[j], lane, w);
-      else if (i == 2) slice_pairs<SRC, 2>(d.t, buf[j], lane, w);
-      else slice_pairs<SRC, 3>(d.t, buf[j], lane, w);
+      if (i == 0) slice_pairs<SRC, 0>(t, buf[j], lane, w);
+      else if (i == 1) slice_pairs<SRC, 1>(t, buf[j], lane, w);
+      else if (i == 2) slice_pairs<SRC, 2>(t, buf[j], lane, w);
+      else slice_pairs<SRC, 3>(t, buf[j], lane, w);
 #pragma unroll
       for (int b = 0; b < BT; ++b) {
 #pragma unroll
@@ -250,97 +273,142 @@ __device__ __forceinline__ uint32_t grab(uint32_t* slot, int lane) {
 // ---------------------------------------------------------------------------
 // The kernel (vector path: K % 32 == 0, aligned streams and x).
 // ---------------------------------------------------------------------------
-template <int SRC, int BT, int R, int MINB, int MODE>
+// One unit as the pipeline sees it.
+template <int R>
+struct UnitState {
+  int ti;
+  int64_t r0;
+  uint32_t nchunks, vlast;
+  bool last_full;
+  bool live[R];
+};
+
+template <int R>
+__device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int lane, UnitState<R>& st) {
+  st.ti = owner(p.set_prefix, p.count, u);
+  const TensorDesc& d = p.d[st.ti];
+  st.r0 = int64_t(u - p.set_prefix[st.ti]) * R;
+  st.nchunks = uint32_t(cdiv(uint64_t(d.K), kChunk));
+  const uint32_t krem = uint32_t(d.K - int64_t(st.nchunks - 1) * kChunk);
+  st.last_full = krem == kChunk;
+  st.vlast = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) st.vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
+#pragma unroll
+  for (int j = 0; j < R; ++j) st.live[j] = st.r0 + j < d.N;
+}
+
+template <int SRC, int R>
+__device__ __forceinline__ void load_unit_chunk(const GemvBatch& p, const UnitState<R>& st, uint32_t c, int lane,
+                                                ChunkBuf (&bb)[R]) {
+  const TensorDesc& d = p.d[st.ti];
+  const Streams ss{d.codes, d.raw, d.pa, d.pb, d.pc};
+  const bool full = c + 1 < st.nchunks || st.last_full;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (!st.live[j]) continue;
+    const uint64_t eb = uint64_t(st.r0 + j) * uint64_t(d.K) + uint64_t(c) * kChunk;
+    if (full) load_chunk<SRC, true>(ss, eb, 0xF, lane, bb[j]);
+    else load_chunk<SRC, false>(ss, eb, st.vlast, lane, bb[j]);
+  }
+}
+
+// The kernel (vector path: K % 32 == 0, aligned streams and x).  The warp
+// runs one continuous pipeline over (unit, chunk) items: while it computes an
+// item, the next item's loads are in flight, including across the boundary
+// between units, so no unit starts with an exposed load latency.
+template <int SRC, int BT, int R, int MINB, int MODE, int DEPTH>
 __global__ void __launch_bounds__(kThreads, MINB)
     gemv_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
   const int lane = threadIdx.x & 31;
   uint32_t u = grab(slot, lane);
-  while (u < total_units) {
-    const uint32_t u_next = grab(slot, lane);  // in flight while this unit runs
-    const int ti = owner(p.set_prefix, p.count, u);
-    const TensorDesc& d = p.d[ti];
-    const uint16_t* __restrict__ x = p.x[ti];
-    const int64_t r0 = int64_t(u - p.set_prefix[ti]) * R;
-    const int64_t K = d.K;
-    bool live[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) live[j] = r0 + j < d.N;
-    float2 acc[R][BT];
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
-
-    // valid slices of the last (partial) chunk: slice i of this lane ends by K
-    const uint32_t nchunks = uint32_t(cdiv(uint64_t(K), kChunk));
-    const uint32_t krem = uint32_t(K - int64_t(nchunks - 1) * kChunk);
-    uint32_t vlast = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
-    const bool last_full = krem == kChunk;
-
+  if (u < total_units) {
+    uint32_t u_next = grab(slot, lane);
+    UnitState<R> cur, nxt;
+    unit_state<R>(p, u, lane, cur);
+    // load cursor: the item after the one being computed
     ChunkBuf b0[R], b1[R];
-    auto load = [&](uint32_t c, ChunkBuf (&bb)[R]) {
-      const bool full = c + 1 < nchunks || last_full;
+    load_unit_chunk<SRC, R>(p, cur, 0, lane, b0);
+    float2 acc[R][BT];
+    uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
+    auto begin_unit = [&]() {
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        if (!live[j]) continue;
-        const uint64_t eb = uint64_t(r0 + j) * uint64_t(K) + uint64_t(c) * kChunk;
-        if (full) load_chunk<SRC, true>(d, eb, 0xF, lane, bb[j]);
-        else load_chunk<SRC, false>(d, eb, vlast, lane, bb[j]);
+      for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
+      if (SRC != kPlain) {
+        const TensorDesc& d = p.d[cur.ti];
+        const int64_t r_end = cur.r0 + R < d.N ? cur.r0 + R : d.N;
+        e_lo = d.row_index[cur.r0];
+        e_hi = d.row_index[r_end];
+        if (e_lo + lane < e_hi) {
+          p0 = d.esc_pos[e_lo + lane];
+          v0 = load_esc_val(d, e_lo + lane);
+        }
       }
+    };
+    auto end_unit = [&]() {
+      const TensorDesc& d = p.d[cur.ti];
+      const int64_t K = d.K;
+      float s[R][BT];
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) s[j][b] = acc[j][b].x + acc[j][b].y;
+      if (SRC != kPlain) {
+        const uint16_t* __restrict__ x = p.x[cur.ti];
+        for (uint32_t e = e_lo + lane; e < e_hi; e += 32) {
+          uint32_t pos = p0, val = v0;
+          if (e != e_lo + lane) {
+            pos = d.esc_pos[e];
+            val = load_esc_val(d, e);
+          }
+          const int64_t j = int64_t(pos / uint64_t(K)) - cur.r0;
+#pragma unroll
+          for (int jj = 0; jj < R; ++jj)
+            if (jj == j) add_escape<BT>(d, x, B, uint64_t(cur.r0 + jj) * uint64_t(K), pos, val, s[jj]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        if (cur.live[j]) warp_reduce_store<BT>(s[j], B, p.y[cur.ti], d.N, cur.r0 + j, lane);
     };
     auto compute = [&](uint32_t c, const ChunkBuf (&bb)[R]) {
-      const uint16_t* xc = x + uint64_t(c) * kChunk;
-      if (c + 1 < nchunks || last_full)
-        compute_chunk<SRC, BT, R, MODE, true>(d, xc, K, B, bb, live, 0xF, lane, acc);
+      const TensorDesc& d = p.d[cur.ti];
+      const uint16_t* xc = p.x[cur.ti] + uint64_t(c) * kChunk;
+      if (c + 1 < cur.nchunks || cur.last_full)
+        compute_chunk<SRC, BT, R, MODE, true>(d.t, xc, d.K, B, bb, cur.live, 0xF, lane, acc);
       else
-        compute_chunk<SRC, BT, R, MODE, false>(d, xc, K, B, bb, live, vlast, lane, acc);
+        compute_chunk<SRC, BT, R, MODE, false>(d.t, xc, d.K, B, bb, cur.live, cur.vlast, lane, acc);
     };
-    load(0, b0);
-    // escape slice of the unit: index now, first entries right after
-    uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
-    if (SRC != kPlain) {
-      const int64_t r_end = r0 + R < d.N ? r0 + R : d.N;
-      e_lo = d.row_index[r0];
-      e_hi = d.row_index[r_end];
-      if (e_lo + lane < e_hi) {
-        p0 = d.esc_pos[e_lo + lane];
-        v0 = load_esc_val(d, e_lo + lane);
+    begin_unit();
+    // position of the item held in the "current" buffer
+    uint32_t c = 0;
+    bool have_next_unit = u_next < total_units;
+    if (have_next_unit) unit_state<R>(p, u_next, lane, nxt);
+    // One step: request the item after (cur, c) into `ld`, compute (cur, c)
+    // from `cb`, then advance.  Returns false when nothing is left.
+    auto step = [&](ChunkBuf (&cb)[R], ChunkBuf (&ld)[R]) -> bool {
+      const bool last_of_unit = c + 1 == cur.nchunks;
+      if (!last_of_unit) load_unit_chunk<SRC, R>(p, cur, c + 1, lane, ld);
+      else if (have_next_unit) load_unit_chunk<SRC, R>(p, nxt, 0, lane, ld);
+      compute(c, cb);
+      if (!last_of_unit) {
+        ++c;
+        return true;
       }
+      end_unit();
+      if (!have_next_unit) return false;
+      cur = nxt;
+      c = 0;
+      begin_unit();
+      u_next = grab(slot, lane);
+      have_next_unit = u_next < total_units;
+      if (have_next_unit) unit_state<R>(p, u_next, lane, nxt);
+      return true;
+    };
+    while (step(b0, b1) && step(b1, b0)) {
     }
-    for (uint32_t c = 0; c < nchunks; c += 2) {
-      const bool more = c + 1 < nchunks;
-      if (more) load(c + 1, b1);
-      compute(c, b0);
-      if (!more) break;
-      if (c + 2 < nchunks) load(c + 2, b0);
-      compute(c + 1, b1);
-    }
-
-    float s[R][BT];
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) s[j][b] = acc[j][b].x + acc[j][b].y;
-    if (SRC != kPlain) {
-      // escapes of the unit, lane-strided; each goes to the row that holds it
-      for (uint32_t e = e_lo + lane; e < e_hi; e += 32) {
-        uint32_t pos = p0, val = v0;
-        if (e != e_lo + lane) {
-          pos = d.esc_pos[e];
-          val = load_esc_val(d, e);
-        }
-        const int64_t j = int64_t(pos / uint64_t(K)) - r0;
-#pragma unroll
-        for (int jj = 0; jj < R; ++jj)
-          if (jj == j) add_escape<BT>(d, x, B, uint64_t(r0 + jj) * uint64_t(K), pos, val, s[jj]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-      if (live[j]) warp_reduce_store<BT>(s[j], B, p.y[ti], d.N, r0 + j, lane);
-    u = u_next;
   }
   // The last warp to finish returns the counter slot to zero for the next launch.
   if (lane == 0) {
@@ -367,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // double buffering.  Waits are bounded: a stage that never completes sets the
 // device error word and the warp stops after draining its own copies.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls of try_wait before giving up (well over a second)
+constexpr uint32_t kWaitLimit = 1u << 27;  // polls before giving up (well over a second)
 
 template <int SRC>
 struct Geom {
@@ -468,7 +536,9 @@ __device__ __forceinline__ void issue_chunk(const GemvBatch& p, uint32_t u, uint
 #pragma unroll
     for (int q = 0; q < 4; ++q) bytes += sz[j][q];
   }
+#if WCOMP_GEMV_PROXY_FENCE
   fence_proxy_async();  // earlier generic reads of this stage come before the new async writes
+#endif
   mbar_expect_tx(bar, bytes);
 #pragma unroll
   for (int j = 0; j < R; ++j) {
@@ -496,8 +566,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
   __syncwarp();
 
-  // producer state (warp-uniform): next unit / chunk to request
+  // producer state (warp-uniform): next unit / chunk to request; the unit
+  // after it is grabbed one unit ahead so the atomic's latency stays hidden
   uint32_t pu = grab(slot, lane), pc = 0, pseq = 0;
+  uint32_t pu_next = grab(slot, lane);
   uint32_t issued = 0, consumed = 0;
   auto chunks_of = [&](uint32_t u) -> uint32_t {
     const int ti = owner(p.set_prefix, p.count, u);
@@ -523,9 +595,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
       if (lane == 0) issue_chunk<SRC, R>(p, pu, pc, ring + (issued % S) * kStage, &bars[issued % S]);
       ++issued;
       if (++pc == pn) {
-        pu = grab(slot, lane);
+        pu = pu_next;
         pc = 0;
         pn = pu < total_units ? chunks_of(pu) : 0;
+        if (pu < total_units) pu_next = grab(slot, lane);
       }
     }
     __syncwarp();
@@ -731,7 +804,9 @@ int counter_slot(int dev, uint32_t** slot) {
   return WCOMP_OK;
 }
 
-template <int SRC, int BT, int R, int MINB, int MODE = (BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0)>
+template <int SRC, int BT, int R, int MINB,
+          int MODE = (BT == 1 ? WCOMP_GEMV_MODE1 : BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0),
+          int DEPTH = 2>
 int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
   uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
@@ -745,21 +820,19 @@ int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   static int per_sm_cache = 0;
   if (!per_sm_cache) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE, DEPTH>, kThreads, 0) !=
             cudaSuccess ||
         per_sm <= 0)
       per_sm = 1;
     per_sm_cache = per_sm;
   }
   const int blocks = per_sm_cache * sms;
-  gemv_kernel<SRC, BT, R, MINB, MODE><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
+  gemv_kernel<SRC, BT, R, MINB, MODE, DEPTH><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }
 
-#ifndef WCOMP_GEMV_TMA
-#define WCOMP_GEMV_TMA 1
-#endif
+
 
 constexpr uint32_t kStageBudget = 8800;  // shared-memory bytes of staged chunks per warp
 
@@ -800,6 +873,9 @@ int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
 }
 
 // Rows per unit and CTAs per SM for each batch size (build-time tunables).
+#ifndef WCOMP_GEMV_R1
+#define WCOMP_GEMV_R1 1
+#endif
 #ifndef WCOMP_GEMV_R2
 #define WCOMP_GEMV_R2 1
 #endif
@@ -825,7 +901,7 @@ int dispatch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaS
     }
   }
   switch (pow2_batch(B)) {
-    case 1: return launch_vec<SRC, 1, 1, 3>(b, Ns, B, dev, sms, s);
+    case 1: return launch_vec<SRC, 1, WCOMP_GEMV_R1, SRC == kK15 ? WCOMP_GEMV_MINB1_K15 : WCOMP_GEMV_MINB1>(b, Ns, B, dev, sms, s);
     case 2: return launch_vec<SRC, 2, WCOMP_GEMV_R2, 3>(b, Ns, B, dev, sms, s);
     case 4: return launch_vec<SRC, 4, WCOMP_GEMV_R4, 2>(b, Ns, B, dev, sms, s);
     case 8: return launch_vec<SRC, 8, WCOMP_GEMV_R8, 1>(b, Ns, B, dev, sms, s);

@@ -360,11 +360,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase of the given parity; false if it did not complete
-// within `limit` polls (each poll suspends for a short, hardware-chosen time).
+// within `limit` polls.  Non-blocking polls (test_wait) keep the warp awake so
+// it resumes as soon as the bytes land; try_wait suspends the warp instead.
+#ifndef WCOMP_MBAR_SPIN
+#define WCOMP_MBAR_SPIN 1
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (WCOMP_MBAR_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   return false;
 }
 
