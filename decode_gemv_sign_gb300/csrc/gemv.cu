@@ -1065,3 +1065,104 @@ extern "C" int wcomp_gemv_bf16_batched(const uint16_t* const* d_w, const int64_t
   if (!d_w || !N || !K || !d_x || !d_y || count <= 0) return WCOMP_EINVAL;
   return gemv_plain(d_w, N, K, d_x, B, d_y, count, static_cast<cudaStream_t>(stream));
 }
+
+// ---------------------------------------------------------------------------
+// Fused GEMV that allocates nothing.
+//
+// wcomp_gemv takes its work counters from a device buffer that the library
+// allocates with cudaMalloc on first use.  Some callers cannot let a library
+// allocate device memory: a serving loop that fixed its memory budget up
+// front, or code that must not meet the implicit device synchronisation that
+// a first cudaMalloc (or any cudaFree) can bring.  wcomp_gemv_noalloc runs the
+// same kernel with its counters in the static device array below instead.
+// The array is part of the library image, so every GPU that loads the library
+// keeps it until the process exits.  Every call shares it.
+// ---------------------------------------------------------------------------
+namespace wc {
+namespace {
+
+constexpr int kNoAllocWords = 64;  // 256 bytes: [0] work counter, [1] completion counter, rest unused
+// A call may cover at most this many rows: the work counter runs past the
+// row count by one grab per warp of the grid and must stay within 32 bits.
+constexpr int64_t kNoAllocMaxRows = (int64_t(1) << 31) - (int64_t(1) << 20);
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the static array on device `dev` (which must be current).
+// The host-side name of the array is not a device address; the runtime gives
+// the real one, looked up once per device.
+int noalloc_scratch(int dev, uint32_t** out) {
+  if (dev < 0 || dev >= 64) return WCOMP_EUNSUPPORTED;
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return map_cuda(e);
+    g_noalloc_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return WCOMP_OK;
+}
+
+template <int SRC, int BT, int R, int MINB,
+          int MODE = (BT == 1 ? WCOMP_GEMV_MODE1 : BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0)>
+int launch_vec_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaStream_t s) {
+  b.set_prefix[0] = 0;
+  const uint32_t units = uint32_t(cdiv(uint64_t(N), R));
+  b.set_prefix[1] = units;
+  auto kern = gemv_kernel<SRC, BT, R, MINB, MODE, 2>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm <= 0)
+    per_sm = 1;
+  kern<<<per_sm * sms, kThreads, 0, s>>>(b, units, B, slot);
+  count_launches(1);
+  return map_cuda(cudaGetLastError());
+}
+
+template <int SRC>
+int dispatch_vec_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaStream_t s) {
+  switch (pow2_batch(B)) {
+    case 1: return launch_vec_on<SRC, 1, WCOMP_GEMV_R1, SRC == kK15 ? WCOMP_GEMV_MINB1_K15 : WCOMP_GEMV_MINB1>(
+        b, N, B, sms, slot, s);
+    case 2: return launch_vec_on<SRC, 2, WCOMP_GEMV_R2, 3>(b, N, B, sms, slot, s);
+    case 4: return launch_vec_on<SRC, 4, WCOMP_GEMV_R4, 2>(b, N, B, sms, slot, s);
+    case 8: return launch_vec_on<SRC, 8, WCOMP_GEMV_R8, 1>(b, N, B, sms, slot, s);
+    default: return launch_vec_on<SRC, 16, WCOMP_GEMV_R16, 1>(b, N, B, sms, slot, s);
+  }
+}
+
+}  // namespace
+}  // namespace wc
+
+extern "C" int wcomp_gemv_noalloc(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream) {
+  if (!c || !d_x || !d_y || B < 1 || B > 16) return WCOMP_EINVAL;
+  if (c->L.N > kNoAllocMaxRows) return WCOMP_EUNSUPPORTED;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  uint32_t* scratch = nullptr;
+  int st = noalloc_scratch(dev, &scratch);
+  if (st != WCOMP_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The counters must start at zero; a memset allocates nothing.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return map_cuda(e);
+  const int sms = sm_count(dev);
+  GemvBatch b;
+  memset(&b, 0, sizeof(b));
+  b.count = 1;
+  b.d[0] = make_desc(c);
+  b.x[0] = d_x;
+  b.y[0] = d_y;
+  const int64_t N = c->L.N;
+  const bool vec = c->L.K % kGroup == 0 && aligned16(d_x) && aligned32(c->d_main);
+  if (!vec) {
+    // the element path uses no scratch at all
+    return c->L.scheme == WCOMP_BYTESPLIT ? dispatch_generic<kBytesplit>(b, &N, B, sms, s)
+                                          : dispatch_generic<kK15>(b, &N, B, sms, s);
+  }
+  return c->L.scheme == WCOMP_BYTESPLIT ? dispatch_vec_on<kBytesplit>(b, N, B, sms, scratch, s)
+                                        : dispatch_vec_on<kK15>(b, N, B, sms, scratch, s);
+}

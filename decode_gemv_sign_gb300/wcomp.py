@@ -69,6 +69,7 @@ def lib():
                                        P, ctypes.POINTER(P)]
     L.wcomp_decode.argtypes = [P, P, P]
     L.wcomp_gemv.argtypes = [P, P, ctypes.c_int, P, P]
+    L.wcomp_gemv_noalloc.argtypes = [P, P, ctypes.c_int, P, P]
     L.wcomp_gemv_bf16.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int, P, P]
     L.wcomp_gemv_bf16_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(P), ctypes.c_int,
@@ -88,7 +89,8 @@ def lib():
     L.wcomp_device_check.restype = ctypes.c_int
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
-    for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
+    for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
+                 "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
                  "wcomp_decode_batched",
                  "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_version"):
         getattr(L, name).restype = ctypes.c_int
@@ -230,6 +232,26 @@ def gemv(c: Container, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream
     if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * inf["N"]:
         raise ValueError("y must be a contiguous float32 tensor of B*N elements")
     _check(lib().wcomp_gemv(P(c.handle), P(x.data_ptr()), B, P(y.data_ptr()), P(_stream(stream))), "wcomp_gemv")
+    return y
+
+
+def gemv_noalloc(c: Container, x: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
+    """wcomp_gemv without any device allocation by the library.
+
+    For callers that cannot let a library allocate device memory (a fixed
+    memory budget, or no implicit synchronisation from cudaMalloc / cudaFree).
+    ``y`` must be supplied by the caller.  Calls share one small static device
+    array: do not let two of them run at the same time on different streams.
+    """
+    x = _bits16(x, "x")
+    inf = c.info()
+    B = x.shape[0] if x.dim() == 2 else 1
+    if x.numel() != B * inf["K"]:
+        raise ValueError("x has the wrong size")
+    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * inf["N"]:
+        raise ValueError("y must be a contiguous float32 tensor of B*N elements")
+    _check(lib().wcomp_gemv_noalloc(P(c.handle), P(x.data_ptr()), B, P(y.data_ptr()), P(_stream(stream))),
+           "wcomp_gemv_noalloc")
     return y
 
 

@@ -141,6 +141,28 @@ WCOMP_API int wcomp_decode(const wcomp_container* c, uint16_t* d_out, void* stre
 WCOMP_API int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream);
 
 /*
+ * wcomp_gemv without any allocation.  The method on the pages has no
+ * counterpart to this entry point; it exists for callers that cannot let the
+ * library allocate device memory: a serving loop that fixed its memory budget
+ * up front, or code that must not meet the implicit device synchronisation a
+ * first cudaMalloc or any cudaFree can bring.  wcomp_gemv takes its work
+ * counters from a buffer it allocates on first use; this variant keeps them
+ * in a 256-byte static device array inside the library instead, which every
+ * GPU that loads the library holds until the process exits.
+ *   Arguments and results are those of wcomp_gemv.
+ *   The first call on a device looks up the array's device address (a
+ *   host-side runtime query, no allocation); make that first call before any
+ *   stream capture.
+ *   Every call shares the one array and zeroes its counters in stream order
+ *   before the kernel starts: calls whose kernels overlap on the GPU (on
+ *   different streams) race and must be ordered by the caller.
+ *   A call covers at most 2^31 - 2^20 rows (N); larger N returns
+ *   WCOMP_EUNSUPPORTED.  No cudaMalloc, cudaFree or other allocating routine
+ *   is called.
+ */
+WCOMP_API int wcomp_gemv_noalloc(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream);
+
+/*
  * Plain BF16 GEMV over an uncompressed W[N, K] with the same contract as
  * wcomp_gemv; the comparison kernel for the fused path ("0.733x the BF16 GEMV
  * time", forgeeks page, "Qué queda por demostrar").

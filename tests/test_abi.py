@@ -30,7 +30,8 @@ def declared():
 
 def test_header_declares_the_api():
     names = declared()
-    for n in ["wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
+    for n in ["wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
+              "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
               "wcomp_decode_batched", "wcomp_launch_count", "wcomp_device_check",
               "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_free",
               "wcomp_strerror", "wcomp_version"]:
