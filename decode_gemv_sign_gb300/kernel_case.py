@@ -28,7 +28,8 @@ def main():
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["encode", "decode", "gemv", "gemv_bf16"], required=True)
-    ap.add_argument("--scheme", choices=["bytesplit", "k15"], default="bytesplit")
+    ap.add_argument("--scheme", choices=["bytesplit", "k15", "both"], default="bytesplit",
+                    help="both: every tensor in both schemes, one batch (the benchmark's decode launch)")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--tensors", type=int, default=7)
     ap.add_argument("--reps", type=int, default=3)
@@ -37,14 +38,19 @@ def main():
     dev = torch.device("cuda")
     specs = synth.workload_dense_layers()[: a.tensors]
     ws = [synth.gen_weights_torch(s, dev) for s in specs]
-    scheme = W.SCHEMES[a.scheme]
+    if a.scheme == "both":
+        specs = [s for s in specs for _ in (0, 1)]
+        ws = [w for w in ws for _ in (0, 1)]
+        schemes = [0, 1] * (len(ws) // 2)
+    else:
+        schemes = [W.SCHEMES[a.scheme]] * len(ws)
     if a.op == "encode":
         for _ in range(a.reps):
-            for c in W.encode_batched(ws, scheme):
+            for c in W.encode_batched(ws, schemes):
                 c.free()
         torch.cuda.synchronize()
         return
-    cs = W.encode_batched(ws, scheme)
+    cs = W.encode_batched(ws, schemes)
     xs = [synth.gen_x_torch(a.batch, s.K, 5 + i, dev) for i, s in enumerate(specs)]
     outs = [torch.empty_like(w) for w in ws]
     for _ in range(a.reps):
