@@ -1,7 +1,7 @@
 // Encoder: histogram -> top-15 table -> pack codes and raw bits -> tile scan
 // -> escape compaction -> row index, for one tensor or a batch of tensors.
-// All steps run on the GPU; the host reads back the escape counts once per
-// batch to size the escape streams.
+// All steps run on the GPU; the host reads back the tables and escape counts
+// once per batch (right after the table selection) to size the escape streams.
 //
 // Method: forgeeks page "Prueba de GLM-5.2 reduce la memoria BF16 en casi un
 // 25%", section "Cómo funciona la compresión" (frequent sign+exponent symbols
@@ -10,7 +10,9 @@
 //
 // Every kernel takes the whole batch as a parameter-space descriptor array
 // and finds its tensor from a prefix over blocks, tiles or rows, so a batch
-// costs about a dozen launches and one host synchronization.
+// costs about a dozen launches and one host synchronization.  The pack pass
+// stashes each tile's escapes while it holds the source words, so the
+// compaction pass only moves E entries instead of reading the source again.
 #include <string.h>
 
 #include <algorithm>
@@ -34,6 +36,9 @@ struct EncDesc {
   uint8_t* main;
   uint8_t* esc;
   Summary* summary;
+  uint32_t* stash_pos;  // per tile: up to stash_cap escapes found by pack, in tile order
+  uint16_t* stash_val;
+  uint32_t stash_cap;
   uint64_t n;
   int64_t N, K;
   uint64_t E;
@@ -122,6 +127,7 @@ __global__ void __launch_bounds__(256) hist_kernel(const __grid_constant__ EncBa
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(512) select_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t cnt[kMaxBins];
+  __shared__ unsigned long long coded;
   const EncDesc& d = bt.d[blockIdx.x];
   const int nb = d.scheme == WCOMP_BYTESPLIT ? 256 : 512;
   const uint32_t* hist = reinterpret_cast<const uint32_t*>(d.main + d.off_scratch + Scratch::hist);
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(512) select_kernel(const __grid_constant__ Enc
   const int i = threadIdx.x;
   if (i < nb) cnt[i] = hist[i];
   if (i < 16) d.summary->table[i] = 0;
+  if (i == 0) coded = 0;
   __syncthreads();
   if (i < nb) {
     const uint32_t ci = cnt[i];
@@ -138,22 +145,16 @@ __global__ void __launch_bounds__(512) select_kernel(const __grid_constant__ Enc
       rank += (cj > ci) || (cj == ci && j < i);
     }
     lut[i] = rank < kTableSize ? uint8_t(rank) : uint8_t(kEscape);
-    if (rank < kTableSize) d.summary->table[rank] = uint16_t(i);
+    if (rank < kTableSize) {
+      d.summary->table[rank] = uint16_t(i);
+      atomicAdd(&coded, (unsigned long long)ci);
+    }
   }
-}
-
-__device__ __forceinline__ uint32_t block_sum_256(uint32_t v, uint32_t* sm) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
   __syncthreads();
-  uint32_t t = 0;
-  if (threadIdx.x == 0)
-    for (int k = 0; k < kThreads / 32; ++k) t += sm[k];
-  return t;  // valid in thread 0
+  if (i == 0) d.summary->E = uint32_t(d.n - coded);  // every symbol outside the table escapes
 }
 
-// Exclusive prefix of v over the 256 threads of the block.
+// Exclusive prefix of v over the 256 threads of the block (sm: 8 words).
 __device__ __forceinline__ uint32_t block_exclusive_256(uint32_t v, uint32_t* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = v;
@@ -167,6 +168,12 @@ __device__ __forceinline__ uint32_t block_exclusive_256(uint32_t v, uint32_t* sm
   uint32_t before = 0;
   for (int k = 0; k < warp; ++k) before += sm[k];
   return before + inc - v;
+}
+
+__device__ __forceinline__ uint32_t block_total_256(const uint32_t* sm) {
+  uint32_t t = 0;
+  for (int k = 0; k < kThreads / 32; ++k) t += sm[k];
+  return t;
 }
 
 // ---------------------------------------------------------------------------
@@ -190,9 +197,10 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
   const uint64_t G = cdiv(n, kGroup);
   const uint64_t g = uint64_t(tile) * kThreads + threadIdx.x;
   uint32_t esc = 0;
+  uint32_t wv[16];
+  uint32_t cw[4] = {0, 0, 0, 0};
   if (g < G) {
     const uint64_t base = g * kGroup;
-    uint32_t wv[16];
     if (d.aligned && base + kGroup <= n) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -207,7 +215,6 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
         wv[k] = lo | (hi << 16);
       }
     }
-    uint32_t cw[4] = {0, 0, 0, 0};
     uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint32_t a[4] = {0, 0, 0, 0}, b[2] = {0, 0}, c = 0;
 #pragma unroll
@@ -239,8 +246,24 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
       *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;
     }
   }
-  const uint32_t total = block_sum_256(esc, red);
+  // rank the escapes inside the tile; while the source words are still in
+  // registers, stash (position, value) for the gather pass
+  const uint32_t before = block_exclusive_256(esc, red);
+  const uint32_t total = block_total_256(red);
   if (threadIdx.x == 0) reinterpret_cast<uint32_t*>(d.main + d.off_tile)[tile] = total;
+  if (esc && total <= d.stash_cap) {
+    uint64_t o = uint64_t(tile) * d.stash_cap + before;
+    const uint64_t base = g * kGroup;
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) {
+      if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape && base + e < n) {
+        const uint32_t v = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFF;
+        d.stash_pos[o] = uint32_t(base + e);
+        d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
+        ++o;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -272,16 +295,16 @@ __global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncB
     idx[i] = run;
     run += v;
   }
-  if (threadIdx.x == 1023) {
-    idx[n_tiles] = part[1023];
-    d.summary->E = part[1023];
-  }
+  if (threadIdx.x == 1023) idx[n_tiles] = part[1023];
 }
 
 // ---------------------------------------------------------------------------
-// a4: escape compaction.  Thread j of a tile re-reads the 32 codes of its
-// group, ranks its escapes inside the tile with a block scan and writes
-// (position, value) pairs in ascending position order.
+// a4: escape compaction.  A tile whose escapes fit its stash copies them to
+// their final place (tile_index[t] onwards).  A tile with more escapes than
+// the stash holds is ranked again here: thread j re-reads the 32 codes of its
+// group, a block scan gives each escape its place, and the values are read
+// back from the source.  Either way the stream ends up in ascending position
+// order.
 // ---------------------------------------------------------------------------
 template <int SCHEME>
 __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant__ EncBatch bt) {
@@ -290,7 +313,21 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
   const EncDesc& d = bt.d[ti];
   const uint32_t t = blockIdx.x - bt.prefix[ti];
   const uint32_t* tile_index = reinterpret_cast<const uint32_t*>(d.main + d.off_tile);
-  if (tile_index[t + 1] == tile_index[t]) return;  // uniform: no escapes in this tile
+  const uint32_t first = tile_index[t], count = tile_index[t + 1] - first;
+  if (count == 0) return;  // uniform
+  if (count <= d.stash_cap) {
+    uint32_t* pos = reinterpret_cast<uint32_t*>(d.esc + d.off_pos);
+    uint8_t* val = d.esc + d.off_val;
+    for (uint32_t i = threadIdx.x; i < count; i += kThreads) {
+      const uint64_t s = uint64_t(t) * d.stash_cap + i;
+      pos[first + i] = d.stash_pos[s];
+      if (SCHEME == WCOMP_BYTESPLIT)
+        val[first + i] = uint8_t(d.stash_val[s]);
+      else
+        reinterpret_cast<uint16_t*>(val)[first + i] = d.stash_val[s];
+    }
+    return;
+  }
   const uint64_t G = cdiv(d.n, kGroup);
   const uint64_t g = uint64_t(t) * kThreads + threadIdx.x;
   uint4 c4 = make_uint4(0, 0, 0, 0);
@@ -430,11 +467,16 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     z.p[z.count] = c->d_main + L.off_scratch + Scratch::hist;
     z.len[z.count] = kMaxBins * sizeof(uint32_t);
     ++z.count;
+    // every section's padding up to its 32-byte boundary (pack's whole-group
+    // stores cover only part of it for codes, raw bytes and plane A)
+    add_pad(z, c->d_main, L.off_codes, L.sz_codes);
+    add_pad(z, c->d_main, L.off_raw, L.sz_raw);
+    add_pad(z, c->d_main, L.off_a, L.sz_a);
     add_pad(z, c->d_main, L.off_b, L.sz_b);
     add_pad(z, c->d_main, L.off_c, L.sz_c);
     add_pad(z, c->d_main, L.off_tile, L.sz_tile);
     add_pad(z, c->d_main, L.off_row, L.sz_row);
-    if (z.count + 5 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+    if (z.count + 8 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
   }
   if ((e = launch_zero(z, s)) != cudaSuccess) return fail(e);
 
@@ -469,25 +511,9 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   };
   if ((e = hist_launch(WCOMP_BYTESPLIT)) != cudaSuccess) return fail(e);
   if ((e = hist_launch(WCOMP_K15)) != cudaSuccess) return fail(e);
-  // a2: tables
+  // a2: tables, and E from the histogram (n minus the table symbols' counts)
   e = for_chunks(jobs, -1, [&](EncBatch& b) {
     select_kernel<<<b.count, 512, 0, s>>>(b);
-    count_launches(1);
-  });
-  if (e != cudaSuccess) return fail(e);
-  // a3: pack, then the tile scan
-  e = for_chunks(jobs, WCOMP_BYTESPLIT, [&](EncBatch& b) {
-    pack_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
-    count_launches(1);
-  });
-  if (e != cudaSuccess) return fail(e);
-  e = for_chunks(jobs, WCOMP_K15, [&](EncBatch& b) {
-    pack_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
-    count_launches(1);
-  });
-  if (e != cudaSuccess) return fail(e);
-  e = for_chunks(jobs, -1, [&](EncBatch& b) {
-    scan_kernel<<<b.count, 1024, 0, s>>>(b);
     count_launches(1);
   });
   if (e != cudaSuccess) return fail(e);
@@ -500,6 +526,10 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   cudaFreeAsync(d_sum, s);
   d_sum = nullptr;
 
+  // escape streams and the per-tile stash, sized from E: room for twice the
+  // mean escapes per tile plus 64 (a tile that overflows is ranked again)
+  uint64_t stash_entries = 0;
+  std::vector<uint64_t> stash_off(count, 0);
   for (int i = 0; i < count; ++i) {
     wcomp_container* c = jobs[i].c;
     memcpy(c->table, hs[i].table, sizeof(c->table));
@@ -509,6 +539,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     d.E = L.E;
     d.off_pos = L.off_pos;
     d.off_val = L.off_val;
+    d.stash_cap = 0;
     if (L.E) {
       e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
       if (e != cudaSuccess) return fail(e);
@@ -516,9 +547,42 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
       add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
       add_pad(z, c->d_esc, L.off_val, L.sz_val);
       if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+      const uint64_t mean = cdiv(L.E, L.n_tiles);
+      d.stash_cap = uint32_t(std::min<uint64_t>(kTile, (2 * mean + 64 + 31) & ~uint64_t(31)));
+      stash_off[i] = stash_entries;
+      stash_entries += uint64_t(d.stash_cap) * L.n_tiles;
     }
   }
-  if ((e = launch_zero(z, s)) != cudaSuccess) return fail(e);
+  uint8_t* stash = nullptr;
+  if (stash_entries) {
+    e = cudaMallocAsync(reinterpret_cast<void**>(&stash), stash_entries * 6, s);
+    if (e != cudaSuccess) return fail(e);
+    for (int i = 0; i < count; ++i) {
+      jobs[i].d.stash_pos = reinterpret_cast<uint32_t*>(stash) + stash_off[i];
+      jobs[i].d.stash_val = reinterpret_cast<uint16_t*>(stash + 4 * stash_entries) + stash_off[i];
+    }
+  }
+  auto fail2 = [&](cudaError_t err) -> int {
+    if (stash) cudaFreeAsync(stash, s);
+    return fail(err);
+  };
+  if ((e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
+  // a3: pack (with the stash), then the tile scan
+  e = for_chunks(jobs, WCOMP_BYTESPLIT, [&](EncBatch& b) {
+    pack_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail2(e);
+  e = for_chunks(jobs, WCOMP_K15, [&](EncBatch& b) {
+    pack_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail2(e);
+  e = for_chunks(jobs, -1, [&](EncBatch& b) {
+    scan_kernel<<<b.count, 1024, 0, s>>>(b);
+    count_launches(1);
+  });
+  if (e != cudaSuccess) return fail2(e);
   // a4: compaction for tensors with escapes; row indexes for all
   std::vector<Job> with_esc;
   for (auto& j : jobs)
@@ -527,12 +591,12 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     compact_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail(e);
+  if (e != cudaSuccess) return fail2(e);
   e = for_chunks(with_esc, WCOMP_K15, [&](EncBatch& b) {
     compact_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail(e);
+  if (e != cudaSuccess) return fail2(e);
   e = for_chunks(jobs, -1, [&](EncBatch& b) {
     uint32_t rows = 0;
     for (int j = 0; j < b.count; ++j) {
@@ -543,7 +607,8 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     row_index_kernel<<<unsigned(cdiv(rows, 256)), 256, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail(e);
+  if (e != cudaSuccess) return fail2(e);
+  if (stash) cudaFreeAsync(stash, s);
   for (int i = 0; i < count; ++i) out[i] = jobs[i].c;
   return WCOMP_OK;
 }
