@@ -20,6 +20,32 @@ int map_cuda(cudaError_t e) {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!pools[dev]) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t pool;
+      e = cudaMemPoolCreate(&pool, &props);
+      if (e != cudaSuccess) return e;
+      uint64_t keep = ~uint64_t(0);
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      pools[dev] = pool;
+    }
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pools[dev], s);
+}
+
 int sm_count(int device) {
   static std::mutex mu;
   static int cache[64] = {0};
@@ -211,8 +237,8 @@ extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* strea
   memcpy(c->table, table, sizeof(table));
   cudaGetDevice(&c->device);
   const uint8_t* p = static_cast<const uint8_t*>(host_buf) + kHeaderBytes;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
-  if (e == cudaSuccess && L.esc_payload) e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+  cudaError_t e = pool_alloc(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
+  if (e == cudaSuccess && L.esc_payload) e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_main, p, L.main_payload, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && L.esc_payload)
     e = cudaMemcpyAsync(c->d_esc, p + L.main_payload, L.esc_payload, cudaMemcpyHostToDevice, s);

@@ -190,15 +190,14 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
   const int ti = find_owner(bt, blockIdx.x);
   const EncDesc& d = bt.d[ti];
   const uint32_t tile = blockIdx.x - bt.prefix[ti];
-  const uint8_t* lut_g = d.main + d.off_scratch + Scratch::lut;
-  for (int i = threadIdx.x; i < NB; i += blockDim.x) lut[i] = lut_g[i];
-  __syncthreads();
   const uint64_t n = d.n;
   const uint64_t G = cdiv(n, kGroup);
   const uint64_t g = uint64_t(tile) * kThreads + threadIdx.x;
   uint32_t esc = 0;
   uint32_t wv[16];
   uint32_t cw[4] = {0, 0, 0, 0};
+  // the source words are requested first, so their latency overlaps the
+  // table's trip through shared memory
   if (g < G) {
     const uint64_t base = g * kGroup;
     if (d.aligned && base + kGroup <= n) {
@@ -215,6 +214,12 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
         wv[k] = lo | (hi << 16);
       }
     }
+  }
+  const uint8_t* lut_g = d.main + d.off_scratch + Scratch::lut;
+  for (int i = threadIdx.x; i < NB; i += blockDim.x) lut[i] = lut_g[i];
+  __syncthreads();
+  if (g < G) {
+    const uint64_t base = g * kGroup;
     uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint32_t a[4] = {0, 0, 0, 0}, b[2] = {0, 0}, c = 0;
 #pragma unroll
@@ -438,7 +443,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     if (d_sum) cudaFreeAsync(d_sum, s);
     return map_cuda(err);
   };
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d_sum), sizeof(Summary) * count, s);
+  cudaError_t e = pool_alloc(reinterpret_cast<void**>(&d_sum), sizeof(Summary) * count, s);
   if (e != cudaSuccess) return map_cuda(e);
   ZeroList z;
   memset(&z, 0, sizeof(z));
@@ -449,7 +454,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     c->device = dev;
     Layout& L = c->L;
     L.compute(schemes[i], Ns[i], Ks[i], 0);
-    e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
+    e = pool_alloc(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
     if (e != cudaSuccess) return fail(e);
     EncDesc& d = jobs[i].d;
     memset(&d, 0, sizeof(d));
@@ -541,7 +546,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     d.off_val = L.off_val;
     d.stash_cap = 0;
     if (L.E) {
-      e = cudaMallocAsync(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+      e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
       if (e != cudaSuccess) return fail(e);
       d.esc = c->d_esc;
       add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
@@ -555,7 +560,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   }
   uint8_t* stash = nullptr;
   if (stash_entries) {
-    e = cudaMallocAsync(reinterpret_cast<void**>(&stash), stash_entries * 6, s);
+    e = pool_alloc(reinterpret_cast<void**>(&stash), stash_entries * 6, s);
     if (e != cudaSuccess) return fail(e);
     for (int i = 0; i < count; ++i) {
       jobs[i].d.stash_pos = reinterpret_cast<uint32_t*>(stash) + stash_off[i];

@@ -382,6 +382,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // Host-side launch helpers (defined in container.cu).
+// Stream-ordered allocation from the library's own memory pool on the current
+// device (created on first use; it keeps freed blocks for reuse instead of
+// returning them to the driver at every synchronization).
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s);
 int sm_count(int device);
 int map_cuda(cudaError_t e);
 void count_launches(uint64_t k);

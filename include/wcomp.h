@@ -37,7 +37,9 @@
  *     what it allocated.
  *   - Containers are opaque, owned by the library, and released with
  *     wcomp_free.  A container lives on the device that was current when it
- *     was made.
+ *     was made.  Container memory comes from a stream-ordered memory pool the
+ *     library creates per device; freed blocks stay in that pool for reuse
+ *     until the process exits.
  */
 #ifndef WCOMP_H
 #define WCOMP_H
