@@ -53,6 +53,7 @@ enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 #ifndef WCOMP_GEMV_MODE1
 #define WCOMP_GEMV_MODE1 1
 #endif
+
 #ifndef WCOMP_GEMV_MINB1
 #define WCOMP_GEMV_MINB1 4
 #endif
