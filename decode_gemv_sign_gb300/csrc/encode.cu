@@ -36,6 +36,7 @@ struct EncDesc {
   uint8_t* main;
   uint8_t* esc;
   Summary* summary;
+  const uint32_t* hist_k15;  // byte-split job whose K15 twin is in the batch: fold that histogram
   uint32_t* stash_pos;  // per tile: up to stash_cap escapes found by pack, in tile order
   uint16_t* stash_val;
   uint32_t stash_cap;
@@ -133,7 +134,10 @@ __global__ void __launch_bounds__(512) select_kernel(const __grid_constant__ Enc
   const uint32_t* hist = reinterpret_cast<const uint32_t*>(d.main + d.off_scratch + Scratch::hist);
   uint8_t* lut = d.main + d.off_scratch + Scratch::lut;
   const int i = threadIdx.x;
-  if (i < nb) cnt[i] = hist[i];
+  if (i < nb) {
+    // a byte-split symbol is a K15 symbol without its exponent LSB: bins 2s and 2s+1 fold into s
+    cnt[i] = d.hist_k15 ? d.hist_k15[2 * i] + d.hist_k15[2 * i + 1] : hist[i];
+  }
   if (i < 16) d.summary->table[i] = 0;
   if (i == 0) coded = 0;
   __syncthreads();
@@ -486,10 +490,25 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   if ((e = launch_zero(z, s)) != cudaSuccess) return fail(e);
 
   // a1: histogram blocks in proportion to size, at most 8191 elements per thread
+  // A byte-split job whose tensor is also encoded as K15 in this batch takes
+  // its histogram from the K15 one instead of reading the source again.
+  for (auto& j : jobs) j.d.hist_k15 = nullptr;
+  for (auto& j : jobs) {
+    if (j.d.scheme != WCOMP_BYTESPLIT) continue;
+    for (auto& k : jobs)
+      if (k.d.scheme == WCOMP_K15 && k.d.w == j.d.w && k.d.N == j.d.N && k.d.K == j.d.K) {
+        j.d.hist_k15 = reinterpret_cast<const uint32_t*>(k.d.main + k.d.off_scratch + Scratch::hist);
+        break;
+      }
+  }
+  std::vector<Job> need_hist;
+  for (auto& j : jobs)
+    if (!j.d.hist_k15) need_hist.push_back(j);
   uint64_t total_n = 0;
-  for (auto& j : jobs) total_n += j.d.n;
+  for (auto& j : jobs)
+    if (!j.d.hist_k15) total_n += j.d.n;
   auto hist_launch = [&](int scheme) {
-    return for_chunks(jobs, scheme, [&](EncBatch& b) {
+    return for_chunks(need_hist, scheme, [&](EncBatch& b) {
       uint32_t blocks = 0;
       for (int j = 0; j < b.count; ++j) {
         b.prefix[j] = blocks;

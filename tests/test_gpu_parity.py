@@ -209,6 +209,23 @@ def test_encode_batched_matches_single(W):
         assert np.array_equal(host(W.decode(c)).reshape(w.shape), w)
 
 
+def test_encode_batched_both_schemes_of_one_tensor(W):
+    # the byte-split job folds the K15 histogram of the same tensor
+    specs = [synth.WeightSpec(f"t{i}", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=1200 + i)
+             for i, (N, K) in enumerate([(64, 1024), (3, 40000), (7, 301), (1, 31)])]
+    ws = [synth.gen_weights_np(s) for s in specs]
+    wd = [dev(w) for w in ws]
+    cs = W.encode_batched([w for w in wd for _ in (0, 1)], [1, 0] * len(wd))
+    for i, w in enumerate(ws):
+        assert W.serialize(cs[2 * i]) == O.serialize(O.encode(w, 1))
+        assert W.serialize(cs[2 * i + 1]) == O.serialize(O.encode(w, 0))
+    w65 = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    d65 = dev(w65)
+    c0, c1 = W.encode_batched([d65, d65], [0, 1])
+    assert W.serialize(c0) == O.serialize(O.encode(w65, 0))
+    assert W.serialize(c1) == O.serialize(O.encode(w65, 1))
+
+
 def test_many_tensors_batch_over_limit(W):
     # more containers than one launch carries
     ws = [synth.gen_weights_np(synth.WeightSpec(f"m{i}", 16, 512, "normal", 0.02, 0.01, "normal", 1.0, seed=600 + i))
