@@ -23,10 +23,11 @@
 //
 // Escapes.  An escaped weight decodes to the placeholder (symbol 0, so
 // |w| < 2^-125).  Each lane adds x * (w_true - w_placeholder) for a share of
-// the unit's escapes, found in O(1) through the row index; their positions
-// and values are requested before the main loop so the loads overlap it.
-// Lanes are combined with a fixed butterfly: results do not depend on which
-// warp ran which unit.
+// the unit's escapes, found in O(1) through the row index; the first 32
+// positions and values are requested when the unit starts, so those loads
+// overlap its chunks, and the corrections are added when it ends.  Lanes are
+// combined with a fixed butterfly: results do not depend on which warp ran
+// which unit.
 #include <string.h>
 
 #include <algorithm>
@@ -93,9 +94,41 @@ __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
   return v;
 }
 
-// Find the tensor that owns global unit `u`.
-__device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t u) {
-  int i = 0;
+// Loads at a base address plus a compile-time byte offset: the offset goes
+// into the instruction, so the slices of a chunk share one address register.
+template <int OFF>
+__device__ __forceinline__ uint32_t ld_stream_u32_at(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1+%2];" : "=r"(v) : "l"(p), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 ld_stream_v2_at(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "l"(p), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld_stream_v4_at(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld_x_v4_at(const uint16_t* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::evict_last.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "n"(OFF));
+  return v;
+}
+
+// Find the tensor that owns global unit `u`, searching from tensor `start`
+// (a warp's units only increase, so its previous owner is a lower bound).
+__device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t u, int start = 0) {
+  int i = start;
   while (i + 1 < count && prefix[i + 1] <= u) ++i;
   return i;
 }
@@ -124,30 +157,86 @@ struct Streams {
   const uint8_t *codes, *raw, *pa, *pb, *pc;
 };
 
-template <int SRC, bool FULL>
+// Slice I of one row's chunk; `q` holds the lane's stream addresses for
+// slice 0 (chunk_ptrs), the slice offsets are immediates.
+struct ChunkPtrs {
+  const uint8_t *c, *r, *a, *b, *cc;
+};
+
+// e_base is the chunk's first element; it is a multiple of 32 (K % 32 == 0).
+template <int SRC>
+__device__ __forceinline__ ChunkPtrs chunk_ptrs(const Streams& d, uint64_t e_base, int lane) {
+  ChunkPtrs q{};
+  if (SRC == kBytesplit) {
+    q.c = d.codes + (e_base >> 1) + 4 * lane;
+    q.r = d.raw + e_base + 8 * lane;
+  } else if (SRC == kK15) {
+    // group g = e >> 5 of element e = e_base + 256 i + 8 lane; the lane reads
+    // quads 2 (lane & 3), +1: plane A word 16 g + 4 (lane & 3), plane B word
+    // 8 g + 4 ((lane >> 1) & 1), plane C word 4 g
+    q.c = d.codes + (e_base >> 1) + 4 * lane;
+    q.a = d.pa + (e_base >> 1) + 4 * lane;
+    q.b = d.pb + (e_base >> 2) + 8 * (lane >> 2) + 4 * ((lane >> 1) & 1);
+    q.cc = d.pc + (e_base >> 3) + 4 * (lane >> 2);
+  } else {
+    q.r = d.raw + 2 * e_base + 16 * lane;
+  }
+  return q;
+}
+
+template <int SRC, int I>
+__device__ __forceinline__ void load_slice(const ChunkPtrs& q, ChunkBuf& b) {
+  if (SRC == kBytesplit) {
+    b.v[I] = ld_stream_u32_at<128 * I>(q.c);
+    const uint2 r = ld_stream_v2_at<256 * I>(q.r);
+    b.v[4 + 2 * I] = r.x;
+    b.v[5 + 2 * I] = r.y;
+  } else if (SRC == kK15) {
+    b.v[I] = ld_stream_u32_at<128 * I>(q.c);
+    b.v[4 + I] = ld_stream_u32_at<128 * I>(q.a);
+    b.v[8 + I] = ld_stream_u32_at<64 * I>(q.b);
+    b.v[12 + I] = ld_stream_u32_at<32 * I>(q.cc);
+  } else {
+    const uint4 w = ld_stream_v4_at<512 * I>(q.r);
+    b.v[4 * I + 0] = w.x; b.v[4 * I + 1] = w.y; b.v[4 * I + 2] = w.z; b.v[4 * I + 3] = w.w;
+  }
+}
+
+// ADDR 1: per-chunk base addresses with immediate slice offsets; ADDR 0: the
+// address of every slice computed on its own (fewer live registers, which
+// some instantiations schedule better).
+template <int SRC, bool FULL, int ADDR>
 __device__ __forceinline__ void load_chunk(const Streams& d, uint64_t e_base, uint32_t vmask, int lane,
                                            ChunkBuf& b) {
+  if (ADDR == 0) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (!FULL && !((vmask >> i) & 1)) continue;
-    const uint64_t e = e_base + kSlice * i + 8 * lane;
-    if (SRC == kBytesplit) {
-      b.v[i] = ld_stream_u32(d.codes + (e >> 1));
-      const uint2 r = ld_stream_v2(d.raw + e);
-      b.v[4 + 2 * i] = r.x;
-      b.v[5 + 2 * i] = r.y;
-    } else if (SRC == kK15) {
-      const uint64_t g = e >> 5;
-      const uint32_t q2 = lane & 3;  // which 8 elements of the 32-element group
-      b.v[i] = ld_stream_u32(d.codes + (e >> 1));
-      b.v[4 + i] = ld_stream_u32(d.pa + 16 * g + 4 * q2);
-      b.v[8 + i] = ld_stream_u32(d.pb + 8 * g + 4 * (q2 >> 1));
-      b.v[12 + i] = ld_stream_u32(d.pc + 4 * g);
-    } else {
-      const uint4 w = ld_stream_v4(d.raw + 2 * e);
-      b.v[4 * i + 0] = w.x; b.v[4 * i + 1] = w.y; b.v[4 * i + 2] = w.z; b.v[4 * i + 3] = w.w;
+    for (int i = 0; i < 4; ++i) {
+      if (!FULL && !((vmask >> i) & 1)) continue;
+      const uint64_t e = e_base + kSlice * i + 8 * lane;
+      if (SRC == kBytesplit) {
+        b.v[i] = ld_stream_u32(d.codes + (e >> 1));
+        const uint2 r = ld_stream_v2(d.raw + e);
+        b.v[4 + 2 * i] = r.x;
+        b.v[5 + 2 * i] = r.y;
+      } else if (SRC == kK15) {
+        const uint64_t g = e >> 5;
+        const uint32_t q2 = lane & 3;
+        b.v[i] = ld_stream_u32(d.codes + (e >> 1));
+        b.v[4 + i] = ld_stream_u32(d.pa + 16 * g + 4 * q2);
+        b.v[8 + i] = ld_stream_u32(d.pb + 8 * g + 4 * (q2 >> 1));
+        b.v[12 + i] = ld_stream_u32(d.pc + 4 * g);
+      } else {
+        const uint4 w = ld_stream_v4(d.raw + 2 * e);
+        b.v[4 * i + 0] = w.x; b.v[4 * i + 1] = w.y; b.v[4 * i + 2] = w.z; b.v[4 * i + 3] = w.w;
+      }
     }
+    return;
   }
+  const ChunkPtrs q = chunk_ptrs<SRC>(d, e_base, lane);
+  if (FULL || (vmask & 1)) load_slice<SRC, 0>(q, b);
+  if (FULL || (vmask & 2)) load_slice<SRC, 1>(q, b);
+  if (FULL || (vmask & 4)) load_slice<SRC, 2>(q, b);
+  if (FULL || (vmask & 8)) load_slice<SRC, 3>(q, b);
 }
 
 // BF16 pairs (elements 2q, 2q+1 of the slice in w[q]) of slice I.
@@ -181,7 +270,7 @@ __device__ __forceinline__ void slice_pairs(const RegTable& t, const ChunkBuf& b
   w[3] = prmt(l1, h1, 0x7362);
 }
 
-template <int SRC, int BT, int R, int MODE, bool FULL>
+template <int SRC, int BT, int R, int MODE, bool FULL, int ADDR>
 __device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t* __restrict__ xc, int64_t K, int B,
                                               const ChunkBuf (&buf)[R], const bool (&live)[R], uint32_t vmask,
                                               int lane, float2 (&acc)[R][BT]) {
@@ -192,7 +281,12 @@ __device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t*
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
       if (b < B) {
-        const uint4 v = ld_x_v4(xc + int64_t(b) * K + kSlice * i + 8 * lane);
+        const uint16_t* xb = xc + int64_t(b) * K + 8 * lane;
+        const uint4 v = ADDR == 0 ? ld_x_v4(xb + kSlice * i)
+                        : i == 0  ? ld_x_v4_at<0>(xb)
+                        : i == 1  ? ld_x_v4_at<2 * kSlice>(xb)
+                        : i == 2  ? ld_x_v4_at<4 * kSlice>(xb)
+                                  : ld_x_v4_at<6 * kSlice>(xb);
         xw[b][0] = v.x; xw[b][1] = v.y; xw[b][2] = v.z; xw[b][3] = v.w;
       } else {
         xw[b][0] = xw[b][1] = xw[b][2] = xw[b][3] = 0u;
@@ -280,13 +374,14 @@ struct UnitState {
   int ti;
   int64_t r0;
   uint32_t nchunks, vlast;
+  uint32_t e_lo, e_hi;  // the unit's escapes: [e_lo, e_hi) of the tensor's escape list
   bool last_full;
   bool live[R];
 };
 
-template <int R>
-__device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int lane, UnitState<R>& st) {
-  st.ti = owner(p.set_prefix, p.count, u);
+template <int SRC, int R, bool AHEAD>
+__device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int lane, UnitState<R>& st, int start) {
+  st.ti = owner(p.set_prefix, p.count, u, start);
   const TensorDesc& d = p.d[st.ti];
   st.r0 = int64_t(u - p.set_prefix[st.ti]) * R;
   st.nchunks = uint32_t(cdiv(uint64_t(d.K), kChunk));
@@ -297,9 +392,48 @@ __device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int l
   for (int i = 0; i < 4; ++i) st.vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
 #pragma unroll
   for (int j = 0; j < R; ++j) st.live[j] = st.r0 + j < d.N;
+  // requested one unit ahead, so the row index is at hand when the unit starts
+  if (SRC != kPlain && AHEAD) {
+    const int64_t r_end = st.r0 + R < d.N ? st.r0 + R : d.N;
+    st.e_lo = d.row_index[st.r0];
+    st.e_hi = d.row_index[r_end];
+  } else {
+    st.e_lo = st.e_hi = 0;
+  }
 }
 
-template <int SRC, int R>
+// Row (j < R) of the unit and column of escape position `pos`; base is the
+// unit's first element.  R is small, so this is R - 1 compares, no division.
+template <int R>
+__device__ __forceinline__ void esc_locate(uint32_t pos, uint64_t base, int64_t K, int& j, int64_t& k) {
+  int64_t off = int64_t(uint64_t(pos) - base);
+  j = 0;
+#pragma unroll
+  for (int jj = 1; jj < R; ++jj)
+    if (off >= K) {
+      off -= K;
+      ++j;
+    }
+  k = off;
+}
+
+// x * (w_true - w_placeholder) for one escape: `lo` is the placeholder's low
+// byte (byte-split; the escape value holds the high byte) and `val` the
+// escape value (the whole word for K15).
+template <int SCHEME>
+__device__ __forceinline__ float esc_delta(uint32_t val, uint32_t lo) {
+  uint32_t wt, wph;
+  if (SCHEME == WCOMP_BYTESPLIT) {
+    wph = lo;
+    wt = (val << 8) | lo;
+  } else {
+    wt = val;
+    wph = val & 0x7Fu;
+  }
+  return __uint_as_float(wt << 16) - __uint_as_float(wph << 16);
+}
+
+template <int SRC, int R, int ADDR>
 __device__ __forceinline__ void load_unit_chunk(const GemvBatch& p, const UnitState<R>& st, uint32_t c, int lane,
                                                 ChunkBuf (&bb)[R]) {
   const TensorDesc& d = p.d[st.ti];
@@ -309,29 +443,59 @@ __device__ __forceinline__ void load_unit_chunk(const GemvBatch& p, const UnitSt
   for (int j = 0; j < R; ++j) {
     if (!st.live[j]) continue;
     const uint64_t eb = uint64_t(st.r0 + j) * uint64_t(d.K) + uint64_t(c) * kChunk;
-    if (full) load_chunk<SRC, true>(ss, eb, 0xF, lane, bb[j]);
-    else load_chunk<SRC, false>(ss, eb, st.vlast, lane, bb[j]);
+    if (full) load_chunk<SRC, true, ADDR>(ss, eb, 0xF, lane, bb[j]);
+    else load_chunk<SRC, false, ADDR>(ss, eb, st.vlast, lane, bb[j]);
   }
+}
+
+// How a unit finds its escapes' rows and the row index.  All three give the
+// same sums; which one schedules best depends on the kernel's register
+// budget, so each (scheme, batch) instantiation takes the one measured
+// fastest.
+enum EscMode {
+  kEscDivide = 0,  // row index read when the unit starts; row of an escape by division
+  kEscLocate = 1,  // row index read when the unit starts; row by R - 1 compares
+  kEscAhead = 2,   // row index read one unit ahead; row by compares
+};
+
+#ifndef WCOMP_GEMV_ESC
+#define WCOMP_GEMV_ESC -1  // -1: the table below; 0..2 forces one mode everywhere
+#endif
+#ifndef WCOMP_GEMV_ADDR
+#define WCOMP_GEMV_ADDR -1  // -1: the table below; 0 or 1 forces one form everywhere
+#endif
+constexpr int addr_mode(int src, int bt) {
+  return WCOMP_GEMV_ADDR >= 0 ? WCOMP_GEMV_ADDR : src == kPlain ? 0 : 1;
+}
+
+constexpr int esc_mode(int src, int bt) {
+  return WCOMP_GEMV_ESC >= 0 ? WCOMP_GEMV_ESC
+         : src == kBytesplit ? (bt == 1 ? kEscDivide : bt == 2 ? kEscLocate : bt <= 8 ? kEscAhead : kEscLocate)
+         : src == kK15       ? (bt == 1 ? kEscLocate : bt == 2 ? kEscAhead : bt == 4 ? kEscDivide
+                                : bt == 8 ? kEscAhead : kEscLocate)
+                             : kEscLocate;
 }
 
 // The kernel (vector path: K % 32 == 0, aligned streams and x).  The warp
 // runs one continuous pipeline over (unit, chunk) items: while it computes an
 // item, the next item's loads are in flight, including across the boundary
 // between units, so no unit starts with an exposed load latency.
-template <int SRC, int BT, int R, int MINB, int MODE, int DEPTH>
+template <int SRC, int BT, int R, int MINB, int MODE, int ESC>
 __global__ void __launch_bounds__(kThreads, MINB)
     gemv_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
   const int lane = threadIdx.x & 31;
+  constexpr bool kAhead = ESC == kEscAhead;
+  constexpr int kAddr = addr_mode(SRC, BT);
   uint32_t u = grab(slot, lane);
   if (u < total_units) {
     uint32_t u_next = grab(slot, lane);
     UnitState<R> cur, nxt;
-    unit_state<R>(p, u, lane, cur);
+    unit_state<SRC, R, kAhead>(p, u, lane, cur, 0);
     // load cursor: the item after the one being computed
     ChunkBuf b0[R], b1[R];
-    load_unit_chunk<SRC, R>(p, cur, 0, lane, b0);
+    load_unit_chunk<SRC, R, kAddr>(p, cur, 0, lane, b0);
     float2 acc[R][BT];
-    uint32_t e_lo = 0, e_hi = 0, p0 = 0, v0 = 0;
+    uint32_t p0 = 0, v0 = 0;
     auto begin_unit = [&]() {
 #pragma unroll
       for (int j = 0; j < R; ++j)
@@ -339,12 +503,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int b = 0; b < BT; ++b) acc[j][b] = make_float2(0.f, 0.f);
       if (SRC != kPlain) {
         const TensorDesc& d = p.d[cur.ti];
-        const int64_t r_end = cur.r0 + R < d.N ? cur.r0 + R : d.N;
-        e_lo = d.row_index[cur.r0];
-        e_hi = d.row_index[r_end];
-        if (e_lo + lane < e_hi) {
-          p0 = d.esc_pos[e_lo + lane];
-          v0 = load_esc_val(d, e_lo + lane);
+        if (!kAhead) {
+          const int64_t r_end = cur.r0 + R < d.N ? cur.r0 + R : d.N;
+          cur.e_lo = d.row_index[cur.r0];
+          cur.e_hi = d.row_index[r_end];
+        }
+        if (cur.e_lo + lane < cur.e_hi) {
+          p0 = d.esc_pos[cur.e_lo + lane];
+          v0 = load_esc_val(d, cur.e_lo + lane);
         }
       }
     };
@@ -358,16 +524,30 @@ __global__ void __launch_bounds__(kThreads, MINB)
         for (int b = 0; b < BT; ++b) s[j][b] = acc[j][b].x + acc[j][b].y;
       if (SRC != kPlain) {
         const uint16_t* __restrict__ x = p.x[cur.ti];
-        for (uint32_t e = e_lo + lane; e < e_hi; e += 32) {
+        const uint64_t base = uint64_t(cur.r0) * uint64_t(K);
+        for (uint32_t e = cur.e_lo + lane; e < cur.e_hi; e += 32) {
           uint32_t pos = p0, val = v0;
-          if (e != e_lo + lane) {
+          if (e != cur.e_lo + lane) {
             pos = d.esc_pos[e];
             val = load_esc_val(d, e);
           }
-          const int64_t j = int64_t(pos / uint64_t(K)) - cur.r0;
+          int j;
+          int64_t k;
+          if (ESC == kEscDivide) {
+            j = int(int64_t(pos / uint64_t(K)) - cur.r0);
+            k = int64_t(uint64_t(pos) - base) - int64_t(j) * K;
+          } else {
+            esc_locate<R>(pos, base, K, j, k);
+          }
+          const uint32_t lo = SRC == kBytesplit ? uint32_t(d.raw[pos]) : 0u;
+          const float delta = esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(val, lo);
 #pragma unroll
-          for (int jj = 0; jj < R; ++jj)
-            if (jj == j) add_escape<BT>(d, x, B, uint64_t(cur.r0 + jj) * uint64_t(K), pos, val, s[jj]);
+          for (int jj = 0; jj < R; ++jj) {
+            if (jj != j) continue;
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+              if (b < B) s[jj][b] = fmaf(__uint_as_float(uint32_t(x[int64_t(b) * K + k]) << 16), delta, s[jj][b]);
+          }
         }
       }
 #pragma unroll
@@ -378,21 +558,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const TensorDesc& d = p.d[cur.ti];
       const uint16_t* xc = p.x[cur.ti] + uint64_t(c) * kChunk;
       if (c + 1 < cur.nchunks || cur.last_full)
-        compute_chunk<SRC, BT, R, MODE, true>(d.t, xc, d.K, B, bb, cur.live, 0xF, lane, acc);
+        compute_chunk<SRC, BT, R, MODE, true, kAddr>(d.t, xc, d.K, B, bb, cur.live, 0xF, lane, acc);
       else
-        compute_chunk<SRC, BT, R, MODE, false>(d.t, xc, d.K, B, bb, cur.live, cur.vlast, lane, acc);
+        compute_chunk<SRC, BT, R, MODE, false, kAddr>(d.t, xc, d.K, B, bb, cur.live, cur.vlast, lane, acc);
     };
     begin_unit();
     // position of the item held in the "current" buffer
     uint32_t c = 0;
     bool have_next_unit = u_next < total_units;
-    if (have_next_unit) unit_state<R>(p, u_next, lane, nxt);
+    if (have_next_unit) unit_state<SRC, R, kAhead>(p, u_next, lane, nxt, cur.ti);
     // One step: request the item after (cur, c) into `ld`, compute (cur, c)
     // from `cb`, then advance.  Returns false when nothing is left.
     auto step = [&](ChunkBuf (&cb)[R], ChunkBuf (&ld)[R]) -> bool {
       const bool last_of_unit = c + 1 == cur.nchunks;
-      if (!last_of_unit) load_unit_chunk<SRC, R>(p, cur, c + 1, lane, ld);
-      else if (have_next_unit) load_unit_chunk<SRC, R>(p, nxt, 0, lane, ld);
+      if (!last_of_unit) load_unit_chunk<SRC, R, kAddr>(p, cur, c + 1, lane, ld);
+      else if (have_next_unit) load_unit_chunk<SRC, R, kAddr>(p, nxt, 0, lane, ld);
       compute(c, cb);
       if (!last_of_unit) {
         ++c;
@@ -405,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       begin_unit();
       u_next = grab(slot, lane);
       have_next_unit = u_next < total_units;
-      if (have_next_unit) unit_state<R>(p, u_next, lane, nxt);
+      if (have_next_unit) unit_state<SRC, R, kAhead>(p, u_next, lane, nxt, cur.ti);
       return true;
     };
     while (step(b0, b1) && step(b1, b0)) {
@@ -807,7 +987,7 @@ int counter_slot(int dev, uint32_t** slot) {
 
 template <int SRC, int BT, int R, int MINB,
           int MODE = (BT == 1 ? WCOMP_GEMV_MODE1 : BT <= WCOMP_GEMV_MIXED_MAX_B ? 1 : 0),
-          int DEPTH = 2>
+          int ESC = esc_mode(SRC, BT)>
 int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
   uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
@@ -821,14 +1001,14 @@ int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   static int per_sm_cache = 0;
   if (!per_sm_cache) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE, DEPTH>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE, ESC>, kThreads, 0) !=
             cudaSuccess ||
         per_sm <= 0)
       per_sm = 1;
     per_sm_cache = per_sm;
   }
   const int blocks = per_sm_cache * sms;
-  gemv_kernel<SRC, BT, R, MINB, MODE, DEPTH><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
+  gemv_kernel<SRC, BT, R, MINB, MODE, ESC><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }
@@ -1114,7 +1294,7 @@ int launch_vec_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaS
   b.set_prefix[0] = 0;
   const uint32_t units = uint32_t(cdiv(uint64_t(N), R));
   b.set_prefix[1] = units;
-  auto kern = gemv_kernel<SRC, BT, R, MINB, MODE, 2>;
+  auto kern = gemv_kernel<SRC, BT, R, MINB, MODE, esc_mode(SRC, BT)>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0) != cudaSuccess || per_sm <= 0)
     per_sm = 1;
