@@ -916,6 +916,295 @@ __global__ void __launch_bounds__(kThreads, MINB)
 }
 
 // ---------------------------------------------------------------------------
+// Tensor-core path (mma.sync m16n8k16, BF16 in, fp32 accumulate).
+//
+// For larger batches the per-element fp32 FMAs and the x reads through L1
+// bound the kernel above, not HBM.  Here one warp-level MMA takes 16 batch
+// rows (M; the batch padded to 8 or 16) against 8 weight rows (N) over 16
+// elements of K, so the multiply costs one instruction per 128 weights of a
+// warp and x is read once per 8 weight rows.
+//
+// Work unit: 8 consecutive rows of one tensor.  A CTA of 4 warps takes a unit
+// and splits its K range into 4 contiguous runs of 128-element k-blocks; the
+// warps' partial 16x8 tiles are summed in shared memory in a fixed order.
+//
+// Lane (g = lane >> 2, t = lane & 3) holds weight row g of the unit.  In
+// k-block kb, slice i (0..3) covers elements 128 kb + 32 i .. +31 of every
+// row, and the lane owns the 8 elements 32 i + 8 t .. +7 (the same quarter
+// of a 32-element group as in the kernel above, so the slice decode is
+// shared).  The MMA's k order inside a step is a relabelling: step s = 2 i + h
+// pairs the lane's elements 4h .. 4h+3 of slice i with the B-fragment rows
+// 2t, 2t+1, 2t+8, 2t+9 and the same x elements with the A-fragment columns,
+// which leaves the sum unchanged.  Every load of weights and x is therefore
+// the same coalesced 4/8/16-byte piece per lane as above.
+//
+// Escapes: the tile sums the placeholders; after the k-blocks, thread
+// (row j, batch b, part q) adds x[b, k] * (w_true - w_placeholder) over the
+// q-th share of row j's escapes, and the parts are summed in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kMmaWarps = 4;
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kKBlock = 128;
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Stream addresses of slice 0 of k-block data starting at element e_row
+// (row start + 128 kb, a multiple of 32) for quarter t; slices follow at
+// immediate offsets.
+template <int SRC>
+__device__ __forceinline__ ChunkPtrs kblock_ptrs(const Streams& d, uint64_t e, int t) {
+  ChunkPtrs q{};
+  if (SRC == kPlain) {
+    q.r = d.raw + 2 * e + 16 * t;
+    return q;
+  }
+  q.c = d.codes + (e >> 1) + 4 * t;
+  if (SRC == kBytesplit) {
+    q.r = d.raw + e + 8 * t;
+  } else if (SRC == kK15) {
+    q.a = d.pa + (e >> 1) + 4 * t;
+    q.b = d.pb + (e >> 2) + 4 * (t >> 1);
+    q.cc = d.pc + (e >> 3);
+  }
+  return q;
+}
+
+template <int SRC, int I>
+__device__ __forceinline__ void load_kslice(const ChunkPtrs& q, ChunkBuf& b) {
+  if (SRC == kPlain) {
+    const uint4 w = ld_stream_v4_at<64 * I>(q.r);
+    b.v[4 * I + 0] = w.x; b.v[4 * I + 1] = w.y; b.v[4 * I + 2] = w.z; b.v[4 * I + 3] = w.w;
+  } else if (SRC == kBytesplit) {
+    b.v[I] = ld_stream_u32_at<16 * I>(q.c);
+    const uint2 r = ld_stream_v2_at<32 * I>(q.r);
+    b.v[4 + 2 * I] = r.x;
+    b.v[5 + 2 * I] = r.y;
+  } else {
+    b.v[I] = ld_stream_u32_at<16 * I>(q.c);
+    b.v[4 + I] = ld_stream_u32_at<16 * I>(q.a);
+    b.v[8 + I] = ld_stream_u32_at<8 * I>(q.b);
+    b.v[12 + I] = ld_stream_u32_at<4 * I>(q.cc);
+  }
+}
+
+// A unit as the tensor-core kernel sees it.
+struct MmaUnit {
+  int ti;
+  int64_t r0;
+  int rows;          // valid rows (1..8)
+  uint32_t kb0, kb1;  // this warp's k-blocks [kb0, kb1)
+  uint32_t kvalid;   // valid elements of the tensor's last k-block (32..128)
+  uint32_t nkb;      // k-blocks per row
+};
+
+__device__ __forceinline__ void mma_unit(const GemvBatch& p, uint32_t u, int warp, int start, MmaUnit& m) {
+  m.ti = owner(p.set_prefix, p.count, u, start);
+  const TensorDesc& d = p.d[m.ti];
+  m.r0 = int64_t(u - p.set_prefix[m.ti]) * 8;
+  m.rows = int(d.N - m.r0 < 8 ? d.N - m.r0 : 8);
+  m.nkb = uint32_t(cdiv(uint64_t(d.K), kKBlock));
+  m.kvalid = uint32_t(d.K - int64_t(m.nkb - 1) * kKBlock);
+  m.kb0 = uint32_t(uint64_t(m.nkb) * warp / kMmaWarps);
+  m.kb1 = uint32_t(uint64_t(m.nkb) * (warp + 1) / kMmaWarps);
+}
+
+// Loads of k-block kb of unit m for this lane (row g, quarter t).  Lanes whose
+// row is past N or whose quarter is past K load nothing.
+template <int SRC>
+__device__ __forceinline__ void load_kblock(const GemvBatch& p, const MmaUnit& m, uint32_t kb, int g, int t,
+                                            ChunkBuf& b) {
+  if (g >= m.rows) return;
+  const TensorDesc& d = p.d[m.ti];
+  const Streams ss{d.codes, d.raw, d.pa, d.pb, d.pc};
+  const uint64_t e = uint64_t(m.r0 + g) * uint64_t(d.K) + uint64_t(kb) * kKBlock;
+  const ChunkPtrs q = kblock_ptrs<SRC>(ss, e, t);
+  const uint32_t valid = kb + 1 == m.nkb ? m.kvalid : uint32_t(kKBlock);
+  load_kslice<SRC, 0>(q, b);
+  if (valid > 32) load_kslice<SRC, 1>(q, b);
+  if (valid > 64) load_kslice<SRC, 2>(q, b);
+  if (valid > 96) load_kslice<SRC, 3>(q, b);
+}
+
+// One k-block: decode each slice into B fragments and issue its two MMAs.
+template <int SRC, int XB>
+__device__ __forceinline__ void mma_kblock(const RegTable& tab, const uint16_t* __restrict__ x, int64_t K, int B,
+                                           const MmaUnit& m, uint32_t kb, int lane, const ChunkBuf& b,
+                                           float (&acc)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t valid = kb + 1 == m.nkb ? m.kvalid : uint32_t(kKBlock);
+  const bool wrow = g < m.rows;
+  const uint16_t* xg = x + int64_t(g) * K + int64_t(kb) * kKBlock + 8 * t;
+  const uint16_t* xg8 = xg + 8 * K;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (uint32_t(32 * i) >= valid) break;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (wrow) {
+      if (i == 0) slice_pairs<SRC, 0>(tab, b, lane, w);
+      else if (i == 1) slice_pairs<SRC, 1>(tab, b, lane, w);
+      else if (i == 2) slice_pairs<SRC, 2>(tab, b, lane, w);
+      else slice_pairs<SRC, 3>(tab, b, lane, w);
+    }
+    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = make_uint4(0u, 0u, 0u, 0u);
+    if (g < B) xa = ld_x_v4(xg + 32 * i);
+    if (XB == 16 && g + 8 < B) xb = ld_x_v4(xg8 + 32 * i);
+    mma_bf16(acc, xa.x, xb.x, xa.y, xb.y, w[0], w[1]);
+    mma_bf16(acc, xa.z, xb.z, xa.w, xb.w, w[2], w[3]);
+  }
+}
+
+template <int SRC, int XB, int MINB>
+__global__ void __launch_bounds__(kMmaThreads, MINB)
+    gemv_mma_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
+  // Two sets, alternating by unit parity, so one barrier per unit suffices:
+  // a set is rewritten two units later, after every thread has passed the
+  // next unit's barrier and so finished reading it.
+  __shared__ float part[2][kMmaWarps][32][4];
+  __shared__ float corr[2][128];
+  __shared__ uint32_t first_unit, next_unit[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  if (threadIdx.x == 0) {
+    first_unit = atomicAdd(slot, 1u);
+    next_unit[1] = atomicAdd(slot, 1u);
+  }
+  __syncthreads();
+  // This thread's share of the escape corrections: row cj, batch cb, part cq
+  // of cP (cbp batch slots, cP = 16 / cbp parts per (row, batch)).
+  const int cbp = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+  const int cP = 16 / cbp;
+  const int cj = threadIdx.x & 7, cb = (threadIdx.x >> 3) % cbp, cq = (threadIdx.x >> 3) / cbp;
+  uint32_t u = first_unit, u_next = next_unit[1];
+  if (u < total_units) {
+    MmaUnit cur, nxt;
+    uint32_t ce0 = 0, ce1 = 0, ne0 = 0, ne1 = 0;  // row cj's escapes in the current / next unit
+    auto row_escapes = [&](const MmaUnit& m, uint32_t& e0, uint32_t& e1) {
+      if (SRC == kPlain || cj >= m.rows) return;
+      const TensorDesc& d = p.d[m.ti];
+      e0 = d.row_index[m.r0 + cj];
+      e1 = d.row_index[m.r0 + cj + 1];
+    };
+    mma_unit(p, u, warp, 0, cur);
+    row_escapes(cur, ce0, ce1);
+    bool have_next = u_next < total_units;
+    if (have_next) {
+      mma_unit(p, u_next, warp, cur.ti, nxt);
+      row_escapes(nxt, ne0, ne1);
+    }
+    ChunkBuf b0, b1;
+    uint32_t kb = cur.kb0;
+    if (kb < cur.kb1) load_kblock<SRC>(p, cur, kb, g, t, b0);
+    float acc[4];
+    int par = 0;
+    uint32_t grabbed = 0;
+    if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
+    auto unit_end = [&]() {
+      // partial tiles, escape corrections, fixed-order sums
+      const TensorDesc& d = p.d[cur.ti];
+      part[par][warp][lane][0] = acc[0];
+      part[par][warp][lane][1] = acc[1];
+      part[par][warp][lane][2] = acc[2];
+      part[par][warp][lane][3] = acc[3];
+      {
+        float c = 0.f;
+        if (SRC != kPlain && cj < cur.rows && cb < B) {
+          const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
+          const uint16_t* xb = p.x[cur.ti] + int64_t(cb) * d.K;
+          uint32_t e = ce0 + cq;
+          // four escapes at a time: their loads are independent of each other
+          for (; e + 3 * cP < ce1; e += 4 * cP) {
+            uint32_t pos[4], val[4], lo[4], xv[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              pos[v] = d.esc_pos[e + v * cP];
+              val[v] = load_esc_val(d, e + v * cP);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              lo[v] = SRC == kBytesplit ? uint32_t(d.raw[pos[v]]) : 0u;
+              xv[v] = uint32_t(xb[int64_t(uint64_t(pos[v]) - rowbase)]);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              c = fmaf(__uint_as_float(xv[v] << 16),
+                       esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(val[v], lo[v]), c);
+          }
+          for (; e < ce1; e += cP) {
+            const uint32_t pos = d.esc_pos[e];
+            const uint32_t lo = SRC == kBytesplit ? uint32_t(d.raw[pos]) : 0u;
+            c = fmaf(__uint_as_float(uint32_t(xb[int64_t(uint64_t(pos) - rowbase)]) << 16),
+                     esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(load_esc_val(d, e), lo), c);
+          }
+        }
+        corr[par][threadIdx.x] = c;
+      }
+      // the unit after next (requested when this unit started), published
+      // with this unit's partial sums
+      if (threadIdx.x == 0) next_unit[par] = grabbed;
+      __syncthreads();
+      if (threadIdx.x < 8 * B && int(threadIdx.x & 7) < cur.rows) {
+        const int j = threadIdx.x & 7, bb = threadIdx.x >> 3;
+        const int src_lane = (bb & 7) * 4 + (j >> 1), reg = (bb >> 3) * 2 + (j & 1);
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMmaWarps; ++w) y += part[par][w][src_lane][reg];
+        for (int q = 0; q < cP; ++q) y += corr[par][(q * cbp + bb) * 8 + j];
+        p.y[cur.ti][int64_t(bb) * d.N + cur.r0 + j] = y;
+      }
+    };
+    auto step = [&](ChunkBuf& cbuf, ChunkBuf& lbuf) -> bool {
+      // request the item after (cur, kb), then compute (cur, kb)
+      const bool last = kb + 1 >= cur.kb1;
+      if (!last) load_kblock<SRC>(p, cur, kb + 1, g, t, lbuf);
+      else if (have_next && nxt.kb0 < nxt.kb1) load_kblock<SRC>(p, nxt, nxt.kb0, g, t, lbuf);
+      if (kb < cur.kb1) {
+        const TensorDesc& d = p.d[cur.ti];
+        mma_kblock<SRC, XB>(d.t, p.x[cur.ti], d.K, B, cur, kb, lane, cbuf, acc);
+      }
+      if (!last) {
+        ++kb;
+        return true;
+      }
+      unit_end();
+      if (!have_next) return false;
+      cur = nxt;
+      ce0 = ne0;
+      ce1 = ne1;
+      kb = cur.kb0;
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      u_next = next_unit[par];
+      par ^= 1;
+      if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
+      have_next = u_next < total_units;
+      if (have_next) {
+        mma_unit(p, u_next, warp, cur.ti, nxt);
+        row_escapes(nxt, ne0, ne1);
+      }
+      return true;
+    };
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    while (step(b0, b1) && step(b1, b0)) {
+    }
+  }
+  // The last CTA to finish returns the counter slot to zero for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(slot + 1, 1u) == gridDim.x - 1) {
+      atomicExch(slot, 0u);
+      atomicExch(slot + 1, 0u);
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Element path (any K, any alignment): one warp per row, static schedule.
 // ---------------------------------------------------------------------------
 template <int SRC, int BT>
@@ -1053,6 +1342,39 @@ int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   return map_cuda(cudaGetLastError());
 }
 
+template <int SRC, int XB, int MINB>
+int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  uint32_t units = 0;
+  for (int j = 0; j < b.count; ++j) {
+    b.set_prefix[j] = units;
+    units += uint32_t(cdiv(uint64_t(Ns[j]), 8));
+  }
+  b.set_prefix[b.count] = units;
+  uint32_t* slot = nullptr;
+  int st = counter_slot(dev, &slot);
+  if (st != WCOMP_OK) return st;
+  static int per_sm_cache = 0;
+  if (!per_sm_cache) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_mma_kernel<SRC, XB, MINB>, kMmaThreads, 0) !=
+            cudaSuccess ||
+        per_sm <= 0)
+      per_sm = 1;
+    per_sm_cache = per_sm;
+  }
+  gemv_mma_kernel<SRC, XB, MINB><<<per_sm_cache * sms, kMmaThreads, 0, s>>>(b, units, B, slot);
+  count_launches(1);
+  return map_cuda(cudaGetLastError());
+}
+
+// Batches from this size up take the tensor-core kernel (build-time tunable).
+#ifndef WCOMP_GEMV_MMA_MIN_B
+#define WCOMP_GEMV_MMA_MIN_B 5
+#endif
+#ifndef WCOMP_GEMV_MMA_MINB
+#define WCOMP_GEMV_MMA_MINB 6
+#endif
+
 // Rows per unit and CTAs per SM for each batch size (build-time tunables).
 #ifndef WCOMP_GEMV_R1
 #define WCOMP_GEMV_R1 1
@@ -1080,6 +1402,10 @@ int dispatch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaS
       case 8: return launch_tma<SRC, 8, WCOMP_GEMV_R8, 1>(b, Ns, B, dev, sms, s);
       default: return launch_tma<SRC, 16, WCOMP_GEMV_R16, 1>(b, Ns, B, dev, sms, s);
     }
+  }
+  if (B >= WCOMP_GEMV_MMA_MIN_B) {
+    if (B <= 8) return launch_mma<SRC, 8, WCOMP_GEMV_MMA_MINB>(b, Ns, B, dev, sms, s);
+    return launch_mma<SRC, 16, WCOMP_GEMV_MMA_MINB>(b, Ns, B, dev, sms, s);
   }
   switch (pow2_batch(B)) {
     case 1: return launch_vec<SRC, 1, WCOMP_GEMV_R1, SRC == kK15 ? WCOMP_GEMV_MINB1_K15 : WCOMP_GEMV_MINB1>(b, Ns, B, dev, sms, s);
