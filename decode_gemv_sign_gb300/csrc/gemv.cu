@@ -928,23 +928,29 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // and splits its K range into 4 contiguous runs of 128-element k-blocks; the
 // warps' partial 16x8 tiles are summed in shared memory in a fixed order.
 //
-// Lane (g = lane >> 2, t = lane & 3) holds weight row g of the unit.  In
-// k-block kb, slice i (0..3) covers elements 128 kb + 32 i .. +31 of every
-// row, and the lane owns the 8 elements 32 i + 8 t .. +7 (the same quarter
-// of a 32-element group as in the kernel above, so the slice decode is
-// shared).  The MMA's k order inside a step is a relabelling: step s = 2 i + h
-// pairs the lane's elements 4h .. 4h+3 of slice i with the B-fragment rows
-// 2t, 2t+1, 2t+8, 2t+9 and the same x elements with the A-fragment columns,
-// which leaves the sum unchanged.  Every load of weights and x is therefore
-// the same coalesced 4/8/16-byte piece per lane as above.
+// Lane (g = lane >> 2, t = lane & 3) holds weight row g of the unit and, in
+// k-block kb, its elements 128 kb + 32 t .. +31: one whole 32-element group,
+// fetched with one wide load per stream (16 bytes of codes, 32 of raw bytes),
+// so a warp's request for a stream is 8 row segments of 64 or 128 bytes.  The
+// lane decodes its group as four slices of 8 (slice i = elements 8i .. 8i+7).
+// The MMA's k order inside a step is a relabelling: step s = 2 i + h pairs
+// the lane's elements 8i + 4h .. +3 with the B-fragment rows 2t, 2t+1, 2t+8,
+// 2t+9 and the same x elements with the A-fragment columns, which leaves the
+// sum unchanged.
 //
 // Escapes: the tile sums the placeholders; after the k-blocks, thread
 // (row j, batch b, part q) adds x[b, k] * (w_true - w_placeholder) over the
 // q-th share of row j's escapes, and the parts are summed in a fixed order.
 // ---------------------------------------------------------------------------
-constexpr int kMmaWarps = 4;
+#ifndef WCOMP_GEMV_MMA_WARPS
+#define WCOMP_GEMV_MMA_WARPS 8
+#endif
+constexpr int kMmaWarps = WCOMP_GEMV_MMA_WARPS;  // warps splitting one unit's K range
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kKBlock = 128;
+// The escape corrections give every (row, batch) pair of a unit at least one
+// thread (8 rows x 16 batches) and the final sums one thread per output.
+static_assert(kMmaThreads >= 8 * 16 && kMmaThreads % (8 * 16) == 0, "MMA CTA too small for 8 rows x 16 batches");
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -955,43 +961,27 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Stream addresses of slice 0 of k-block data starting at element e_row
-// (row start + 128 kb, a multiple of 32) for quarter t; slices follow at
-// immediate offsets.
-template <int SRC>
-__device__ __forceinline__ ChunkPtrs kblock_ptrs(const Streams& d, uint64_t e, int t) {
-  ChunkPtrs q{};
-  if (SRC == kPlain) {
-    q.r = d.raw + 2 * e + 16 * t;
-    return q;
-  }
-  q.c = d.codes + (e >> 1) + 4 * t;
-  if (SRC == kBytesplit) {
-    q.r = d.raw + e + 8 * t;
-  } else if (SRC == kK15) {
-    q.a = d.pa + (e >> 1) + 4 * t;
-    q.b = d.pb + (e >> 2) + 4 * (t >> 1);
-    q.cc = d.pc + (e >> 3);
-  }
-  return q;
-}
-
-template <int SRC, int I>
-__device__ __forceinline__ void load_kslice(const ChunkPtrs& q, ChunkBuf& b) {
-  if (SRC == kPlain) {
-    const uint4 w = ld_stream_v4_at<64 * I>(q.r);
-    b.v[4 * I + 0] = w.x; b.v[4 * I + 1] = w.y; b.v[4 * I + 2] = w.z; b.v[4 * I + 3] = w.w;
-  } else if (SRC == kBytesplit) {
-    b.v[I] = ld_stream_u32_at<16 * I>(q.c);
-    const uint2 r = ld_stream_v2_at<32 * I>(q.r);
-    b.v[4 + 2 * I] = r.x;
-    b.v[5 + 2 * I] = r.y;
-  } else {
-    b.v[I] = ld_stream_u32_at<16 * I>(q.c);
-    b.v[4 + I] = ld_stream_u32_at<16 * I>(q.a);
-    b.v[8 + I] = ld_stream_u32_at<8 * I>(q.b);
-    b.v[12 + I] = ld_stream_u32_at<4 * I>(q.cc);
-  }
+// K15 pairs of slice I of a lane that holds a whole 32-element group (its
+// four slices are the group's four quarters, so the plane bit positions are
+// compile-time constants): code word v[I], plane A word v[4 + I], plane B
+// word v[8 + I / 2], plane C word v[12].
+template <int I>
+__device__ __forceinline__ void group_slice_pairs_k15(const RegTable& t, const ChunkBuf& b, uint32_t (&w)[4]) {
+  const uint32_t cw = b.v[I];
+  const QuadMasks m = code_masks(cw);
+  const uint32_t m7 = cw & 0x77777777u;
+  uint32_t h0, h1, e0, e1;
+  lookup8(t.hi, m7, m, h0, h1);
+  lookup8(t.e0, m7, m, e0, e1);
+  const uint32_t A = b.v[4 + I], Bw = b.v[8 + (I >> 1)], C = b.v[12];
+  constexpr int sb0 = 4 * (I & 1), q0 = 2 * I;
+  const uint32_t l0 = (A & 0x0F0F0F0Fu) | (((Bw >> sb0) << 4) & 0x30303030u) | (((C >> q0) << 6) & 0x40404040u) | e0;
+  const uint32_t l1 = ((A >> 4) & 0x0F0F0F0Fu) | (((Bw >> (sb0 + 2)) << 4) & 0x30303030u) |
+                      (((C >> (q0 + 1)) << 6) & 0x40404040u) | e1;
+  w[0] = prmt(l0, h0, 0x5140);
+  w[1] = prmt(l0, h0, 0x7362);
+  w[2] = prmt(l1, h1, 0x5140);
+  w[3] = prmt(l1, h1, 0x7362);
 }
 
 // A unit as the tensor-core kernel sees it.
@@ -1015,21 +1005,45 @@ __device__ __forceinline__ void mma_unit(const GemvBatch& p, uint32_t u, int war
   m.kb1 = uint32_t(uint64_t(m.nkb) * (warp + 1) / kMmaWarps);
 }
 
-// Loads of k-block kb of unit m for this lane (row g, quarter t).  Lanes whose
-// row is past N or whose quarter is past K load nothing.
+// Loads of k-block kb of unit m for this lane: row g, elements 32 t .. +31 of
+// the k-block, one wide load per stream.  Lanes whose row is past N or whose
+// quarter is past K load nothing.  The lane's first element is a multiple of
+// 32 (K % 32 == 0), so every load is aligned to its width.
+//   byte-split: v[0..3] codes, v[4..11] raw bytes
+//   K15:        v[0..3] codes, v[4..7] plane A, v[8..9] plane B, v[12] plane C
+//   plain:      v[0..15] the 32 BF16 values
 template <int SRC>
 __device__ __forceinline__ void load_kblock(const GemvBatch& p, const MmaUnit& m, uint32_t kb, int g, int t,
                                             ChunkBuf& b) {
   if (g >= m.rows) return;
-  const TensorDesc& d = p.d[m.ti];
-  const Streams ss{d.codes, d.raw, d.pa, d.pb, d.pc};
-  const uint64_t e = uint64_t(m.r0 + g) * uint64_t(d.K) + uint64_t(kb) * kKBlock;
-  const ChunkPtrs q = kblock_ptrs<SRC>(ss, e, t);
   const uint32_t valid = kb + 1 == m.nkb ? m.kvalid : uint32_t(kKBlock);
-  load_kslice<SRC, 0>(q, b);
-  if (valid > 32) load_kslice<SRC, 1>(q, b);
-  if (valid > 64) load_kslice<SRC, 2>(q, b);
-  if (valid > 96) load_kslice<SRC, 3>(q, b);
+  if (uint32_t(32 * t) >= valid) return;
+  const TensorDesc& d = p.d[m.ti];
+  const uint64_t e = uint64_t(m.r0 + g) * uint64_t(d.K) + uint64_t(kb) * kKBlock + 32 * t;
+  if (SRC == kPlain) {
+    uint32_t r[8];
+    ld_stream_v8(d.raw + 2 * e, r);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b.v[k] = r[k];
+    ld_stream_v8(d.raw + 2 * e + 32, r);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b.v[8 + k] = r[k];
+    return;
+  }
+  const uint4 c = ld_stream_v4(d.codes + (e >> 1));
+  b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
+  if (SRC == kBytesplit) {
+    uint32_t r[8];
+    ld_stream_v8(d.raw + e, r);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b.v[4 + k] = r[k];
+  } else {
+    const uint4 a = ld_stream_v4(d.pa + (e >> 1));
+    b.v[4] = a.x; b.v[5] = a.y; b.v[6] = a.z; b.v[7] = a.w;
+    const uint2 bb = ld_stream_v2(d.pb + (e >> 2));
+    b.v[8] = bb.x; b.v[9] = bb.y;
+    b.v[12] = ld_stream_u32(d.pc + (e >> 3));
+  }
 }
 
 // One k-block: decode each slice into B fragments and issue its two MMAs.
@@ -1039,22 +1053,29 @@ __device__ __forceinline__ void mma_kblock(const RegTable& tab, const uint16_t* 
                                            float (&acc)[4]) {
   const int g = lane >> 2, t = lane & 3;
   const uint32_t valid = kb + 1 == m.nkb ? m.kvalid : uint32_t(kKBlock);
-  const bool wrow = g < m.rows;
-  const uint16_t* xg = x + int64_t(g) * K + int64_t(kb) * kKBlock + 8 * t;
+  const bool live = uint32_t(32 * t) < valid;
+  const bool wlive = live && g < m.rows;
+  const uint16_t* xg = x + int64_t(g) * K + int64_t(kb) * kKBlock + 32 * t;
   const uint16_t* xg8 = xg + 8 * K;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    if (uint32_t(32 * i) >= valid) break;
     uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (wrow) {
-      if (i == 0) slice_pairs<SRC, 0>(tab, b, lane, w);
-      else if (i == 1) slice_pairs<SRC, 1>(tab, b, lane, w);
-      else if (i == 2) slice_pairs<SRC, 2>(tab, b, lane, w);
-      else slice_pairs<SRC, 3>(tab, b, lane, w);
+    if (wlive) {
+      if (SRC == kK15) {
+        if (i == 0) group_slice_pairs_k15<0>(tab, b, w);
+        else if (i == 1) group_slice_pairs_k15<1>(tab, b, w);
+        else if (i == 2) group_slice_pairs_k15<2>(tab, b, w);
+        else group_slice_pairs_k15<3>(tab, b, w);
+      } else {
+        if (i == 0) slice_pairs<SRC, 0>(tab, b, lane, w);
+        else if (i == 1) slice_pairs<SRC, 1>(tab, b, lane, w);
+        else if (i == 2) slice_pairs<SRC, 2>(tab, b, lane, w);
+        else slice_pairs<SRC, 3>(tab, b, lane, w);
+      }
     }
     uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = make_uint4(0u, 0u, 0u, 0u);
-    if (g < B) xa = ld_x_v4(xg + 32 * i);
-    if (XB == 16 && g + 8 < B) xb = ld_x_v4(xg8 + 32 * i);
+    if (live && g < B) xa = ld_x_v4(xg + 8 * i);
+    if (XB == 16 && live && g + 8 < B) xb = ld_x_v4(xg8 + 8 * i);
     mma_bf16(acc, xa.x, xb.x, xa.y, xb.y, w[0], w[1]);
     mma_bf16(acc, xa.z, xb.z, xa.w, xb.w, w[2], w[3]);
   }
@@ -1067,7 +1088,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
   // a set is rewritten two units later, after every thread has passed the
   // next unit's barrier and so finished reading it.
   __shared__ float part[2][kMmaWarps][32][4];
-  __shared__ float corr[2][128];
+  __shared__ float corr[2][kMmaThreads];
   __shared__ uint32_t first_unit, next_unit[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -1077,9 +1098,9 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
   }
   __syncthreads();
   // This thread's share of the escape corrections: row cj, batch cb, part cq
-  // of cP (cbp batch slots, cP = 16 / cbp parts per (row, batch)).
+  // of cP (cbp batch slots, cP = threads / (8 cbp) parts per (row, batch)).
   const int cbp = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
-  const int cP = 16 / cbp;
+  const int cP = kMmaThreads / (8 * cbp);
   const int cj = threadIdx.x & 7, cb = (threadIdx.x >> 3) % cbp, cq = (threadIdx.x >> 3) / cbp;
   uint32_t u = first_unit, u_next = next_unit[1];
   if (u < total_units) {
@@ -1367,13 +1388,18 @@ int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   return map_cuda(cudaGetLastError());
 }
 
-// Batches from this size up take the tensor-core kernel (build-time tunable).
+// Batches from this size up take the tensor-core kernel.  Byte-split decodes
+// cheaply enough that the FMA kernel keeps up to B = 4; K15's heavier decode
+// and the plain GEMV gain from B = 2.  WCOMP_GEMV_MMA_MIN_B overrides all.
 #ifndef WCOMP_GEMV_MMA_MIN_B
-#define WCOMP_GEMV_MMA_MIN_B 5
+#define WCOMP_GEMV_MMA_MIN_B 0
 #endif
 #ifndef WCOMP_GEMV_MMA_MINB
-#define WCOMP_GEMV_MMA_MINB 6
+#define WCOMP_GEMV_MMA_MINB 3
 #endif
+constexpr int mma_min_batch(int src) {
+  return WCOMP_GEMV_MMA_MIN_B > 0 ? WCOMP_GEMV_MMA_MIN_B : src == kBytesplit ? 5 : 2;
+}
 
 // Rows per unit and CTAs per SM for each batch size (build-time tunables).
 #ifndef WCOMP_GEMV_R1
@@ -1403,7 +1429,7 @@ int dispatch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaS
       default: return launch_tma<SRC, 16, WCOMP_GEMV_R16, 1>(b, Ns, B, dev, sms, s);
     }
   }
-  if (B >= WCOMP_GEMV_MMA_MIN_B) {
+  if (B >= mma_min_batch(SRC)) {
     if (B <= 8) return launch_mma<SRC, 8, WCOMP_GEMV_MMA_MINB>(b, Ns, B, dev, sms, s);
     return launch_mma<SRC, 16, WCOMP_GEMV_MMA_MINB>(b, Ns, B, dev, sms, s);
   }
@@ -1629,8 +1655,24 @@ int launch_vec_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaS
   return map_cuda(cudaGetLastError());
 }
 
+template <int SRC, int XB>
+int launch_mma_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaStream_t s) {
+  b.set_prefix[0] = 0;
+  const uint32_t units = uint32_t(cdiv(uint64_t(N), 8));
+  b.set_prefix[1] = units;
+  auto kern = gemv_mma_kernel<SRC, XB, WCOMP_GEMV_MMA_MINB>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, 0) != cudaSuccess || per_sm <= 0)
+    per_sm = 1;
+  kern<<<per_sm * sms, kMmaThreads, 0, s>>>(b, units, B, slot);
+  count_launches(1);
+  return map_cuda(cudaGetLastError());
+}
+
 template <int SRC>
 int dispatch_vec_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaStream_t s) {
+  if (B >= mma_min_batch(SRC))
+    return B <= 8 ? launch_mma_on<SRC, 8>(b, N, B, sms, slot, s) : launch_mma_on<SRC, 16>(b, N, B, sms, slot, s);
   switch (pow2_batch(B)) {
     case 1: return launch_vec_on<SRC, 1, WCOMP_GEMV_R1, SRC == kK15 ? WCOMP_GEMV_MINB1_K15 : WCOMP_GEMV_MINB1>(
         b, N, B, sms, slot, s);
