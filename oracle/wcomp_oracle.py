@@ -35,7 +35,14 @@ Readings where the pages are silent (each is listed in the design notes):
   16-bit word (its top 9 bits are the symbol, the low 7 repeat the raw
   mantissa so the weight can be rebuilt from the entry alone);
 * the physical container layout (nibble order, K15 bit planes, indexes,
-  header, checksums) is this library's own and is defined here;
+  header, checksums) is this library's own and is defined here; it has two
+  serialized forms: version 1 keeps the (position, value) escape stream and
+  both indexes, version 2 (compact) keeps only what the pages count: the
+  escape symbols at their symbol width (8 bits, or 9 bits packed for K15)
+  and one 16-bit escape count per tile, with every position implied by its
+  code 15 (forgeeks page, "Cómo funciona la compresión": the escape stream
+  holds the rare symbols exactly; its bits/weight counts them at symbol
+  width);
 * the GEMV is y[b, r] = sum_k x[b, k] * W[r, k] evaluated in float64 from
   the exact BF16 values (accumulation order is not part of the method).
 
@@ -58,6 +65,7 @@ import numpy as np
 # ---------------------------------------------------------------------------
 MAGIC = b"WCMP"
 VERSION = 1
+VERSION_COMPACT = 2
 BYTESPLIT = 0
 K15 = 1
 SCHEMES = (BYTESPLIT, K15)
@@ -355,14 +363,7 @@ def serialize(c: Container) -> bytes:
         assert name == name2 and arr.size == size, (name, arr.size, size)
         payload += arr.tobytes()
         payload += b"\0" * (_pad(size) - size)
-    table16 = struct.pack("<15H", *[int(t) for t in c.table])
-    head = (MAGIC + struct.pack("<HBB", VERSION, c.scheme, 0) +
-            struct.pack("<qqQ", c.N, c.K, c.E) + struct.pack("<II", TILE, 0) +
-            table16 + struct.pack("<H", 0) +
-            struct.pack("<QI", len(payload), zlib.crc32(payload)) + b"\0" * 8)
-    assert len(head) == 92
-    head += struct.pack("<I", zlib.crc32(head))
-    return bytes(head) + bytes(payload)
+    return _header(VERSION, c, bytes(payload)) + bytes(payload)
 
 
 class CorruptContainer(ValueError):
@@ -378,7 +379,7 @@ def deserialize(buf: bytes) -> Container:
     if struct.unpack_from("<I", head, 92)[0] != zlib.crc32(head[:92]):
         raise CorruptContainer("header checksum")
     version, scheme, _ = struct.unpack_from("<HBB", head, 4)
-    if version != VERSION or scheme not in SCHEMES:
+    if version not in (VERSION, VERSION_COMPACT) or scheme not in SCHEMES:
         raise CorruptContainer("version/scheme")
     N, K, E = struct.unpack_from("<qqQ", head, 8)
     tile, _ = struct.unpack_from("<II", head, 32)
@@ -386,6 +387,10 @@ def deserialize(buf: bytes) -> Container:
     plen, pcrc = struct.unpack_from("<QI", head, 72)
     if tile != TILE or N <= 0 or K <= 0 or not N * K < 2**32 or E > N * K:
         raise CorruptContainer("sizes")
+    if len(set(table.tolist())) != TABLE_SIZE or int(table.max()) >= NBINS[scheme]:
+        raise CorruptContainer("table")
+    if version == VERSION_COMPACT:
+        return _deserialize_compact(buf, scheme, N, K, E, table, plen, pcrc)
     sizes = section_sizes(scheme, N, K, E)
     if plen != sum(_pad(s) for _, s in sizes) or len(buf) != HEADER_BYTES + plen:
         raise CorruptContainer("payload length")
@@ -420,6 +425,114 @@ def deserialize(buf: bytes) -> Container:
     return Container(scheme, N, K, table, codes, np.zeros(0, np.uint8),
                      sec["plane_a"].copy(), sec["plane_b"].copy(), sec["plane_c"].copy(),
                      tile_index, row_index, esc_pos, esc_val, np.zeros(0, np.int64))
+
+
+# ---------------------------------------------------------------------------
+# Compact serialized form (version 2): no positions, no row index.
+# ---------------------------------------------------------------------------
+def pack_bits9(vals: np.ndarray) -> np.ndarray:
+    """9-bit values into a little-endian bit stream: value r occupies stream
+    bits 9r .. 9r+8, least significant first; stream bit b is bit (b % 8) of
+    byte b // 8.  The last byte is zero-padded."""
+    vals = np.asarray(vals, dtype=np.uint32)
+    bits = ((vals[:, None] >> np.arange(9, dtype=np.uint32)) & 1).astype(np.uint8).reshape(-1)
+    out = np.zeros(_cdiv(bits.size, 8), dtype=np.uint8)
+    if bits.size:
+        padded = np.zeros(out.size * 8, dtype=np.uint8)
+        padded[: bits.size] = bits
+        out = np.packbits(padded.reshape(-1, 8), axis=1, bitorder="little").reshape(-1)
+    return out
+
+
+def unpack_bits9(buf: np.ndarray, count: int) -> np.ndarray:
+    bits = np.unpackbits(np.asarray(buf, dtype=np.uint8), bitorder="little")[: 9 * count]
+    return (bits.reshape(count, 9).astype(np.uint32) << np.arange(9, dtype=np.uint32)).sum(axis=1).astype(np.uint32)
+
+
+def section_sizes_compact(scheme: int, N: int, K: int, E: int) -> list:
+    """Unpadded byte size of every payload section of the compact form, in order."""
+    n = N * K
+    groups = _cdiv(n, GROUP)
+    if scheme == BYTESPLIT:
+        raw = [("raw", n)]
+        sym = E
+    else:
+        raw = [("plane_a", 16 * groups), ("plane_b", 8 * groups), ("plane_c", 4 * groups)]
+        sym = _cdiv(9 * E, 8)
+    return [("codes", _cdiv(n, 2))] + raw + [("tile_count", 2 * _cdiv(n, TILE)), ("esc_sym", sym)]
+
+
+def _header(version: int, c: "Container", payload: bytes) -> bytes:
+    table16 = struct.pack("<15H", *[int(t) for t in c.table])
+    head = (MAGIC + struct.pack("<HBB", version, c.scheme, 0) +
+            struct.pack("<qqQ", c.N, c.K, c.E) + struct.pack("<II", TILE, 0) +
+            table16 + struct.pack("<H", 0) +
+            struct.pack("<QI", len(payload), zlib.crc32(payload)) + b"\0" * 8)
+    assert len(head) == 92
+    return head + struct.pack("<I", zlib.crc32(head))
+
+
+def serialize_compact(c: Container) -> bytes:
+    """Version 2: codes, raw bytes or K15 planes, the escape count of every
+    tile (u16; a tile holds at most 8192 escapes) and the escape symbols in
+    ascending position order (byte-split: the high byte; K15: the 9-bit
+    symbol, the top 9 bits of the escaped word, packed by pack_bits9)."""
+    parts = [("codes", c.codes)]
+    if c.scheme == BYTESPLIT:
+        parts.append(("raw", c.raw))
+        sym = c.esc_val.astype(np.uint8)
+    else:
+        parts += [("plane_a", c.plane_a), ("plane_b", c.plane_b), ("plane_c", c.plane_c)]
+        sym = pack_bits9(c.esc_val.astype(np.uint32) >> 7)
+    parts += [("tile_count", np.diff(c.tile_index.astype(np.int64)).astype("<u2").view(np.uint8)),
+              ("esc_sym", sym)]
+    payload = bytearray()
+    for (name, arr), (name2, size) in zip(parts, section_sizes_compact(c.scheme, c.N, c.K, c.E)):
+        assert name == name2 and arr.size == size, (name, arr.size, size)
+        payload += arr.tobytes()
+        payload += b"\0" * (_pad(size) - size)
+    return _header(VERSION_COMPACT, c, bytes(payload)) + bytes(payload)
+
+
+def _deserialize_compact(buf: bytes, scheme: int, N: int, K: int, E: int, table: np.ndarray,
+                         plen: int, pcrc: int) -> Container:
+    sizes = section_sizes_compact(scheme, N, K, E)
+    if plen != sum(_pad(s) for _, s in sizes) or len(buf) != HEADER_BYTES + plen:
+        raise CorruptContainer("payload length")
+    payload = np.frombuffer(buf, dtype=np.uint8, offset=HEADER_BYTES)
+    if zlib.crc32(payload.tobytes()) != pcrc:
+        raise CorruptContainer("payload checksum")
+    sec = {}
+    off = 0
+    for name, size in sizes:
+        sec[name] = payload[off: off + size]
+        off += _pad(size)
+    n = N * K
+    codes = sec["codes"].copy()
+    # every position is implied by its code 15
+    esc_pos = np.flatnonzero(unpack_codes(codes, n) == ESCAPE).astype(np.uint32)
+    if esc_pos.size != E:
+        raise CorruptContainer("escape count")
+    n_tiles = _cdiv(n, TILE)
+    tile_index = escape_index(esc_pos, np.arange(n_tiles + 1, dtype=np.int64) * TILE)
+    counts = sec["tile_count"].view("<u2").astype(np.int64)
+    if not np.array_equal(counts, np.diff(tile_index.astype(np.int64))):
+        raise CorruptContainer("tile counts")
+    row_index = escape_index(esc_pos, np.arange(N + 1, dtype=np.int64) * K)
+    if scheme == BYTESPLIT:
+        esc_val = sec["esc_sym"].copy()
+        return Container(scheme, N, K, table, codes, sec["raw"].copy(), None, None, None,
+                         tile_index, row_index, esc_pos, esc_val, np.zeros(0, np.int64))
+    sym9 = unpack_bits9(sec["esc_sym"], E)
+    pa, pb, pc = sec["plane_a"].copy(), sec["plane_b"].copy(), sec["plane_c"].copy()
+    mant = unpack_k15_planes(pa, pb, pc, n)[esc_pos] if E else np.zeros(0, np.uint32)
+    esc_val = ((sym9 << 7) | mant).astype(np.uint16)
+    return Container(scheme, N, K, table, codes, np.zeros(0, np.uint8), pa, pb, pc,
+                     tile_index, row_index, esc_pos, esc_val, np.zeros(0, np.int64))
+
+
+def serialized_len_compact(scheme: int, N: int, K: int, E: int) -> int:
+    return HEADER_BYTES + sum(_pad(s) for _, s in section_sizes_compact(scheme, N, K, E))
 
 
 # ---------------------------------------------------------------------------
