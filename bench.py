@@ -488,7 +488,10 @@ def run_ours(args):
         "bpw": {SCHEME_NAMES[s]: {"entropy": round(sum(i["entropy_bpw"] * i["n"] for i in hp.infos if i["scheme"] == s) /
                                                    sum(i["n"] for i in hp.infos if i["scheme"] == s), 4),
                                   "physical": round(sum(8 * i["serialized_bytes"] for i in hp.infos if i["scheme"] == s) /
-                                                    sum(i["n"] for i in hp.infos if i["scheme"] == s), 4)}
+                                                    sum(i["n"] for i in hp.infos if i["scheme"] == s), 4),
+                                  "physical_compact": round(
+                                      sum(8 * i["serialized_compact_bytes"] for i in hp.infos if i["scheme"] == s) /
+                                      sum(i["n"] for i in hp.infos if i["scheme"] == s), 4)}
                 for s in (0, 1)},
         "roofline": roofline,
         "clocks": clk,

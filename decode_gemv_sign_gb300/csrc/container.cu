@@ -106,6 +106,25 @@ extern "C" const char* wcomp_strerror(int s) {
   }
 }
 
+// The compact serialized form (format version 2).  Its codes and raw bytes /
+// K15 planes keep their version-1 offsets (they lead both forms); then one
+// u16 escape count per tile and the escape symbols (u8, or 9 bits packed
+// least significant bit first for K15).  Positions, the row index and the
+// K15 escape mantissas are rebuilt from the codes and planes when loading.
+constexpr uint16_t kVersionCompact = 2;
+
+struct CompactLayout {
+  uint64_t sz_tilecount, sz_sym, off_tilecount, off_sym, payload;
+  void compute(const Layout& L) {
+    sz_tilecount = 2 * L.n_tiles;
+    sz_sym = L.scheme == WCOMP_BYTESPLIT ? L.E : cdiv(9 * L.E, 8);
+    off_tilecount = L.off_tile;
+    off_sym = off_tilecount + padsec(sz_tilecount);
+    payload = off_sym + padsec(sz_sym);
+  }
+  uint64_t serialized() const { return kHeaderBytes + payload; }
+};
+
 extern "C" int wcomp_info(const wcomp_container* c, wcomp_info_t* info) {
   if (!c || !info) return WCOMP_EINVAL;
   const Layout& L = c->L;
@@ -128,21 +147,26 @@ extern "C" int wcomp_info(const wcomp_container* c, wcomp_info_t* info) {
   const double raw_bits = L.scheme == WCOMP_BYTESPLIT ? 8.0 : 7.0;
   info->entropy_bpw = 4.0 + raw_bits + (double(L.E) + kTableSize) * sym_bits / double(L.n);
   info->physical_bpw = 8.0 * double(L.serialized()) / double(L.n);
+  CompactLayout C;
+  C.compute(L);
+  info->serialized_compact_bytes = C.serialized();
+  info->physical_compact_bpw = 8.0 * double(C.serialized()) / double(L.n);
   return WCOMP_OK;
 }
 
-static void write_header(const wcomp_container* c, uint32_t payload_crc, uint8_t* h) {
+static void write_header(const wcomp_container* c, uint16_t version, uint64_t payload_len, uint32_t payload_crc,
+                         uint8_t* h) {
   const Layout& L = c->L;
   memset(h, 0, kHeaderBytes);
   memcpy(h, "WCMP", 4);
-  put16(h + 4, WCOMP_VERSION);
+  put16(h + 4, version);
   h[6] = uint8_t(L.scheme);
   put64(h + 8, uint64_t(L.N));
   put64(h + 16, uint64_t(L.K));
   put64(h + 24, L.E);
   put32(h + 32, kTile);
   for (int i = 0; i < kTableSize; ++i) put16(h + 40 + 2 * i, c->table[i]);
-  put64(h + 72, L.main_payload + L.esc_payload);
+  put64(h + 72, payload_len);
   put32(h + 80, payload_crc);
   put32(h + 92, crc32_update(0, h, 92));
 }
@@ -162,17 +186,64 @@ extern "C" int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return map_cuda(e);
   uint32_t crc = crc32_update(0, out + kHeaderBytes, L.main_payload + L.esc_payload);
-  write_header(c, crc, out);
+  write_header(c, WCOMP_VERSION, L.main_payload + L.esc_payload, crc, out);
+  return WCOMP_OK;
+}
+
+extern "C" int wcomp_serialize_compact(const wcomp_container* c, void* host_buf, uint64_t cap, uint64_t* len,
+                                       void* stream) {
+  if (!c || !len) return WCOMP_EINVAL;
+  const Layout& L = c->L;
+  CompactLayout C;
+  C.compute(L);
+  *len = C.serialized();
+  if (!host_buf) return WCOMP_OK;
+  if (cap < C.serialized()) return WCOMP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* out = static_cast<uint8_t*>(host_buf);
+  uint8_t* p = out + kHeaderBytes;
+  std::vector<uint32_t> tile(L.n_tiles + 1);
+  std::vector<uint8_t> val(L.sz_val);
+  // codes and raw bytes / planes in one copy (same offsets in both forms)
+  cudaError_t e = cudaMemcpyAsync(p, c->d_main, L.off_tile, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(tile.data(), c->d_main + L.off_tile, L.sz_tile, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && L.E)
+    e = cudaMemcpyAsync(val.data(), c->d_esc + L.off_val, L.sz_val, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return map_cuda(e);
+  uint8_t* tc = p + C.off_tilecount;
+  memset(tc, 0, padsec(C.sz_tilecount));
+  for (uint64_t t = 0; t < L.n_tiles; ++t) put16(tc + 2 * t, uint16_t(tile[t + 1] - tile[t]));
+  uint8_t* sym = p + C.off_sym;
+  memset(sym, 0, padsec(C.sz_sym));
+  if (L.scheme == WCOMP_BYTESPLIT) {
+    if (L.E) memcpy(sym, val.data(), L.E);
+  } else {
+    for (uint64_t r = 0; r < L.E; ++r) {
+      const uint32_t v = uint32_t(get16(val.data() + 2 * r)) >> 7;  // the 9-bit symbol
+      const uint64_t bit = 9 * r;
+      const uint32_t w = v << (bit & 7);
+      sym[bit >> 3] |= uint8_t(w);
+      sym[(bit >> 3) + 1] |= uint8_t(w >> 8);
+    }
+  }
+  const uint32_t crc = crc32_update(0, p, C.payload);
+  write_header(c, kVersionCompact, C.payload, crc, out);
   return WCOMP_OK;
 }
 
 // Host-side validation of a serialized container (nothing reaches the device
 // unless every check passes, so the kernels never see out-of-range positions).
-static int validate(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table) {
+// Header fields shared by both forms: magic, header checksum, version,
+// scheme, sizes, tile size and the table (15 distinct symbols in range).
+// Fills L for the container's shape and returns the format version.
+static int check_header(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table, uint16_t* version) {
   if (len < uint64_t(kHeaderBytes)) return WCOMP_ECORRUPT;
   if (memcmp(b, "WCMP", 4) != 0) return WCOMP_ECORRUPT;
   if (get32(b + 92) != crc32_update(0, b, 92)) return WCOMP_ECORRUPT;
-  if (get16(b + 4) != WCOMP_VERSION) return WCOMP_ECORRUPT;
+  *version = get16(b + 4);
+  if (*version != WCOMP_VERSION && *version != kVersionCompact) return WCOMP_ECORRUPT;
   int scheme = b[6];
   if (scheme != WCOMP_BYTESPLIT && scheme != WCOMP_K15) return WCOMP_ECORRUPT;
   int64_t N = int64_t(get64(b + 8)), K = int64_t(get64(b + 16));
@@ -182,10 +253,6 @@ static int validate(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table) 
   uint64_t n = uint64_t(N) * uint64_t(K);
   if (n >= (uint64_t(1) << 32) || E > n) return WCOMP_ECORRUPT;
   L.compute(scheme, N, K, E);
-  if (get64(b + 72) != L.main_payload + L.esc_payload) return WCOMP_ECORRUPT;
-  if (len != L.serialized()) return WCOMP_ECORRUPT;
-  const uint8_t* p = b + kHeaderBytes;
-  if (get32(b + 80) != crc32_update(0, p, L.main_payload + L.esc_payload)) return WCOMP_ECORRUPT;
   const int nb = scheme == WCOMP_BYTESPLIT ? 256 : 512;
   for (int i = 0; i < kTableSize; ++i) {
     table[i] = get16(b + 40 + 2 * i);
@@ -193,6 +260,16 @@ static int validate(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table) 
     for (int j = 0; j < i; ++j)
       if (table[j] == table[i]) return WCOMP_ECORRUPT;
   }
+  return WCOMP_OK;
+}
+
+static int validate(const uint8_t* b, uint64_t len, const Layout& L) {
+  const int64_t N = L.N, K = L.K;
+  const uint64_t n = L.n, E = L.E;
+  if (get64(b + 72) != L.main_payload + L.esc_payload) return WCOMP_ECORRUPT;
+  if (len != L.serialized()) return WCOMP_ECORRUPT;
+  const uint8_t* p = b + kHeaderBytes;
+  if (get32(b + 80) != crc32_update(0, p, L.main_payload + L.esc_payload)) return WCOMP_ECORRUPT;
   // escape positions: strictly ascending, below n, exactly the elements coded 15
   const uint8_t* codes = p + L.off_codes;
   const uint8_t* pos = p + L.main_payload + L.off_pos;
@@ -223,12 +300,93 @@ static int validate(const uint8_t* b, uint64_t len, Layout& L, uint16_t* table) 
   return WCOMP_OK;
 }
 
+// K15 mantissa of element i from the three planes (a 32-element group holds
+// 16 bytes of plane A, 8 of plane B, 4 of plane C; element 4q + l of the
+// group sits in byte l of its words, bit field q of the quad order).
+static uint32_t k15_mantissa(const uint8_t* pa, const uint8_t* pb, const uint8_t* pc, uint64_t i) {
+  const uint64_t g = i >> 5;
+  const uint32_t e = uint32_t(i & 31), q = e >> 2, lane = e & 3;
+  const uint32_t wa = get32(pa + 16 * g + 4 * (q >> 1));
+  const uint32_t wb = get32(pb + 8 * g + 4 * (q >> 2));
+  const uint32_t wc = get32(pc + 4 * g);
+  return ((wa >> (8 * lane + 4 * (q & 1))) & 15u) | (((wb >> (8 * lane + 2 * (q & 3))) & 3u) << 4) |
+         (((wc >> (8 * lane + q)) & 1u) << 6);
+}
+
+// Compact form: check the payload and rebuild the version-1 sections
+// (positions from the codes 15, tile and row indexes, whole K15 escape
+// words) into main / esc images laid out like a version-1 payload.
+static int load_compact(const uint8_t* b, uint64_t len, const Layout& L, std::vector<uint8_t>& main_img,
+                        std::vector<uint8_t>& esc_img) {
+  CompactLayout C;
+  C.compute(L);
+  if (get64(b + 72) != C.payload || len != C.serialized()) return WCOMP_ECORRUPT;
+  const uint8_t* p = b + kHeaderBytes;
+  if (get32(b + 80) != crc32_update(0, p, C.payload)) return WCOMP_ECORRUPT;
+  main_img.assign(L.main_payload, 0);
+  esc_img.assign(L.esc_payload, 0);
+  memcpy(main_img.data(), p, L.off_tile);  // codes and raw bytes / planes
+  const uint8_t* codes = p + L.off_codes;
+  const uint8_t* tc = p + C.off_tilecount;
+  uint8_t* pos = esc_img.data() + L.off_pos;
+  uint8_t* ti = main_img.data() + L.off_tile;
+  // positions: the elements coded 15, in order; E of them, matching every tile count
+  uint64_t e = 0;
+  for (uint64_t t = 0; t < L.n_tiles; ++t) {
+    put32(ti + 4 * t, uint32_t(e));
+    const uint64_t lo = t * kTile, hi = lo + kTile < L.n ? lo + kTile : L.n;
+    const uint64_t e0 = e;
+    for (uint64_t i = lo; i < hi; ++i) {
+      if (((codes[i >> 1] >> (4 * (i & 1))) & 0xF) != kEscape) continue;
+      if (e >= L.E) return WCOMP_ECORRUPT;
+      put32(pos + 4 * e, uint32_t(i));
+      ++e;
+    }
+    if (e - e0 != get16(tc + 2 * t)) return WCOMP_ECORRUPT;
+  }
+  if (e != L.E) return WCOMP_ECORRUPT;
+  put32(ti + 4 * L.n_tiles, uint32_t(e));
+  uint8_t* ri = main_img.data() + L.off_row;
+  uint64_t k = 0;
+  for (uint64_t r = 0; r <= uint64_t(L.N); ++r) {
+    const uint64_t bound = r * uint64_t(L.K);
+    while (k < L.E && get32(pos + 4 * k) < bound) ++k;
+    put32(ri + 4 * r, uint32_t(k));
+  }
+  const uint8_t* sym = p + C.off_sym;
+  uint8_t* val = esc_img.data() + L.off_val;
+  if (L.scheme == WCOMP_BYTESPLIT) {
+    if (L.E) memcpy(val, sym, L.E);
+  } else {
+    for (uint64_t r = 0; r < L.E; ++r) {
+      const uint64_t bit = 9 * r;
+      const uint32_t v = ((uint32_t(sym[bit >> 3]) | (uint32_t(sym[(bit >> 3) + 1]) << 8)) >> (bit & 7)) & 0x1FFu;
+      const uint32_t m = k15_mantissa(p + L.off_a, p + L.off_b, p + L.off_c, get32(pos + 4 * r));
+      put16(val + 2 * r, uint16_t((v << 7) | m));
+    }
+  }
+  return WCOMP_OK;
+}
+
 extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* stream, wcomp_container** out) {
   if (!host_buf || !out) return WCOMP_EINVAL;
   *out = nullptr;
+  const uint8_t* b = static_cast<const uint8_t*>(host_buf);
   Layout L;
   uint16_t table[kTableSize];
-  int st = validate(static_cast<const uint8_t*>(host_buf), len, L, table);
+  uint16_t version = 0;
+  int st = check_header(b, len, L, table, &version);
+  if (st != WCOMP_OK) return st;
+  std::vector<uint8_t> main_img, esc_img;
+  const uint8_t* main_src = b + kHeaderBytes;
+  const uint8_t* esc_src = main_src + L.main_payload;
+  if (version == WCOMP_VERSION) {
+    st = validate(b, len, L);
+  } else {
+    st = load_compact(b, len, L, main_img, esc_img);
+    main_src = main_img.data();
+    esc_src = esc_img.data();
+  }
   if (st != WCOMP_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   wcomp_container* c = new (std::nothrow) wcomp_container();
@@ -236,12 +394,11 @@ extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* strea
   c->L = L;
   memcpy(c->table, table, sizeof(table));
   cudaGetDevice(&c->device);
-  const uint8_t* p = static_cast<const uint8_t*>(host_buf) + kHeaderBytes;
   cudaError_t e = pool_alloc(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
   if (e == cudaSuccess && L.esc_payload) e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_main, p, L.main_payload, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_main, main_src, L.main_payload, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && L.esc_payload)
-    e = cudaMemcpyAsync(c->d_esc, p + L.main_payload, L.esc_payload, cudaMemcpyHostToDevice, s);
+    e = cudaMemcpyAsync(c->d_esc, esc_src, L.esc_payload, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     wcomp_free(c, stream);

@@ -94,6 +94,7 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
                     exact = bool(torch.equal(ws[s.name].view(-1), o.view(-1)))
                     rec = {"name": s.name, "scheme": sc, "N": s.N, "K": s.K, "n": inf["n"],
                            "escapes": inf["n_escapes"], "serialized_bytes": inf["serialized_bytes"],
+                           "serialized_compact_bytes": inf["serialized_compact_bytes"],
                            "entropy_bpw": inf["entropy_bpw"], "exact": exact}
                     done[(s.name, sc)] = rec
                     if log:
@@ -115,6 +116,7 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
         recs = [done[(nm, sc)] for nm in names if (nm, sc) in done]
         n = sum(r["n"] for r in recs)
         ser = sum(r["serialized_bytes"] for r in recs)
+        ser_c = sum(r.get("serialized_compact_bytes", r["serialized_bytes"]) for r in recs)
         ebits = sum(r["entropy_bpw"] * r["n"] for r in recs)
         bpw_e = ebits / n if n else 0.0
         out["schemes"][SCHEME_NAMES[sc]] = {
@@ -123,6 +125,9 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
             "entropy_bpw": round(bpw_e, 5), "physical_bpw": round(8.0 * ser / n, 5) if n else 0.0,
             "entropy_reduction_pct": round(100.0 * (1 - bpw_e / 16.0), 3) if n else 0.0,
             "physical_reduction_pct": round(100.0 * (1 - ser / (2.0 * n)), 3) if n else 0.0,
+            "serialized_compact_bytes": ser_c,
+            "physical_compact_bpw": round(8.0 * ser_c / n, 5) if n else 0.0,
+            "physical_compact_reduction_pct": round(100.0 * (1 - ser_c / (2.0 * n)), 3) if n else 0.0,
             "not_exact": [r["name"] for r in recs if not r["exact"]],
         }
     return out

@@ -42,6 +42,7 @@ class Info(ctypes.Structure):
         ("bytes_codes", ctypes.c_uint64), ("bytes_raw", ctypes.c_uint64), ("bytes_index", ctypes.c_uint64),
         ("bytes_escapes", ctypes.c_uint64), ("serialized_bytes", ctypes.c_uint64),
         ("entropy_bpw", ctypes.c_double), ("physical_bpw", ctypes.c_double),
+        ("serialized_compact_bytes", ctypes.c_uint64), ("physical_compact_bpw", ctypes.c_double),
     ]
 
     def as_dict(self) -> dict:
@@ -79,6 +80,7 @@ def lib():
                                      ctypes.c_int, P]
     L.wcomp_info.argtypes = [P, ctypes.POINTER(Info)]
     L.wcomp_serialize.argtypes = [P, P, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), P]
+    L.wcomp_serialize_compact.argtypes = [P, P, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), P]
     L.wcomp_deserialize.argtypes = [P, ctypes.c_uint64, P, ctypes.POINTER(P)]
     L.wcomp_free.argtypes = [P, P]
     L.wcomp_free.restype = None
@@ -92,7 +94,8 @@ def lib():
     for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
                  "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
                  "wcomp_decode_batched",
-                 "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_deserialize", "wcomp_version"):
+                 "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_serialize_compact",
+                 "wcomp_deserialize", "wcomp_version"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -328,11 +331,14 @@ def gemv_batched(cs: Sequence[Container], xs: Sequence[torch.Tensor], ys: Option
     return ys
 
 
-def serialize(c: Container, stream=None) -> bytes:
+def serialize(c: Container, stream=None, compact: bool = False) -> bytes:
+    """Container bytes: format version 1, or version 2 (compact) with compact=True."""
+    fn = lib().wcomp_serialize_compact if compact else lib().wcomp_serialize
+    name = "wcomp_serialize_compact" if compact else "wcomp_serialize"
     n = ctypes.c_uint64()
-    _check(lib().wcomp_serialize(P(c.handle), None, 0, ctypes.byref(n), P(_stream(stream))), "wcomp_serialize")
+    _check(fn(P(c.handle), None, 0, ctypes.byref(n), P(_stream(stream))), name)
     buf = ctypes.create_string_buffer(n.value)
-    _check(lib().wcomp_serialize(P(c.handle), buf, n.value, ctypes.byref(n), P(_stream(stream))), "wcomp_serialize")
+    _check(fn(P(c.handle), buf, n.value, ctypes.byref(n), P(_stream(stream))), name)
     return buf.raw[: n.value]
 
 

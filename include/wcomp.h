@@ -90,6 +90,8 @@ typedef struct {
   uint64_t serialized_bytes; /* header + padded payload */
   double entropy_bpw;        /* 4 + raw bits + (E + 15) * symbol bits / n */
   double physical_bpw;       /* 8 * serialized_bytes / n */
+  uint64_t serialized_compact_bytes; /* header + padded payload of the compact form */
+  double physical_compact_bpw;       /* 8 * serialized_compact_bytes / n */
 } wcomp_info_t;
 
 /*
@@ -215,13 +217,35 @@ WCOMP_API int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_t
                     void* stream);
 
 /*
- * Rebuild a container from serialized bytes (host buffer).  The header, both
- * checksums, the section sizes, the escape positions (strictly ascending,
- * below n), both escape indexes and the agreement between escape codes and
- * positions are validated on the host before anything is copied to the
- * device; any mismatch returns WCOMP_ECORRUPT ("inject corruption" and
- * "validate hashes", wavect page, "Un piloto de producción de 14 días").
+ * Serialize to the compact form (format version 2): the same header, then
+ * the code stream, the raw bytes (byte-split) or the three K15 mantissa
+ * planes, one little-endian uint16 escape count per 8192-element tile, and
+ * the escape symbols in ascending position order (byte-split: one byte, the
+ * high byte; K15: the 9-bit sign+exponent symbol, packed least significant
+ * bit first so that symbol r occupies stream bits 9r .. 9r+8).  Positions,
+ * the row index and the K15 escape mantissas are implied (by the codes 15
+ * and the planes), so the physical size tracks the bits/weight accounting of
+ * forgeeks page "Prueba de GLM-5.2 reduce la memoria BF16 en casi un 25%",
+ * section "Cómo funciona la compresión", which counts each escape at its
+ * symbol width.  Sections are padded to 32 bytes with zeros.  With host_buf
+ * == NULL only *len is set.  Returns WCOMP_EINVAL if cap is too small.
  * Synchronizes `stream`.
+ */
+WCOMP_API int wcomp_serialize_compact(const wcomp_container* c, void* host_buf, uint64_t cap, uint64_t* len,
+                                      void* stream);
+
+/*
+ * Rebuild a container from serialized bytes (host buffer), either form.
+ * Version 1: the header, both checksums, the section sizes, the escape
+ * positions (strictly ascending, below n), both escape indexes and the
+ * agreement between escape codes and positions are validated on the host.
+ * Version 2 (compact): the header, both checksums and the section sizes are
+ * validated, the positions are rebuilt from the codes 15 and must number E,
+ * and every tile's escape count must match.  Nothing is copied to the device
+ * unless every check passes; any mismatch returns WCOMP_ECORRUPT ("inject
+ * corruption" and "validate hashes", wavect page, "Un piloto de producción
+ * de 14 días").  Both forms give the same device container.  Synchronizes
+ * `stream`.
  */
 WCOMP_API int wcomp_deserialize(const void* host_buf, uint64_t len, void* stream, wcomp_container** out);
 

@@ -130,3 +130,41 @@ def test_semantic_corruption_with_valid_checksums(lib):
     struct.pack_into("<H", bad, 42, t0)
     _recrc(bad)
     assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_host_validation_of_compact_form(lib, scheme):
+    """The compact form (version 2) is validated on the host like version 1:
+    intact oracle bytes pass, flipped bits and count mismatches with re-computed
+    checksums are rejected before any device call."""
+    import struct
+    w = synth.gen_weights_np(synth.WeightSpec("t", 8, 4096, "t4", 0.02, 0.02, "normal", 1.0, seed=7))
+    c = O.encode(w, scheme)
+    assert c.E >= 2
+    buf = bytearray(O.serialize_compact(c))
+    assert _deser_status(lib, bytes(buf)) != wcomp.ECORRUPT
+    rng = np.random.default_rng(2)
+    for off in [4, 8, 24, 72, 80] + list(rng.integers(96, len(buf), size=12)):
+        bad = bytearray(buf)
+        bad[off] ^= 0x10
+        assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    assert _deser_status(lib, bytes(buf[:-32])) == wcomp.ECORRUPT
+    sizes = O.section_sizes_compact(c.scheme, c.N, c.K, c.E)
+    off = {}
+    p = 96
+    for name, sz in sizes:
+        off[name] = p
+        p += O._pad(sz)
+    # an escape code cleared: fewer codes 15 than E
+    bad = bytearray(buf)
+    i = int(c.esc_pos[0])
+    bad[off["codes"] + i // 2] &= 0x0F if i % 2 else 0xF0
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+    # a tile count changed while E stays the same
+    bad = bytearray(buf)
+    t0 = struct.unpack_from("<H", bad, off["tile_count"])[0]
+    struct.pack_into("<H", bad, off["tile_count"], t0 + 1)
+    struct.pack_into("<H", bad, off["tile_count"] + 2, struct.unpack_from("<H", bad, off["tile_count"] + 2)[0] - 1)
+    _recrc(bad)
+    assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT

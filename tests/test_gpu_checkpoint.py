@@ -54,6 +54,9 @@ def test_checkpoint_streamed_full(W, tmp_path):
     assert 12.0 < bs["entropy_bpw"] < 12.05
     assert 11.1 < k15["entropy_bpw"] < 11.35
     assert bs["physical_bpw"] < 12.1
+    # the compact form's physical size tracks the accounting (no positions, 9-bit K15 symbols)
+    assert bs["physical_compact_bpw"] - bs["entropy_bpw"] < 0.02
+    assert k15["physical_compact_bpw"] - k15["entropy_bpw"] < 0.02
     # resume: everything is in the log, nothing is redone
     lines = open(log).read().splitlines()
     assert len(lines) == 2 * 1923
@@ -75,7 +78,9 @@ def test_checkpoint_small_shapes_match_oracle(W):
         w_np = host(w).reshape(s.N, s.K)
         for scheme in O.SCHEMES:
             c = W.encode(w, scheme)
-            assert W.serialize(c) == O.serialize(O.encode(w_np, scheme))
+            ref = O.encode(w_np, scheme)
+            assert W.serialize(c) == O.serialize(ref)
+            assert W.serialize(c, compact=True) == O.serialize_compact(ref)
             c.free()
 
 

@@ -55,6 +55,7 @@ def run_workload(W, specs, schemes, batches, n_oracle_shapes=1, sample_rows=48):
             w_np = host(ws[i]).reshape(s.N, s.K)
             ref = O.encode(w_np, scheme)
             assert W.serialize(cs[i]) == O.serialize(ref)
+            assert W.serialize(cs[i], compact=True) == O.serialize_compact(ref)
             seen[(s.N, s.K)] = (i, ref)
         for B in batches:
             xs_np = [synth.gen_x_np(B, s.K, 9000 + i) for i, s in enumerate(specs)]

@@ -68,9 +68,17 @@ def test_container_and_decode_bit_exact(W, case, scheme):
     assert inf["n_escapes"] == ref.E
     assert inf["table"] == [int(t) for t in ref.table]
     assert W.serialize(c) == O.serialize(ref)
+    compact = O.serialize_compact(ref)
+    assert W.serialize(c, compact=True) == compact
+    assert inf["serialized_compact_bytes"] == len(compact)
     out = W.decode(c)
     assert np.array_equal(host(out).reshape(w.shape), w)
     c.free()
+    # the compact bytes load back into the same device container
+    c2 = W.deserialize(compact)
+    assert W.serialize(c2) == O.serialize(ref)
+    assert np.array_equal(host(W.decode(c2)).reshape(w.shape), w)
+    c2.free()
 
 
 @pytest.mark.parametrize("scheme", O.SCHEMES)
@@ -101,6 +109,27 @@ def test_deserialize_roundtrip_on_gpu(W, scheme):
     bad[200] ^= 1
     with pytest.raises(W.CorruptContainer):
         W.deserialize(bytes(bad))
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_compact_form_on_gpu(W, scheme):
+    """Library-made compact bytes load back (oracle and library agree both ways),
+    and a container loaded from them runs the fused GEMV like the original."""
+    spec = synth.WeightSpec("d", 64, 2048, "t4", 0.02, 0.01, "normal", 1.0, seed=14)
+    w = synth.gen_weights_np(spec)
+    c = W.encode(dev(w), scheme)
+    buf = W.serialize(c, compact=True)
+    back = O.deserialize(buf)
+    assert O.serialize(back) == W.serialize(c)
+    c2 = W.deserialize(buf)
+    x = synth.gen_x_np(4, spec.K, 15)
+    assert torch.equal(W.gemv(c2, dev(x)), W.gemv(c, dev(x)))
+    bad = bytearray(buf)
+    bad[300] ^= 1
+    with pytest.raises(W.CorruptContainer):
+        W.deserialize(bytes(bad))
+    c.free()
+    c2.free()
 
 
 @pytest.mark.parametrize("scheme", O.SCHEMES)
