@@ -224,32 +224,52 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
   __syncthreads();
   if (g < G) {
     const uint64_t base = g * kGroup;
-    uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    uint32_t a[4] = {0, 0, 0, 0}, b[2] = {0, 0}, c = 0;
+    // lo[q]: low bytes of elements 4q .. 4q+3 (one word per quad)
+    uint32_t lo[8];
 #pragma unroll
-    for (int e = 0; e < kGroup; ++e) {
-      const uint32_t v = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFF;
-      const bool valid = base + e < n;
-      uint32_t code = lut[v >> SHIFT];
-      code = valid ? code : 0u;
-      esc += (code == kEscape);
-      cw[e >> 3] |= code << (4 * (e & 7));
-      const int q = e >> 2, ln = e & 3;
-      if (SCHEME == WCOMP_BYTESPLIT) {
-        r[e >> 2] |= (valid ? (v & 0xFF) : 0u) << (8 * (e & 3));
-      } else {
-        const uint32_t m = valid ? (v & 0x7F) : 0u;
-        a[q >> 1] |= (m & 0xF) << (8 * ln + 4 * (q & 1));
-        b[q >> 2] |= ((m >> 4) & 0x3) << (8 * ln + 2 * (q & 3));
-        c |= ((m >> 6) & 0x1) << (8 * ln + q);
+    for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
+    // codes: element e at bits 4 (e mod 8) of cw[e / 8]; the symbol of an
+    // element pair word is bits 8.. (byte-split) or 7.. (K15) of each half
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t s0 = (wv[k] >> SHIFT) & (NB - 1), s1 = wv[k] >> (16 + SHIFT);
+      const uint32_t c0 = lut[s0], c1 = lut[s1];
+      cw[k >> 2] += (c0 | (c1 << 4)) << (8 * (k & 3));
+    }
+    if (base + kGroup > n) {
+      // the tensor's last group: elements past n get code 0 (the source words were zero-filled)
+      const uint32_t valid = uint32_t(n - base);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int keep = int(valid) - 8 * k;
+        cw[k] &= keep >= 8 ? 0xFFFFFFFFu : keep <= 0 ? 0u : (1u << (4 * keep)) - 1u;
       }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t c = cw[k];
+      esc += __popc(c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u);
     }
     uint8_t* m = d.main;
     *reinterpret_cast<uint4*>(m + d.off_codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     if (SCHEME == WCOMP_BYTESPLIT) {
-      *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(r[0], r[1], r[2], r[3]);
-      if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(r[4], r[5], r[6], r[7]);
+      *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     } else {
+      // K15 planes from the mantissa bytes (bit 7 of a low byte is exponent
+      // bit 0 and is never selected): plane A word q/2 takes bits 0..3 of
+      // quad q (high nibble for odd q), plane B word q/4 bits 4..5 at bit
+      // offset 2 (q mod 4), plane C bit 6 at bit offset q of every byte
+      uint32_t a[4], b[2] = {0u, 0u}, c = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = (lo[2 * i] & 0x0F0F0F0Fu) | ((lo[2 * i + 1] << 4) & 0xF0F0F0F0u);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = q & 3;
+        b[q >> 2] |= j <= 2 ? ((lo[q] >> (4 - 2 * j)) & (0x03030303u << (2 * j)))
+                            : ((lo[q] << 2) & 0xC0C0C0C0u);
+        c |= q <= 6 ? ((lo[q] >> (6 - q)) & (0x01010101u << q)) : ((lo[q] << 1) & 0x80808080u);
+      }
       *reinterpret_cast<uint4*>(m + d.off_a + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
       *reinterpret_cast<uint2*>(m + d.off_b + 8 * g) = make_uint2(b[0], b[1]);
       *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;
