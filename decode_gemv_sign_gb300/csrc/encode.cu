@@ -94,9 +94,27 @@ __global__ void __launch_bounds__(256) hist_kernel(const __grid_constant__ EncBa
   const int lane = threadIdx.x & 31;
   const uint32_t col = lane & 15, inc = lane < 16 ? 1u : 65536u;
   const uint64_t chunks = cdiv(d.n, 8);
-  for (uint64_t ch = uint64_t(blk) * blockDim.x + threadIdx.x; ch < chunks; ch += uint64_t(nblk) * blockDim.x) {
+  const uint64_t stride = uint64_t(nblk) * blockDim.x;
+  const uint64_t full = d.aligned ? d.n / 8 : 0;  // chunks of 8 that take one 16-byte load
+  uint64_t ch = uint64_t(blk) * blockDim.x + threadIdx.x;
+  // four loads in flight before their counts
+  for (; ch + 3 * stride < full; ch += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(d.w + (ch + u * stride) * 8);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        atomicAdd(&h[((wd[j] & 0xFFFF) >> SHIFT) * 16 + col], inc);
+        atomicAdd(&h[(wd[j] >> (16 + SHIFT)) * 16 + col], inc);
+      }
+    }
+  }
+  for (; ch < chunks; ch += stride) {
     const uint64_t base = ch * 8;
-    if (d.aligned && base + 8 <= d.n) {
+    if (ch < full) {
       const uint4 v = ld_stream_v4(d.w + base);
       const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -281,13 +299,21 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
   const uint32_t total = block_total_256(red);
   if (threadIdx.x == 0) reinterpret_cast<uint32_t*>(d.main + d.off_tile)[tile] = total;
   if (esc && total <= d.stash_cap) {
+    // visit only the escaped elements: the set bits of each word's code-15
+    // mask (codes past n were cleared, so every visited element is valid)
     uint64_t o = uint64_t(tile) * d.stash_cap + before;
     const uint64_t base = g * kGroup;
 #pragma unroll
-    for (int e = 0; e < kGroup; ++e) {
-      if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape && base + e < n) {
-        const uint32_t v = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFF;
-        d.stash_pos[o] = uint32_t(base + e);
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t c = cw[k];
+      uint32_t m = c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u;
+      while (m) {
+        const int j = (__ffs(m) - 1) >> 2;
+        m &= m - 1;
+        const uint32_t pw = (j >> 1) == 0 ? wv[4 * k] : (j >> 1) == 1 ? wv[4 * k + 1]
+                            : (j >> 1) == 2 ? wv[4 * k + 2] : wv[4 * k + 3];
+        const uint32_t v = (pw >> (16 * (j & 1))) & 0xFFFF;
+        d.stash_pos[o] = uint32_t(base + 8 * k + j);
         d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
         ++o;
       }
