@@ -202,12 +202,41 @@ __device__ __forceinline__ void load_slice(const ChunkPtrs& q, ChunkBuf& b) {
   }
 }
 
-// ADDR 1: per-chunk base addresses with immediate slice offsets; ADDR 0: the
-// address of every slice computed on its own (fewer live registers, which
-// some instantiations schedule better).
+// Loads of one row's chunk in address form ADDR (see addr_mode).
 template <int SRC, bool FULL, int ADDR>
 __device__ __forceinline__ void load_chunk(const Streams& d, uint64_t e_base, uint32_t vmask, int lane,
                                            ChunkBuf& b) {
+  if (ADDR == 2) {
+    // lane l holds elements 32 l .. +31 of the chunk (one whole group); in a
+    // partial chunk vmask is 0xF or 0 per lane
+    if (!FULL && !vmask) return;
+    const uint64_t e = e_base + 32 * uint64_t(lane);
+    if (SRC == kPlain) {
+      uint32_t r[8];
+      ld_stream_v8(d.raw + 2 * e, r);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) b.v[k] = r[k];
+      ld_stream_v8(d.raw + 2 * e + 32, r);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) b.v[8 + k] = r[k];
+      return;
+    }
+    const uint4 c = ld_stream_v4(d.codes + (e >> 1));
+    b.v[0] = c.x; b.v[1] = c.y; b.v[2] = c.z; b.v[3] = c.w;
+    if (SRC == kBytesplit) {
+      uint32_t r[8];
+      ld_stream_v8(d.raw + e, r);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) b.v[4 + k] = r[k];
+    } else {
+      const uint4 a = ld_stream_v4(d.pa + (e >> 1));
+      b.v[4] = a.x; b.v[5] = a.y; b.v[6] = a.z; b.v[7] = a.w;
+      const uint2 bb = ld_stream_v2(d.pb + (e >> 2));
+      b.v[8] = bb.x; b.v[9] = bb.y;
+      b.v[12] = ld_stream_u32(d.pc + (e >> 3));
+    }
+    return;
+  }
   if (ADDR == 0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -270,6 +299,29 @@ __device__ __forceinline__ void slice_pairs(const RegTable& t, const ChunkBuf& b
   w[3] = prmt(l1, h1, 0x7362);
 }
 
+// K15 pairs of slice I of a lane that holds a whole 32-element group (its
+// four slices are the group's four quarters, so the plane bit positions are
+// compile-time constants): code word v[I], plane A word v[4 + I], plane B
+// word v[8 + I / 2], plane C word v[12].
+template <int I>
+__device__ __forceinline__ void group_slice_pairs_k15(const RegTable& t, const ChunkBuf& b, uint32_t (&w)[4]) {
+  const uint32_t cw = b.v[I];
+  const QuadMasks m = code_masks(cw);
+  const uint32_t m7 = cw & 0x77777777u;
+  uint32_t h0, h1, e0, e1;
+  lookup8(t.hi, m7, m, h0, h1);
+  lookup8(t.e0, m7, m, e0, e1);
+  const uint32_t A = b.v[4 + I], Bw = b.v[8 + (I >> 1)], C = b.v[12];
+  constexpr int sb0 = 4 * (I & 1), q0 = 2 * I;
+  const uint32_t l0 = (A & 0x0F0F0F0Fu) | (((Bw >> sb0) << 4) & 0x30303030u) | (((C >> q0) << 6) & 0x40404040u) | e0;
+  const uint32_t l1 = ((A >> 4) & 0x0F0F0F0Fu) | (((Bw >> (sb0 + 2)) << 4) & 0x30303030u) |
+                      (((C >> (q0 + 1)) << 6) & 0x40404040u) | e1;
+  w[0] = prmt(l0, h0, 0x5140);
+  w[1] = prmt(l0, h0, 0x7362);
+  w[2] = prmt(l1, h1, 0x5140);
+  w[3] = prmt(l1, h1, 0x7362);
+}
+
 template <int SRC, int BT, int R, int MODE, bool FULL, int ADDR>
 __device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t* __restrict__ xc, int64_t K, int B,
                                               const ChunkBuf (&buf)[R], const bool (&live)[R], uint32_t vmask,
@@ -281,12 +333,16 @@ __device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t*
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
       if (b < B) {
-        const uint16_t* xb = xc + int64_t(b) * K + 8 * lane;
-        const uint4 v = ADDR == 0 ? ld_x_v4(xb + kSlice * i)
-                        : i == 0  ? ld_x_v4_at<0>(xb)
-                        : i == 1  ? ld_x_v4_at<2 * kSlice>(xb)
-                        : i == 2  ? ld_x_v4_at<4 * kSlice>(xb)
-                                  : ld_x_v4_at<6 * kSlice>(xb);
+        const uint16_t* xb = xc + int64_t(b) * K + (ADDR == 2 ? 32 : 8) * lane;
+        const uint4 v = ADDR == 2 ? (i == 0   ? ld_x_v4_at<0>(xb)
+                                     : i == 1 ? ld_x_v4_at<16>(xb)
+                                     : i == 2 ? ld_x_v4_at<32>(xb)
+                                              : ld_x_v4_at<48>(xb))
+                        : ADDR == 0 ? ld_x_v4(xb + kSlice * i)
+                        : i == 0    ? ld_x_v4_at<0>(xb)
+                        : i == 1    ? ld_x_v4_at<2 * kSlice>(xb)
+                        : i == 2    ? ld_x_v4_at<4 * kSlice>(xb)
+                                    : ld_x_v4_at<6 * kSlice>(xb);
         xw[b][0] = v.x; xw[b][1] = v.y; xw[b][2] = v.z; xw[b][3] = v.w;
       } else {
         xw[b][0] = xw[b][1] = xw[b][2] = xw[b][3] = 0u;
@@ -306,7 +362,12 @@ __device__ __forceinline__ void compute_chunk(const RegTable& t, const uint16_t*
     for (int j = 0; j < R; ++j) {
       if (!live[j]) continue;
       uint32_t w[4];
-      if (i == 0) slice_pairs<SRC, 0>(t, buf[j], lane, w);
+      if (ADDR == 2 && SRC == kK15) {
+        if (i == 0) group_slice_pairs_k15<0>(t, buf[j], w);
+        else if (i == 1) group_slice_pairs_k15<1>(t, buf[j], w);
+        else if (i == 2) group_slice_pairs_k15<2>(t, buf[j], w);
+        else group_slice_pairs_k15<3>(t, buf[j], w);
+      } else if (i == 0) slice_pairs<SRC, 0>(t, buf[j], lane, w);
       else if (i == 1) slice_pairs<SRC, 1>(t, buf[j], lane, w);
       else if (i == 2) slice_pairs<SRC, 2>(t, buf[j], lane, w);
       else slice_pairs<SRC, 3>(t, buf[j], lane, w);
@@ -379,7 +440,7 @@ struct UnitState {
   bool live[R];
 };
 
-template <int SRC, int R, bool AHEAD>
+template <int SRC, int R, bool AHEAD, int ADDR>
 __device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int lane, UnitState<R>& st, int start) {
   st.ti = owner(p.set_prefix, p.count, u, start);
   const TensorDesc& d = p.d[st.ti];
@@ -388,8 +449,12 @@ __device__ __forceinline__ void unit_state(const GemvBatch& p, uint32_t u, int l
   const uint32_t krem = uint32_t(d.K - int64_t(st.nchunks - 1) * kChunk);
   st.last_full = krem == kChunk;
   st.vlast = 0;
+  if (ADDR == 2) {
+    st.vlast = 32 * lane + 32 <= int(krem) ? 0xFu : 0u;  // the lane's group is whole or absent
+  } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) st.vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
+    for (int i = 0; i < 4; ++i) st.vlast |= (kSlice * i + 8 * lane + 8 <= int(krem) ? 1u : 0u) << i;
+  }
 #pragma unroll
   for (int j = 0; j < R; ++j) st.live[j] = st.r0 + j < d.N;
   // requested one unit ahead, so the row index is at hand when the unit starts
@@ -461,11 +526,16 @@ enum EscMode {
 #ifndef WCOMP_GEMV_ESC
 #define WCOMP_GEMV_ESC -1  // -1: the table below; 0..2 forces one mode everywhere
 #endif
+// Address forms of the FMA kernel: 0 every slice address computed on its
+// own, 1 per-chunk bases with immediate slice offsets, 2 one whole 32-element
+// group per lane (one wide load per stream and compile-time K15 plane shifts,
+// at the price of x loads strided by 64 bytes across lanes, which only pays
+// at B = 1 and only for K15's heavier decode).
 #ifndef WCOMP_GEMV_ADDR
-#define WCOMP_GEMV_ADDR -1  // -1: the table below; 0 or 1 forces one form everywhere
+#define WCOMP_GEMV_ADDR -1  // -1: the table below; 0..2 forces one form everywhere
 #endif
 constexpr int addr_mode(int src, int bt) {
-  return WCOMP_GEMV_ADDR >= 0 ? WCOMP_GEMV_ADDR : src == kPlain ? 0 : 1;
+  return WCOMP_GEMV_ADDR >= 0 ? WCOMP_GEMV_ADDR : src == kPlain ? 0 : src == kK15 && bt == 1 ? 2 : 1;
 }
 
 constexpr int esc_mode(int src, int bt) {
@@ -490,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
   if (u < total_units) {
     uint32_t u_next = grab(slot, lane);
     UnitState<R> cur, nxt;
-    unit_state<SRC, R, kAhead>(p, u, lane, cur, 0);
+    unit_state<SRC, R, kAhead, kAddr>(p, u, lane, cur, 0);
     // load cursor: the item after the one being computed
     ChunkBuf b0[R], b1[R];
     load_unit_chunk<SRC, R, kAddr>(p, cur, 0, lane, b0);
@@ -566,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // position of the item held in the "current" buffer
     uint32_t c = 0;
     bool have_next_unit = u_next < total_units;
-    if (have_next_unit) unit_state<SRC, R, kAhead>(p, u_next, lane, nxt, cur.ti);
+    if (have_next_unit) unit_state<SRC, R, kAhead, kAddr>(p, u_next, lane, nxt, cur.ti);
     // One step: request the item after (cur, c) into `ld`, compute (cur, c)
     // from `cb`, then advance.  Returns false when nothing is left.
     auto step = [&](ChunkBuf (&cb)[R], ChunkBuf (&ld)[R]) -> bool {
@@ -585,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
       begin_unit();
       u_next = grab(slot, lane);
       have_next_unit = u_next < total_units;
-      if (have_next_unit) unit_state<SRC, R, kAhead>(p, u_next, lane, nxt, cur.ti);
+      if (have_next_unit) unit_state<SRC, R, kAhead, kAddr>(p, u_next, lane, nxt, cur.ti);
       return true;
     };
     while (step(b0, b1) && step(b1, b0)) {
@@ -959,29 +1029,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// K15 pairs of slice I of a lane that holds a whole 32-element group (its
-// four slices are the group's four quarters, so the plane bit positions are
-// compile-time constants): code word v[I], plane A word v[4 + I], plane B
-// word v[8 + I / 2], plane C word v[12].
-template <int I>
-__device__ __forceinline__ void group_slice_pairs_k15(const RegTable& t, const ChunkBuf& b, uint32_t (&w)[4]) {
-  const uint32_t cw = b.v[I];
-  const QuadMasks m = code_masks(cw);
-  const uint32_t m7 = cw & 0x77777777u;
-  uint32_t h0, h1, e0, e1;
-  lookup8(t.hi, m7, m, h0, h1);
-  lookup8(t.e0, m7, m, e0, e1);
-  const uint32_t A = b.v[4 + I], Bw = b.v[8 + (I >> 1)], C = b.v[12];
-  constexpr int sb0 = 4 * (I & 1), q0 = 2 * I;
-  const uint32_t l0 = (A & 0x0F0F0F0Fu) | (((Bw >> sb0) << 4) & 0x30303030u) | (((C >> q0) << 6) & 0x40404040u) | e0;
-  const uint32_t l1 = ((A >> 4) & 0x0F0F0F0Fu) | (((Bw >> (sb0 + 2)) << 4) & 0x30303030u) |
-                      (((C >> (q0 + 1)) << 6) & 0x40404040u) | e1;
-  w[0] = prmt(l0, h0, 0x5140);
-  w[1] = prmt(l0, h0, 0x7362);
-  w[2] = prmt(l1, h1, 0x5140);
-  w[3] = prmt(l1, h1, 0x7362);
 }
 
 // A unit as the tensor-core kernel sees it.
