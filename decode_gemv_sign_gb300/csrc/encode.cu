@@ -203,122 +203,182 @@ __device__ __forceinline__ uint32_t block_total_256(const uint32_t* sm) {
 // code bytes, the raw bytes (byte-split) or the three mantissa planes (K15),
 // and the tile's escape count.
 // ---------------------------------------------------------------------------
+
+// The group's 32 source elements as 16 element-pair words (zero past n).
+__device__ __forceinline__ void load_group(const EncDesc& d, uint64_t g, uint32_t (&wv)[16]) {
+  const uint64_t n = d.n, base = g * kGroup;
+  if (d.aligned && base + kGroup <= n) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = ld_stream_v4(d.w + base + 8 * k);
+      wv[4 * k + 0] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint64_t i0 = base + 2 * k;
+      const uint32_t lo = i0 < n ? d.w[i0] : 0u, hi = i0 + 1 < n ? d.w[i0 + 1] : 0u;
+      wv[k] = lo | (hi << 16);
+    }
+  }
+}
+
+template <int SCHEME>
+__device__ __forceinline__ void load_lut(const EncDesc& d, uint8_t* lut) {
+  constexpr int NB = SCHEME == WCOMP_BYTESPLIT ? 256 : 512;
+  const uint8_t* lut_g = d.main + d.off_scratch + Scratch::lut;
+  for (int i = threadIdx.x; i < NB; i += blockDim.x) lut[i] = lut_g[i];
+}
+
+// Codes (cw: element e at bits 4 (e mod 8) of cw[e / 8]) and raw bytes /
+// planes of group g, written to the container; returns the escape count.
+template <int SCHEME>
+__device__ __forceinline__ uint32_t pack_group(const EncDesc& d, const uint8_t* lut, uint64_t g,
+                                               const uint32_t (&wv)[16], const uint32_t (&lo)[8],
+                                               uint32_t (&cw)[4]) {
+  constexpr int NB = SCHEME == WCOMP_BYTESPLIT ? 256 : 512;
+  constexpr int SHIFT = SCHEME == WCOMP_BYTESPLIT ? 8 : 7;
+  const uint64_t n = d.n, base = g * kGroup;
+  cw[0] = cw[1] = cw[2] = cw[3] = 0u;
+  // the symbol of an element pair word is bits 8.. (byte-split) or 7.. (K15) of each half
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t s0 = (wv[k] >> SHIFT) & (NB - 1), s1 = wv[k] >> (16 + SHIFT);
+    const uint32_t c0 = lut[s0], c1 = lut[s1];
+    cw[k >> 2] += (c0 | (c1 << 4)) << (8 * (k & 3));
+  }
+  if (base + kGroup > n) {
+    // the tensor's last group: elements past n get code 0 (the source words were zero-filled)
+    const uint32_t valid = uint32_t(n - base);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int keep = int(valid) - 8 * k;
+      cw[k] &= keep >= 8 ? 0xFFFFFFFFu : keep <= 0 ? 0u : (1u << (4 * keep)) - 1u;
+    }
+  }
+  uint32_t esc = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t c = cw[k];
+    esc += __popc(c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u);
+  }
+  uint8_t* m = d.main;
+  *reinterpret_cast<uint4*>(m + d.off_codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  if (SCHEME == WCOMP_BYTESPLIT) {
+    *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  } else {
+    // K15 planes from the mantissa bytes (bit 7 of a low byte is exponent
+    // bit 0 and is never selected): plane A word q/2 takes bits 0..3 of
+    // quad q (high nibble for odd q), plane B word q/4 bits 4..5 at bit
+    // offset 2 (q mod 4), plane C bit 6 at bit offset q of every byte
+    uint32_t a[4], b[2] = {0u, 0u}, c = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = (lo[2 * i] & 0x0F0F0F0Fu) | ((lo[2 * i + 1] << 4) & 0xF0F0F0F0u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = q & 3;
+      b[q >> 2] |= j <= 2 ? ((lo[q] >> (4 - 2 * j)) & (0x03030303u << (2 * j)))
+                          : ((lo[q] << 2) & 0xC0C0C0C0u);
+      c |= q <= 6 ? ((lo[q] >> (6 - q)) & (0x01010101u << q)) : ((lo[q] << 1) & 0x80808080u);
+    }
+    *reinterpret_cast<uint4*>(m + d.off_a + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
+    *reinterpret_cast<uint2*>(m + d.off_b + 8 * g) = make_uint2(b[0], b[1]);
+    *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;
+  }
+  return esc;
+}
+
+// Stash (position, value) of the group's escapes at slots before.. of the
+// tile's stash; visits only the set bits of each word's code-15 mask (codes
+// past n were cleared, so every visited element is valid).
+template <int SCHEME>
+__device__ __forceinline__ void stash_group(const EncDesc& d, uint32_t tile, uint64_t g, uint32_t before,
+                                            const uint32_t (&wv)[16], const uint32_t (&cw)[4]) {
+  uint64_t o = uint64_t(tile) * d.stash_cap + before;
+  const uint64_t base = g * kGroup;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t c = cw[k];
+    uint32_t m = c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u;
+    while (m) {
+      const int j = (__ffs(m) - 1) >> 2;
+      m &= m - 1;
+      const uint32_t pw = (j >> 1) == 0 ? wv[4 * k] : (j >> 1) == 1 ? wv[4 * k + 1]
+                          : (j >> 1) == 2 ? wv[4 * k + 2] : wv[4 * k + 3];
+      const uint32_t v = (pw >> (16 * (j & 1))) & 0xFFFF;
+      d.stash_pos[o] = uint32_t(base + 8 * k + j);
+      d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
+      ++o;
+    }
+  }
+}
+
 template <int SCHEME>
 __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint8_t lut[kMaxBins];
   __shared__ uint32_t red[kThreads / 32];
-  constexpr int NB = SCHEME == WCOMP_BYTESPLIT ? 256 : 512;
-  constexpr int SHIFT = SCHEME == WCOMP_BYTESPLIT ? 8 : 7;
   const int ti = find_owner(bt, blockIdx.x);
   const EncDesc& d = bt.d[ti];
   const uint32_t tile = blockIdx.x - bt.prefix[ti];
-  const uint64_t n = d.n;
-  const uint64_t G = cdiv(n, kGroup);
   const uint64_t g = uint64_t(tile) * kThreads + threadIdx.x;
-  uint32_t esc = 0;
-  uint32_t wv[16];
-  uint32_t cw[4] = {0, 0, 0, 0};
+  const bool live = g < cdiv(d.n, kGroup);
+  uint32_t wv[16], cw[4] = {0u, 0u, 0u, 0u}, esc = 0;
   // the source words are requested first, so their latency overlaps the
   // table's trip through shared memory
-  if (g < G) {
-    const uint64_t base = g * kGroup;
-    if (d.aligned && base + kGroup <= n) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = ld_stream_v4(d.w + base + 8 * k);
-        wv[4 * k + 0] = v.x; wv[4 * k + 1] = v.y; wv[4 * k + 2] = v.z; wv[4 * k + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint64_t i0 = base + 2 * k;
-        const uint32_t lo = i0 < n ? d.w[i0] : 0u, hi = i0 + 1 < n ? d.w[i0 + 1] : 0u;
-        wv[k] = lo | (hi << 16);
-      }
-    }
-  }
-  const uint8_t* lut_g = d.main + d.off_scratch + Scratch::lut;
-  for (int i = threadIdx.x; i < NB; i += blockDim.x) lut[i] = lut_g[i];
+  if (live) load_group(d, g, wv);
+  load_lut<SCHEME>(d, lut);
   __syncthreads();
-  if (g < G) {
-    const uint64_t base = g * kGroup;
-    // lo[q]: low bytes of elements 4q .. 4q+3 (one word per quad)
-    uint32_t lo[8];
+  if (live) {
+    uint32_t lo[8];  // low bytes of elements 4q .. 4q+3
 #pragma unroll
     for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
-    // codes: element e at bits 4 (e mod 8) of cw[e / 8]; the symbol of an
-    // element pair word is bits 8.. (byte-split) or 7.. (K15) of each half
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t s0 = (wv[k] >> SHIFT) & (NB - 1), s1 = wv[k] >> (16 + SHIFT);
-      const uint32_t c0 = lut[s0], c1 = lut[s1];
-      cw[k >> 2] += (c0 | (c1 << 4)) << (8 * (k & 3));
-    }
-    if (base + kGroup > n) {
-      // the tensor's last group: elements past n get code 0 (the source words were zero-filled)
-      const uint32_t valid = uint32_t(n - base);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int keep = int(valid) - 8 * k;
-        cw[k] &= keep >= 8 ? 0xFFFFFFFFu : keep <= 0 ? 0u : (1u << (4 * keep)) - 1u;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t c = cw[k];
-      esc += __popc(c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u);
-    }
-    uint8_t* m = d.main;
-    *reinterpret_cast<uint4*>(m + d.off_codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    if (SCHEME == WCOMP_BYTESPLIT) {
-      *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-    } else {
-      // K15 planes from the mantissa bytes (bit 7 of a low byte is exponent
-      // bit 0 and is never selected): plane A word q/2 takes bits 0..3 of
-      // quad q (high nibble for odd q), plane B word q/4 bits 4..5 at bit
-      // offset 2 (q mod 4), plane C bit 6 at bit offset q of every byte
-      uint32_t a[4], b[2] = {0u, 0u}, c = 0u;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = (lo[2 * i] & 0x0F0F0F0Fu) | ((lo[2 * i + 1] << 4) & 0xF0F0F0F0u);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int j = q & 3;
-        b[q >> 2] |= j <= 2 ? ((lo[q] >> (4 - 2 * j)) & (0x03030303u << (2 * j)))
-                            : ((lo[q] << 2) & 0xC0C0C0C0u);
-        c |= q <= 6 ? ((lo[q] >> (6 - q)) & (0x01010101u << q)) : ((lo[q] << 1) & 0x80808080u);
-      }
-      *reinterpret_cast<uint4*>(m + d.off_a + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
-      *reinterpret_cast<uint2*>(m + d.off_b + 8 * g) = make_uint2(b[0], b[1]);
-      *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;
-    }
+    esc = pack_group<SCHEME>(d, lut, g, wv, lo, cw);
   }
   // rank the escapes inside the tile; while the source words are still in
   // registers, stash (position, value) for the gather pass
   const uint32_t before = block_exclusive_256(esc, red);
   const uint32_t total = block_total_256(red);
   if (threadIdx.x == 0) reinterpret_cast<uint32_t*>(d.main + d.off_tile)[tile] = total;
-  if (esc && total <= d.stash_cap) {
-    // visit only the escaped elements: the set bits of each word's code-15
-    // mask (codes past n were cleared, so every visited element is valid)
-    uint64_t o = uint64_t(tile) * d.stash_cap + before;
-    const uint64_t base = g * kGroup;
+  if (esc && total <= d.stash_cap) stash_group<SCHEME>(d, tile, g, before, wv, cw);
+}
+
+// Both schemes of one tensor in one pass: a tile is read once and packed
+// into its byte-split and its K15 container.  bt.d[2i] is the byte-split job
+// and bt.d[2i + 1] its K15 twin; bt.prefix counts tiles per pair.  The two
+// escape counts share one block scan as 16-bit halves (a tile holds at most
+// 8192 escapes per scheme).
+__global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_constant__ EncBatch bt) {
+  __shared__ uint8_t lut0[256], lut1[512];
+  __shared__ uint32_t red[kThreads / 32];
+  int pi = 0;
+  while (2 * (pi + 1) < bt.count && bt.prefix[pi + 1] <= blockIdx.x) ++pi;
+  const EncDesc& d0 = bt.d[2 * pi];
+  const EncDesc& d1 = bt.d[2 * pi + 1];
+  const uint32_t tile = blockIdx.x - bt.prefix[pi];
+  const uint64_t g = uint64_t(tile) * kThreads + threadIdx.x;
+  const bool live = g < cdiv(d0.n, kGroup);
+  uint32_t wv[16], cw0[4] = {0u, 0u, 0u, 0u}, cw1[4] = {0u, 0u, 0u, 0u}, esc = 0;
+  if (live) load_group(d1, g, wv);
+  load_lut<WCOMP_BYTESPLIT>(d0, lut0);
+  load_lut<WCOMP_K15>(d1, lut1);
+  __syncthreads();
+  if (live) {
+    uint32_t lo[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t c = cw[k];
-      uint32_t m = c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u;
-      while (m) {
-        const int j = (__ffs(m) - 1) >> 2;
-        m &= m - 1;
-        const uint32_t pw = (j >> 1) == 0 ? wv[4 * k] : (j >> 1) == 1 ? wv[4 * k + 1]
-                            : (j >> 1) == 2 ? wv[4 * k + 2] : wv[4 * k + 3];
-        const uint32_t v = (pw >> (16 * (j & 1))) & 0xFFFF;
-        d.stash_pos[o] = uint32_t(base + 8 * k + j);
-        d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
-        ++o;
-      }
-    }
+    for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
+    esc = pack_group<WCOMP_BYTESPLIT>(d0, lut0, g, wv, lo, cw0);
+    esc |= pack_group<WCOMP_K15>(d1, lut1, g, wv, lo, cw1) << 16;
   }
+  const uint32_t before = block_exclusive_256(esc, red);
+  const uint32_t total = block_total_256(red);
+  if (threadIdx.x == 0) {
+    reinterpret_cast<uint32_t*>(d0.main + d0.off_tile)[tile] = total & 0xFFFF;
+    reinterpret_cast<uint32_t*>(d1.main + d1.off_tile)[tile] = total >> 16;
+  }
+  if ((esc & 0xFFFF) && (total & 0xFFFF) <= d0.stash_cap)
+    stash_group<WCOMP_BYTESPLIT>(d0, tile, g, before & 0xFFFF, wv, cw0);
+  if ((esc >> 16) && (total >> 16) <= d1.stash_cap) stash_group<WCOMP_K15>(d1, tile, g, before >> 16, wv, cw1);
 }
 
 // ---------------------------------------------------------------------------
@@ -637,13 +697,46 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     return fail(err);
   };
   if ((e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
-  // a3: pack (with the stash), then the tile scan
-  e = for_chunks(jobs, WCOMP_BYTESPLIT, [&](EncBatch& b) {
+  // a3: pack (with the stash), then the tile scan.  A byte-split job and a
+  // K15 job of the same tensor are packed together, reading the source once.
+  std::vector<Job> pairs, singles;  // pairs: byte-split, K15, byte-split, K15, ...
+  {
+    std::vector<char> paired(jobs.size(), 0);
+    for (size_t j = 0; j < jobs.size(); ++j) {
+      if (jobs[j].d.scheme != WCOMP_BYTESPLIT) continue;
+      for (size_t k = 0; k < jobs.size(); ++k)
+        if (!paired[k] && jobs[k].d.scheme == WCOMP_K15 && jobs[k].d.w == jobs[j].d.w &&
+            jobs[k].d.N == jobs[j].d.N && jobs[k].d.K == jobs[j].d.K) {
+          paired[j] = paired[k] = 1;
+          pairs.push_back(jobs[j]);
+          pairs.push_back(jobs[k]);
+          break;
+        }
+    }
+    for (size_t j = 0; j < jobs.size(); ++j)
+      if (!paired[j]) singles.push_back(jobs[j]);
+  }
+  for (size_t s0 = 0; s0 < pairs.size(); s0 += kMaxBatch) {
+    EncBatch b;
+    memset(&b, 0, sizeof(b));
+    b.count = int(std::min<size_t>(kMaxBatch, pairs.size() - s0));
+    uint32_t t = 0;
+    for (int j = 0; j < b.count; ++j) b.d[j] = pairs[s0 + j].d;
+    for (int i = 0; i < b.count / 2; ++i) {
+      b.prefix[i] = t;
+      t += b.d[2 * i].n_tiles;
+    }
+    b.prefix[b.count / 2] = t;
+    pack_twin_kernel<<<t, kThreads, 0, s>>>(b);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail2(e);
+  }
+  e = for_chunks(singles, WCOMP_BYTESPLIT, [&](EncBatch& b) {
     pack_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
   if (e != cudaSuccess) return fail2(e);
-  e = for_chunks(jobs, WCOMP_K15, [&](EncBatch& b) {
+  e = for_chunks(singles, WCOMP_K15, [&](EncBatch& b) {
     pack_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });

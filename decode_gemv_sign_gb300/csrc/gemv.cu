@@ -1172,6 +1172,32 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
     float acc[4];
     int par = 0;
     uint32_t grabbed = 0;
+    // This thread's first escape of the unit: position and value requested
+    // when the unit starts, its low byte and x value one k-block later, so the
+    // correction after the unit's barrier does not wait on a dependent load.
+    // Byte-split with 8 batch rows only: with 16 batch rows the extra live
+    // registers spill, and K15's many escapes per thread gain nothing from
+    // prefetching one (both measured slower).
+    constexpr bool kFirst = SRC == kBytesplit && XB == 8;
+    uint32_t f_pos = 0, f_val = 0, f_lo = 0, f_x = 0, steps_in_unit = 0;
+    bool f_ready = false;
+    auto request_first = [&]() {
+      f_ready = false;
+      steps_in_unit = 0;
+      if (!kFirst || cj >= cur.rows || cb >= B || ce0 + cq >= ce1) return;
+      const TensorDesc& d = p.d[cur.ti];
+      f_pos = d.esc_pos[ce0 + cq];
+      f_val = load_esc_val(d, ce0 + cq);
+    };
+    auto fetch_first = [&]() {
+      f_ready = true;
+      if (!kFirst || cj >= cur.rows || cb >= B || ce0 + cq >= ce1) return;
+      const TensorDesc& d = p.d[cur.ti];
+      const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
+      f_lo = SRC == kBytesplit ? uint32_t(d.raw[f_pos]) : 0u;
+      f_x = uint32_t(p.x[cur.ti][int64_t(cb) * d.K + int64_t(uint64_t(f_pos) - rowbase)]);
+    };
+    request_first();
     if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
     auto unit_end = [&]() {
       // partial tiles, escape corrections, fixed-order sums
@@ -1186,6 +1212,13 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
           const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
           const uint16_t* xb = p.x[cur.ti] + int64_t(cb) * d.K;
           uint32_t e = ce0 + cq;
+          if (kFirst && e < ce1) {
+            // the first one was requested while the unit streamed
+            if (!f_ready) fetch_first();
+            c = fmaf(__uint_as_float(f_x << 16),
+                     esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(f_val, f_lo), c);
+            e += cP;
+          }
           // four escapes at a time: their loads are independent of each other
           for (; e + 3 * cP < ce1; e += 4 * cP) {
             uint32_t pos[4], val[4], lo[4], xv[4];
@@ -1236,6 +1269,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
         const TensorDesc& d = p.d[cur.ti];
         mma_kblock<SRC, XB>(d.t, p.x[cur.ti], d.K, B, cur, kb, lane, cbuf, acc);
       }
+      if (kFirst && ++steps_in_unit == 2 && !f_ready) fetch_first();
       if (!last) {
         ++kb;
         return true;
@@ -1247,6 +1281,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       ce1 = ne1;
       kb = cur.kb0;
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      request_first();
       u_next = next_unit[par];
       par ^= 1;
       if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);

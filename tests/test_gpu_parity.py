@@ -255,6 +255,22 @@ def test_encode_batched_both_schemes_of_one_tensor(W):
     assert W.serialize(c1) == O.serialize(O.encode(w65, 1))
 
 
+def test_encode_twins_over_one_launch_and_unpaired(W):
+    # 20 tensors in both schemes (20 byte-split/K15 pairs: more than one twin
+    # launch carries), plus a third encode of one tensor that has no twin left
+    specs = [synth.WeightSpec(f"p{i}", 8 + i, 512 + 32 * i, "normal", 0.02, 0.01, "normal", 1.0, seed=1300 + i)
+             for i in range(20)]
+    ws = [synth.gen_weights_np(s) for s in specs]
+    wd = [dev(w) for w in ws]
+    tensors = [w for w in wd for _ in (0, 1)] + [wd[3]]
+    schemes = [0, 1] * len(wd) + [0]
+    cs = W.encode_batched(tensors, schemes)
+    for i, w in enumerate(ws):
+        assert W.serialize(cs[2 * i]) == O.serialize(O.encode(w, 0))
+        assert W.serialize(cs[2 * i + 1]) == O.serialize(O.encode(w, 1))
+    assert W.serialize(cs[-1]) == O.serialize(O.encode(ws[3], 0))
+
+
 def test_many_tensors_batch_over_limit(W):
     # more containers than one launch carries
     ws = [synth.gen_weights_np(synth.WeightSpec(f"m{i}", 16, 512, "normal", 0.02, 0.01, "normal", 1.0, seed=600 + i))
