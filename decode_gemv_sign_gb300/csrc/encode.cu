@@ -383,8 +383,7 @@ __global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_consta
 
 // ---------------------------------------------------------------------------
 // Exclusive scan of the per-tile escape counts, in place; entry n_tiles
-// receives E (also written to the tensor's summary).  One CTA per tensor, two
-// passes, no inter-block waits.
+// receives E.  One CTA per tensor, two passes, no inter-block waits.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t part[1024];
@@ -531,6 +530,28 @@ cudaError_t launch_zero(ZeroList& z, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Escapes a tile's stash holds (pack records them, compaction copies them;
+// a tile with more is ranked again from its codes).
+constexpr uint32_t kStashCap = 256;
+
+// Pinned host memory for one call's summaries, kept per host thread and
+// grown on demand.  A call returns only after its copy into it completed.
+Summary* pinned_summaries(int count) {
+  thread_local Summary* buf = nullptr;
+  thread_local int cap = 0;
+  if (count > cap) {
+    if (buf) cudaFreeHost(buf);
+    buf = nullptr;
+    cap = 0;
+    if (cudaMallocHost(reinterpret_cast<void**>(&buf), sizeof(Summary) * size_t(count)) != cudaSuccess) {
+      buf = nullptr;
+      return nullptr;
+    }
+    cap = count;
+  }
+  return buf;
+}
+
 int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks, const int* schemes, int count,
                 cudaStream_t s, wcomp_container** out) {
   for (int i = 0; i < count; ++i) out[i] = nullptr;
@@ -648,55 +669,47 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   });
   if (e != cudaSuccess) return fail(e);
 
-  // the one synchronization: escape counts and tables
-  std::vector<Summary> hs(count);
-  e = cudaMemcpyAsync(hs.data(), d_sum, sizeof(Summary) * count, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(e);
-  cudaFreeAsync(d_sum, s);
-  d_sum = nullptr;
-
-  // escape streams and the per-tile stash, sized from E: room for twice the
-  // mean escapes per tile plus 64 (a tile that overflows is ranked again)
+  // Pack does not need E: its stash holds a fixed number of escapes per
+  // tile (a tile with more is ranked again by the compaction), so pack and
+  // the tile scan are queued before the host waits for E, and the wait (on
+  // an event after the summaries' copy, not on the stream) overlaps them.
   uint64_t stash_entries = 0;
-  std::vector<uint64_t> stash_off(count, 0);
-  for (int i = 0; i < count; ++i) {
-    wcomp_container* c = jobs[i].c;
-    memcpy(c->table, hs[i].table, sizeof(c->table));
-    Layout& L = c->L;
-    L.compute(L.scheme, L.N, L.K, hs[i].E);
-    EncDesc& d = jobs[i].d;
-    d.E = L.E;
-    d.off_pos = L.off_pos;
-    d.off_val = L.off_val;
-    d.stash_cap = 0;
-    if (L.E) {
-      e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
-      if (e != cudaSuccess) return fail(e);
-      d.esc = c->d_esc;
-      add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
-      add_pad(z, c->d_esc, L.off_val, L.sz_val);
-      if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail(e);
-      const uint64_t mean = cdiv(L.E, L.n_tiles);
-      d.stash_cap = uint32_t(std::min<uint64_t>(kTile, (2 * mean + 64 + 31) & ~uint64_t(31)));
-      stash_off[i] = stash_entries;
-      stash_entries += uint64_t(d.stash_cap) * L.n_tiles;
-    }
-  }
+  for (int i = 0; i < count; ++i) stash_entries += uint64_t(kStashCap) * jobs[i].c->L.n_tiles;
   uint8_t* stash = nullptr;
-  if (stash_entries) {
-    e = pool_alloc(reinterpret_cast<void**>(&stash), stash_entries * 6, s);
-    if (e != cudaSuccess) return fail(e);
+  e = pool_alloc(reinterpret_cast<void**>(&stash), stash_entries * 6, s);
+  if (e != cudaSuccess) return fail(e);
+  {
+    uint64_t off = 0;
     for (int i = 0; i < count; ++i) {
-      jobs[i].d.stash_pos = reinterpret_cast<uint32_t*>(stash) + stash_off[i];
-      jobs[i].d.stash_val = reinterpret_cast<uint16_t*>(stash + 4 * stash_entries) + stash_off[i];
+      jobs[i].d.stash_cap = kStashCap;
+      jobs[i].d.stash_pos = reinterpret_cast<uint32_t*>(stash) + off;
+      jobs[i].d.stash_val = reinterpret_cast<uint16_t*>(stash + 4 * stash_entries) + off;
+      off += uint64_t(kStashCap) * jobs[i].c->L.n_tiles;
     }
   }
   auto fail2 = [&](cudaError_t err) -> int {
     if (stash) cudaFreeAsync(stash, s);
     return fail(err);
   };
-  if ((e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
+  // escape counts and tables to pinned host memory, then the event the host waits on
+  Summary* hs = pinned_summaries(count);
+  if (!hs) return fail2(cudaErrorMemoryAllocation);
+  cudaEvent_t ready = nullptr;
+  e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(hs, d_sum, sizeof(Summary) * count, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaEventRecord(ready, s);
+  if (e != cudaSuccess) {
+    if (ready) cudaEventDestroy(ready);
+    return fail2(e);
+  }
+  cudaFreeAsync(d_sum, s);
+  d_sum = nullptr;
+  // past this point the copy into the pinned buffer may be in flight: wait for it before leaving
+  auto fail3 = [&](cudaError_t err) -> int {
+    cudaEventSynchronize(ready);
+    cudaEventDestroy(ready);
+    return fail2(err);
+  };
   // a3: pack (with the stash), then the tile scan.  A byte-split job and a
   // K15 job of the same tensor are packed together, reading the source once.
   std::vector<Job> pairs, singles;  // pairs: byte-split, K15, byte-split, K15, ...
@@ -729,23 +742,46 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     b.prefix[b.count / 2] = t;
     pack_twin_kernel<<<t, kThreads, 0, s>>>(b);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return fail2(e);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail3(e);
   }
   e = for_chunks(singles, WCOMP_BYTESPLIT, [&](EncBatch& b) {
     pack_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail2(e);
+  if (e != cudaSuccess) return fail3(e);
   e = for_chunks(singles, WCOMP_K15, [&](EncBatch& b) {
     pack_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail2(e);
+  if (e != cudaSuccess) return fail3(e);
   e = for_chunks(jobs, -1, [&](EncBatch& b) {
     scan_kernel<<<b.count, 1024, 0, s>>>(b);
     count_launches(1);
   });
+  if (e != cudaSuccess) return fail3(e);
+  // the one synchronization: escape counts and tables
+  e = cudaEventSynchronize(ready);
+  cudaEventDestroy(ready);
   if (e != cudaSuccess) return fail2(e);
+  for (int i = 0; i < count; ++i) {
+    wcomp_container* c = jobs[i].c;
+    memcpy(c->table, hs[i].table, sizeof(c->table));
+    Layout& L = c->L;
+    L.compute(L.scheme, L.N, L.K, hs[i].E);
+    EncDesc& d = jobs[i].d;
+    d.E = L.E;
+    d.off_pos = L.off_pos;
+    d.off_val = L.off_val;
+    if (L.E) {
+      e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+      if (e != cudaSuccess) return fail2(e);
+      d.esc = c->d_esc;
+      add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
+      add_pad(z, c->d_esc, L.off_val, L.sz_val);
+      if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
+    }
+  }
+  if ((e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
   // a4: compaction for tensors with escapes; row indexes for all
   std::vector<Job> with_esc;
   for (auto& j : jobs)
