@@ -615,7 +615,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 200 for ours, so the timed region spans several clock "
+                         "samples; 10 for the reference arm, whose steps take seconds each)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -624,6 +626,8 @@ def main():
     if args.oracle_sample:
         print(json.dumps(oracle_sample_run()))
         return
+    if args.steps is None:
+        args.steps = 200 if args.impl == "ours" else 10
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
