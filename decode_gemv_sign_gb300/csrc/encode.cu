@@ -233,12 +233,9 @@ __device__ __forceinline__ void load_lut(const EncDesc& d, uint8_t* lut) {
 // Codes (cw: element e at bits 4 (e mod 8) of cw[e / 8]) and raw bytes /
 // planes of group g, written to the container; returns the escape count.
 template <int SCHEME>
-__device__ __forceinline__ uint32_t pack_group(const EncDesc& d, const uint8_t* lut, uint64_t g,
-                                               const uint32_t (&wv)[16], const uint32_t (&lo)[8],
-                                               uint32_t (&cw)[4]) {
+__device__ __forceinline__ void group_codes(const uint8_t* lut, const uint32_t (&wv)[16], uint32_t (&cw)[4]) {
   constexpr int NB = SCHEME == WCOMP_BYTESPLIT ? 256 : 512;
   constexpr int SHIFT = SCHEME == WCOMP_BYTESPLIT ? 8 : 7;
-  const uint64_t n = d.n, base = g * kGroup;
   cw[0] = cw[1] = cw[2] = cw[3] = 0u;
   // the symbol of an element pair word is bits 8.. (byte-split) or 7.. (K15) of each half
 #pragma unroll
@@ -247,6 +244,14 @@ __device__ __forceinline__ uint32_t pack_group(const EncDesc& d, const uint8_t* 
     const uint32_t c0 = lut[s0], c1 = lut[s1];
     cw[k >> 2] += (c0 | (c1 << 4)) << (8 * (k & 3));
   }
+}
+
+// Codes in cw are given; clears codes past n, writes the group's sections
+// and returns its escape count.
+template <int SCHEME>
+__device__ __forceinline__ uint32_t pack_group(const EncDesc& d, uint64_t g, const uint32_t (&lo)[8],
+                                               uint32_t (&cw)[4]) {
+  const uint64_t n = d.n, base = g * kGroup;
   if (base + kGroup > n) {
     // the tensor's last group: elements past n get code 0 (the source words were zero-filled)
     const uint32_t valid = uint32_t(n - base);
@@ -333,7 +338,8 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
     uint32_t lo[8];  // low bytes of elements 4q .. 4q+3
 #pragma unroll
     for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
-    esc = pack_group<SCHEME>(d, lut, g, wv, lo, cw);
+    group_codes<SCHEME>(lut, wv, cw);
+    esc = pack_group<SCHEME>(d, g, lo, cw);
   }
   // rank the escapes inside the tile; while the source words are still in
   // registers, stash (position, value) for the gather pass
@@ -349,7 +355,10 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
 // escape counts share one block scan as 16-bit halves (a tile holds at most
 // 8192 escapes per scheme).
 __global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_constant__ EncBatch bt) {
-  __shared__ uint8_t lut0[256], lut1[512];
+  // one table for both: entry s (a K15 symbol) holds the K15 code of s in its
+  // low nibble and the byte-split code of s >> 1 (the high byte) in its high
+  // nibble, so one lookup per element gives both codes
+  __shared__ uint8_t lut2[512];
   __shared__ uint32_t red[kThreads / 32];
   int pi = 0;
   while (2 * (pi + 1) < bt.count && bt.prefix[pi + 1] <= blockIdx.x) ++pi;
@@ -360,15 +369,25 @@ __global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_consta
   const bool live = g < cdiv(d0.n, kGroup);
   uint32_t wv[16], cw0[4] = {0u, 0u, 0u, 0u}, cw1[4] = {0u, 0u, 0u, 0u}, esc = 0;
   if (live) load_group(d1, g, wv);
-  load_lut<WCOMP_BYTESPLIT>(d0, lut0);
-  load_lut<WCOMP_K15>(d1, lut1);
+  {
+    const uint8_t* l0 = d0.main + d0.off_scratch + Scratch::lut;
+    const uint8_t* l1 = d1.main + d1.off_scratch + Scratch::lut;
+    for (int i = threadIdx.x; i < 512; i += blockDim.x) lut2[i] = uint8_t(l1[i] | (l0[i >> 1] << 4));
+  }
   __syncthreads();
   if (live) {
     uint32_t lo[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
-    esc = pack_group<WCOMP_BYTESPLIT>(d0, lut0, g, wv, lo, cw0);
-    esc |= pack_group<WCOMP_K15>(d1, lut1, g, wv, lo, cw1) << 16;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t c0 = lut2[(wv[k] >> 7) & 511u], c1 = lut2[wv[k] >> 23];
+      const uint32_t pair = c0 | (c1 << 8);  // K15 codes in bits 0-3 and 8-11, byte-split in 4-7 and 12-15
+      cw1[k >> 2] += ((pair & 0xFu) | ((pair >> 4) & 0xF0u)) << (8 * (k & 3));
+      cw0[k >> 2] += (((pair >> 4) & 0xFu) | ((pair >> 8) & 0xF0u)) << (8 * (k & 3));
+    }
+    esc = pack_group<WCOMP_BYTESPLIT>(d0, g, lo, cw0);
+    esc |= pack_group<WCOMP_K15>(d1, g, lo, cw1) << 16;
   }
   const uint32_t before = block_exclusive_256(esc, red);
   const uint32_t total = block_total_256(red);

@@ -1041,15 +1041,22 @@ struct MmaUnit {
   uint32_t nkb;      // k-blocks per row
 };
 
-__device__ __forceinline__ void mma_unit(const GemvBatch& p, uint32_t u, int warp, int start, MmaUnit& m) {
-  m.ti = owner(p.set_prefix, p.count, u, start);
+// The k-block range of this warp, derived from the tensor's K.
+__device__ __forceinline__ void mma_unit_range(const GemvBatch& p, int warp, MmaUnit& m) {
   const TensorDesc& d = p.d[m.ti];
-  m.r0 = int64_t(u - p.set_prefix[m.ti]) * 8;
-  m.rows = int(d.N - m.r0 < 8 ? d.N - m.r0 : 8);
   m.nkb = uint32_t(cdiv(uint64_t(d.K), kKBlock));
   m.kvalid = uint32_t(d.K - int64_t(m.nkb - 1) * kKBlock);
   m.kb0 = uint32_t(uint64_t(m.nkb) * warp / kMmaWarps);
   m.kb1 = uint32_t(uint64_t(m.nkb) * (warp + 1) / kMmaWarps);
+}
+
+// Tensor, first row and rows of unit u (the range is filled in separately,
+// so a unit held for later costs three values, not seven).
+__device__ __forceinline__ void mma_unit(const GemvBatch& p, uint32_t u, int start, MmaUnit& m) {
+  m.ti = owner(p.set_prefix, p.count, u, start);
+  const TensorDesc& d = p.d[m.ti];
+  m.r0 = int64_t(u - p.set_prefix[m.ti]) * 8;
+  m.rows = int(d.N - m.r0 < 8 ? d.N - m.r0 : 8);
 }
 
 // Loads of k-block kb of unit m for this lane: row g, elements 32 t .. +31 of
@@ -1159,11 +1166,12 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       e0 = d.row_index[m.r0 + cj];
       e1 = d.row_index[m.r0 + cj + 1];
     };
-    mma_unit(p, u, warp, 0, cur);
+    mma_unit(p, u, 0, cur);
+    mma_unit_range(p, warp, cur);
     row_escapes(cur, ce0, ce1);
     bool have_next = u_next < total_units;
     if (have_next) {
-      mma_unit(p, u_next, warp, cur.ti, nxt);
+      mma_unit(p, u_next, cur.ti, nxt);
       row_escapes(nxt, ne0, ne1);
     }
     ChunkBuf b0, b1;
@@ -1264,7 +1272,11 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       // request the item after (cur, kb), then compute (cur, kb)
       const bool last = kb + 1 >= cur.kb1;
       if (!last) load_kblock<SRC>(p, cur, kb + 1, g, t, lbuf);
-      else if (have_next && nxt.kb0 < nxt.kb1) load_kblock<SRC>(p, nxt, nxt.kb0, g, t, lbuf);
+      else if (have_next) {
+        MmaUnit first = nxt;
+        mma_unit_range(p, warp, first);
+        if (first.kb0 < first.kb1) load_kblock<SRC>(p, first, first.kb0, g, t, lbuf);
+      }
       if (kb < cur.kb1) {
         const TensorDesc& d = p.d[cur.ti];
         mma_kblock<SRC, XB>(d.t, p.x[cur.ti], d.K, B, cur, kb, lane, cbuf, acc);
@@ -1277,6 +1289,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       unit_end();
       if (!have_next) return false;
       cur = nxt;
+      mma_unit_range(p, warp, cur);
       ce0 = ne0;
       ce1 = ne1;
       kb = cur.kb0;
@@ -1287,7 +1300,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
       have_next = u_next < total_units;
       if (have_next) {
-        mma_unit(p, u_next, warp, cur.ti, nxt);
+        mma_unit(p, u_next, cur.ti, nxt);
         row_escapes(nxt, ne0, ne1);
       }
       return true;
