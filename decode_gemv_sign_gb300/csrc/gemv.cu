@@ -1483,9 +1483,11 @@ int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   return map_cuda(cudaGetLastError());
 }
 
-// Batches from this size up take the tensor-core kernel.  Byte-split decodes
-// cheaply enough that the FMA kernel keeps up to B = 4; K15's heavier decode
-// and the plain GEMV gain from B = 2.  WCOMP_GEMV_MMA_MIN_B overrides all.
+// Batches from this size up take the tensor-core kernel (measured on the
+// dense-layer set): the plain GEMV at every B (its wide per-lane loads and
+// x read by a quarter of the lanes beat the FMA kernel even at B = 1), K15
+// from B = 2, byte-split from B = 4 (its decode is cheap enough that the FMA
+// kernel keeps B = 1..2).  WCOMP_GEMV_MMA_MIN_B overrides all.
 #ifndef WCOMP_GEMV_MMA_MIN_B
 #define WCOMP_GEMV_MMA_MIN_B 0
 #endif
@@ -1493,7 +1495,7 @@ int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
 #define WCOMP_GEMV_MMA_MINB 3
 #endif
 constexpr int mma_min_batch(int src) {
-  return WCOMP_GEMV_MMA_MIN_B > 0 ? WCOMP_GEMV_MMA_MIN_B : src == kBytesplit ? 5 : 2;
+  return WCOMP_GEMV_MMA_MIN_B > 0 ? WCOMP_GEMV_MMA_MIN_B : src == kBytesplit ? 4 : src == kK15 ? 2 : 1;
 }
 
 // Rows per unit and CTAs per SM for each batch size (build-time tunables).
