@@ -148,6 +148,27 @@ def test_gemv_matches_oracle(W, scheme, B):
     c.free()
 
 
+@pytest.mark.parametrize("scheme", O.SCHEMES + (2,))
+@pytest.mark.parametrize("shape", [(37, 96), (64, 160), (9, 2080), (8, 32), (130, 1056)])
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 9, 16])
+def test_gemv_partial_blocks(W, scheme, shape, B):
+    """K not a multiple of the 1024-element chunk or the 128-element k-block
+    (partial last blocks, lanes past K, warps with no k-block at all when K <
+    1024) and N not a multiple of 8 (a partial 8-row unit), for both GEMV
+    kernels; scheme 2 is the plain BF16 GEMV."""
+    N, K = shape
+    spec = synth.WeightSpec("p", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=31 * N + K)
+    w = synth.gen_weights_np(spec)
+    x = synth.gen_x_np(B, K, 17 * B + K)
+    if scheme == 2:
+        y = W.gemv_bf16(dev(w), dev(x))
+    else:
+        c = W.encode(dev(w), scheme)
+        y = W.gemv(c, dev(x))
+        c.free()
+    check_gemv(y, O.gemv(w, x))
+
+
 @pytest.mark.parametrize("scheme", O.SCHEMES)
 @pytest.mark.parametrize("B", [1, 4, 16])
 def test_gemv_ragged_k_element_path(W, scheme, B):

@@ -37,7 +37,7 @@ def dev(a):
 
 @pytest.mark.parametrize("scheme", [0, 1])
 @pytest.mark.parametrize("B", [1, 4, 16])
-@pytest.mark.parametrize("shape", [(300, 2048), (37, 1000)])
+@pytest.mark.parametrize("shape", [(300, 2048), (37, 1000), (41, 2080)])
 def test_noalloc_matches_gemv_twice(W, scheme, B, shape):
     N, K = shape
     w = synth.gen_weights_np(synth.WeightSpec("na", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=7000 + B + N))
