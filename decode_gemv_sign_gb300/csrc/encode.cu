@@ -439,11 +439,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncB
 // back from the source.  Either way the stream ends up in ascending position
 // order.
 // ---------------------------------------------------------------------------
-template <int SCHEME>
+// Both schemes in one launch: the scheme is uniform per CTA (one tile of one tensor).
 __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t sm[kThreads / 32];
   const int ti = find_owner(bt, blockIdx.x);
   const EncDesc& d = bt.d[ti];
+  const int SCHEME = d.scheme;
   const uint32_t t = blockIdx.x - bt.prefix[ti];
   const uint32_t* tile_index = reinterpret_cast<const uint32_t*>(d.main + d.off_tile);
   const uint32_t first = tile_index[t], count = tile_index[t + 1] - first;
@@ -805,13 +806,8 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   std::vector<Job> with_esc;
   for (auto& j : jobs)
     if (j.d.E) with_esc.push_back(j);
-  e = for_chunks(with_esc, WCOMP_BYTESPLIT, [&](EncBatch& b) {
-    compact_kernel<WCOMP_BYTESPLIT><<<tiles_prefix(b), kThreads, 0, s>>>(b);
-    count_launches(1);
-  });
-  if (e != cudaSuccess) return fail2(e);
-  e = for_chunks(with_esc, WCOMP_K15, [&](EncBatch& b) {
-    compact_kernel<WCOMP_K15><<<tiles_prefix(b), kThreads, 0, s>>>(b);
+  e = for_chunks(with_esc, -1, [&](EncBatch& b) {
+    compact_kernel<<<tiles_prefix(b), kThreads, 0, s>>>(b);
     count_launches(1);
   });
   if (e != cudaSuccess) return fail2(e);
