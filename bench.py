@@ -228,11 +228,13 @@ def dist_env():
 
 
 def init_dist(world):
+    """NCCL on GPUs (one rank per GPU); gloo when the ranks have no GPU (host-side tests)."""
     if world <= 1:
         return None
+    import torch
     import torch.distributed as dist
 
-    dist.init_process_group("nccl")
+    dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return dist
 
 
@@ -241,24 +243,27 @@ def barrier(dist):
         dist.barrier()
 
 
-def allmax(dist, v: float) -> float:
-    if dist is None:
-        return v
+def _all_reduce(dist, v: float, op) -> float:
     import torch
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def allmax(dist, v: float) -> float:
+    return v if dist is None else _all_reduce(dist, v, dist.ReduceOp.MAX)
 
 
 def allsum(dist, v: float) -> float:
-    if dist is None:
-        return v
-    import torch
+    return v if dist is None else _all_reduce(dist, v, dist.ReduceOp.SUM)
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+
+def aggregate_rate(dist, local_bytes: float, local_ms: float) -> tuple:
+    """Whole-job rate of replicas: the bytes all ranks moved over the slowest rank's time."""
+    t_max = allmax(dist, local_ms)
+    return allsum(dist, local_bytes) / (t_max / 1e3) / 1e9, t_max
 
 
 # ---------------------------------------------------------------------------
@@ -419,7 +424,6 @@ def run_ours(args):
     launches = W.launch_count() - n0
     clk = clocks.stop()
     t_ms = start.elapsed_time(end)
-    t_ms_max = allmax(dist, t_ms)
 
     phase_ms = {}
     for marks in ev:
@@ -428,7 +432,7 @@ def run_ours(args):
     phase_ms = {k: v / args.steps for k, v in phase_ms.items()}
     bytes_ = hp.algorithmic_bytes()
     step_bytes = sum(bytes_.values())
-    value = allsum(dist, step_bytes * args.steps) / (t_ms_max / 1e3) / 1e9
+    value, t_ms_max = aggregate_rate(dist, step_bytes * args.steps, t_ms)
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, W, torch, hp, specs, dist)
