@@ -9,7 +9,13 @@
 // sin pérdida vs 8-bit GGUF", section "¿Qué significa “sin pérdida” para los
 // pesos de un LLM?": exact BF16 rebuilt in registers and used at once.
 //
-// Work decomposition.  A unit of work is a set of R consecutive rows of one
+// Two kernels compute it: the FMA kernel below (small batches of the
+// encoded sources) and the tensor-core kernel further down (larger batches,
+// and the plain GEMV at every batch); mma_min_batch() holds the measured
+// crossover per source.  Both take their units from the same kind of global
+// counter and give results independent of scheduling.
+//
+// FMA kernel.  A unit of work is a set of R consecutive rows of one
 // tensor; a launch covers the units of every tensor in the batch.  The grid is
 // persistent (as many CTAs as fit on the GPU at once) and every warp grabs
 // units from a global counter, one at a time, so the GPU drains evenly even
