@@ -1141,14 +1141,49 @@ __device__ __forceinline__ void mma_kblock(const RegTable& tab, const uint16_t* 
   }
 }
 
-template <int SRC, int XB, int MINB>
+// x transposed for the escape corrections: xt[i][k * XB + b] = x_i[b, k]
+// (zero for b >= B), so one thread reads every batch value of column k of
+// tensor i with one or two 16-byte loads.
+struct XtBatch {
+  uint16_t* p[kMaxBatch];
+  uint32_t kprefix[kMaxBatch + 1];  // first column of each tensor in the grid
+  int count;
+};
+
+template <int XB>
+__global__ void __launch_bounds__(256) transpose_x_kernel(const __grid_constant__ GemvBatch b,
+                                                          const __grid_constant__ XtBatch xt, int B) {
+  const uint32_t total = xt.kprefix[xt.count];
+  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += gridDim.x * blockDim.x) {
+    int i = 0;
+    while (i + 1 < xt.count && xt.kprefix[i + 1] <= c) ++i;
+    const int64_t K = b.d[i].K;
+    const uint32_t k = c - xt.kprefix[i];
+    const uint16_t* x = b.x[i];
+    uint32_t v[XB / 2];
+#pragma unroll
+    for (int q = 0; q < XB / 2; ++q) {
+      const uint32_t lo = 2 * q < B ? uint32_t(x[int64_t(2 * q) * K + k]) : 0u;
+      const uint32_t hi = 2 * q + 1 < B ? uint32_t(x[int64_t(2 * q + 1) * K + k]) : 0u;
+      v[q] = lo | (hi << 16);
+    }
+    uint4* out = reinterpret_cast<uint4*>(xt.p[i] + uint64_t(k) * XB);
+#pragma unroll
+    for (int q = 0; q < XB / 8; ++q) out[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+template <int SRC, int XB, int MINB, bool XT = false>
 __global__ void __launch_bounds__(kMmaThreads, MINB)
-    gemv_mma_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot) {
+    gemv_mma_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot,
+                    const __grid_constant__ XtBatch xt) {
   // Two sets, alternating by unit parity, so one barrier per unit suffices:
   // a set is rewritten two units later, after every thread has passed the
   // next unit's barrier and so finished reading it.
   __shared__ float part[2][kMmaWarps][32][4];
-  __shared__ float corr[2][kMmaThreads];
+  // per-thread corrections (x gathered per batch row), or with XT per-warp
+  // sums for every (batch, row) of the unit
+  __shared__ float corr[2][XT ? kMmaWarps * 16 * 8 : kMmaThreads];
   __shared__ uint32_t first_unit, next_unit[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -1220,7 +1255,43 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
       part[par][warp][lane][1] = acc[1];
       part[par][warp][lane][2] = acc[2];
       part[par][warp][lane][3] = acc[3];
-      {
+      if constexpr (XT) {
+        // thread (row j = cj, part q = tid / 8 of 32): every batch row at once
+        // from the transposed x; the four parts of a warp are summed by a
+        // fixed shuffle tree, the warps in order in the final sum
+        float cs[XB];
+#pragma unroll
+        for (int b = 0; b < XB; ++b) cs[b] = 0.f;
+        if (cj < cur.rows) {
+          const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
+          const uint16_t* xtb = xt.p[cur.ti];
+          for (uint32_t e = ce0 + (threadIdx.x >> 3); e < ce1; e += kMmaThreads / 8) {
+            const uint32_t pos = d.esc_pos[e];
+            const float delta = esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(
+                load_esc_val(d, e), SRC == kBytesplit ? uint32_t(d.raw[pos]) : 0u);
+            const uint4* xr = reinterpret_cast<const uint4*>(xtb + uint64_t(uint64_t(pos) - rowbase) * XB);
+#pragma unroll
+            for (int q = 0; q < XB / 8; ++q) {
+              const uint4 v = xr[q];
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                cs[8 * q + 2 * h] = fmaf(bf16_lo(w4[h]), delta, cs[8 * q + 2 * h]);
+                cs[8 * q + 2 * h + 1] = fmaf(bf16_hi(w4[h]), delta, cs[8 * q + 2 * h + 1]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < XB; ++b) {
+          cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 8);
+          cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 16);
+        }
+        if (lane < 8) {
+#pragma unroll
+          for (int b = 0; b < XB; ++b) corr[par][(warp * 16 + b) * 8 + lane] = cs[b];
+        }
+      } else {
         float c = 0.f;
         if (SRC != kPlain && cj < cur.rows && cb < B) {
           const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
@@ -1270,7 +1341,12 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
         float y = 0.f;
 #pragma unroll
         for (int w = 0; w < kMmaWarps; ++w) y += part[par][w][src_lane][reg];
-        for (int q = 0; q < cP; ++q) y += corr[par][(q * cbp + bb) * 8 + j];
+        if (XT) {
+#pragma unroll
+          for (int w = 0; w < kMmaWarps; ++w) y += corr[par][(w * 16 + bb) * 8 + j];
+        } else {
+          for (int q = 0; q < cP; ++q) y += corr[par][(q * cbp + bb) * 8 + j];
+        }
         p.y[cur.ti][int64_t(bb) * d.N + cur.r0 + j] = y;
       }
     };
@@ -1464,8 +1540,16 @@ int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   return map_cuda(cudaGetLastError());
 }
 
-template <int SRC, int XB, int MINB>
-int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+#ifndef WCOMP_GEMV_XT
+#define WCOMP_GEMV_XT 1  // K15's escape corrections read a transposed copy of x
+#endif
+
+// With the transposed x a thread reads all batch rows of an escape's column
+// at once: K15 (escape rate 1.7-3 %) gains from B = 3 (B = 8: 164 -> 131 us,
+// B = 16: 251 -> 167 us on the dense-layer set); at B = 2 the padded copy
+// costs more than it saves, and byte-split's few escapes gain nothing.
+template <int SRC, int XB, int MINB, bool kXt>
+int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
   uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
     b.set_prefix[j] = units;
@@ -1475,18 +1559,45 @@ int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   uint32_t* slot = nullptr;
   int st = counter_slot(dev, &slot);
   if (st != WCOMP_OK) return st;
+  auto kern = gemv_mma_kernel<SRC, XB, MINB, kXt>;
   static int per_sm_cache = 0;
   if (!per_sm_cache) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_mma_kernel<SRC, XB, MINB>, kMmaThreads, 0) !=
-            cudaSuccess ||
-        per_sm <= 0)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, 0) != cudaSuccess || per_sm <= 0)
       per_sm = 1;
     per_sm_cache = per_sm;
   }
-  gemv_mma_kernel<SRC, XB, MINB><<<per_sm_cache * sms, kMmaThreads, 0, s>>>(b, units, B, slot);
+  XtBatch xt;
+  memset(&xt, 0, sizeof(xt));
+  uint16_t* xt_mem = nullptr;
+  if (kXt) {
+    // x transposed into pool memory (freed in stream order after the GEMV)
+    uint64_t cols = 0;
+    for (int j = 0; j < b.count; ++j) {
+      xt.kprefix[j] = uint32_t(cols);
+      cols += uint64_t(b.d[j].K);
+    }
+    if (cols >= (uint64_t(1) << 32)) return WCOMP_EUNSUPPORTED;
+    xt.kprefix[b.count] = uint32_t(cols);
+    xt.count = b.count;
+    cudaError_t e = pool_alloc(reinterpret_cast<void**>(&xt_mem), cols * XB * sizeof(uint16_t), s);
+    if (e != cudaSuccess) return map_cuda(e);
+    for (int j = 0; j < b.count; ++j) xt.p[j] = xt_mem + uint64_t(xt.kprefix[j]) * XB;
+    const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(cols, 256), uint64_t(sms) * 8));
+    transpose_x_kernel<XB><<<blocks, 256, 0, s>>>(b, xt, B);
+    count_launches(1);
+  }
+  kern<<<per_sm_cache * sms, kMmaThreads, 0, s>>>(b, units, B, slot, xt);
   count_launches(1);
-  return map_cuda(cudaGetLastError());
+  const cudaError_t e = cudaGetLastError();
+  if (xt_mem) cudaFreeAsync(xt_mem, s);
+  return map_cuda(e);
+}
+
+template <int SRC, int XB, int MINB>
+int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  if (SRC == kK15 && WCOMP_GEMV_XT && B >= 3) return launch_mma_xt<SRC, XB, MINB, SRC == kK15>(b, Ns, B, dev, sms, s);
+  return launch_mma_xt<SRC, XB, MINB, false>(b, Ns, B, dev, sms, s);
 }
 
 // Batches from this size up take the tensor-core kernel (measured on the
@@ -1767,7 +1878,9 @@ int launch_mma_on(GemvBatch& b, int64_t N, int B, int sms, uint32_t* slot, cudaS
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, 0) != cudaSuccess || per_sm <= 0)
     per_sm = 1;
-  kern<<<per_sm * sms, kMmaThreads, 0, s>>>(b, units, B, slot);
+  XtBatch xt;
+  memset(&xt, 0, sizeof(xt));
+  kern<<<per_sm * sms, kMmaThreads, 0, s>>>(b, units, B, slot, xt);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }
