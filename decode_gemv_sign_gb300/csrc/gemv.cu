@@ -1150,9 +1150,10 @@ struct XtBatch {
   int count;
 };
 
-template <int XB>
+template <int XW>
 __global__ void __launch_bounds__(256) transpose_x_kernel(const __grid_constant__ GemvBatch b,
                                                           const __grid_constant__ XtBatch xt, int B) {
+  static_assert(XW == 2 || XW == 4 || XW == 8 || XW == 16, "transposed width");
   const uint32_t total = xt.kprefix[xt.count];
   for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += gridDim.x * blockDim.x) {
     int i = 0;
@@ -1160,20 +1161,28 @@ __global__ void __launch_bounds__(256) transpose_x_kernel(const __grid_constant_
     const int64_t K = b.d[i].K;
     const uint32_t k = c - xt.kprefix[i];
     const uint16_t* x = b.x[i];
-    uint32_t v[XB / 2];
+    uint32_t v[XW / 2];
 #pragma unroll
-    for (int q = 0; q < XB / 2; ++q) {
+    for (int q = 0; q < XW / 2; ++q) {
       const uint32_t lo = 2 * q < B ? uint32_t(x[int64_t(2 * q) * K + k]) : 0u;
       const uint32_t hi = 2 * q + 1 < B ? uint32_t(x[int64_t(2 * q + 1) * K + k]) : 0u;
       v[q] = lo | (hi << 16);
     }
-    uint4* out = reinterpret_cast<uint4*>(xt.p[i] + uint64_t(k) * XB);
+    uint16_t* out = xt.p[i] + uint64_t(k) * XW;
+    if (XW == 2) {
+      *reinterpret_cast<uint32_t*>(out) = v[0];
+    } else if (XW == 4) {
+      *reinterpret_cast<uint2*>(out) = make_uint2(v[0], v[1 % (XW / 2)]);
+    } else {
 #pragma unroll
-    for (int q = 0; q < XB / 8; ++q) out[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int q = 0; q < XW / 8; ++q)
+        reinterpret_cast<uint4*>(out)[q] = make_uint4(v[(4 * q) % (XW / 2)], v[(4 * q + 1) % (XW / 2)],
+                                                      v[(4 * q + 2) % (XW / 2)], v[(4 * q + 3) % (XW / 2)]);
+    }
   }
 }
 
-template <int SRC, int XB, int MINB, bool XT = false>
+template <int SRC, int XB, int MINB, int XW = 0>
 __global__ void __launch_bounds__(kMmaThreads, MINB)
     gemv_mma_kernel(const __grid_constant__ GemvBatch p, uint32_t total_units, int B, uint32_t* __restrict__ slot,
                     const __grid_constant__ XtBatch xt) {
@@ -1183,6 +1192,7 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
   __shared__ float part[2][kMmaWarps][32][4];
   // per-thread corrections (x gathered per batch row), or with XT per-warp
   // sums for every (batch, row) of the unit
+  constexpr bool XT = XW > 0;  // corrections from x transposed to [K][XW]
   __shared__ float corr[2][XT ? kMmaWarps * 16 * 8 : kMmaThreads];
   __shared__ uint32_t first_unit, next_unit[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1259,9 +1269,10 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
         // thread (row j = cj, part q = tid / 8 of 32): every batch row at once
         // from the transposed x; the four parts of a warp are summed by a
         // fixed shuffle tree, the warps in order in the final sum
-        float cs[XB];
+        constexpr int W = XT ? XW : 1;
+        float cs[W];
 #pragma unroll
-        for (int b = 0; b < XB; ++b) cs[b] = 0.f;
+        for (int b = 0; b < W; ++b) cs[b] = 0.f;
         if (cj < cur.rows) {
           const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
           const uint16_t* xtb = xt.p[cur.ti];
@@ -1269,27 +1280,36 @@ __global__ void __launch_bounds__(kMmaThreads, MINB)
             const uint32_t pos = d.esc_pos[e];
             const float delta = esc_delta<SRC == kBytesplit ? WCOMP_BYTESPLIT : WCOMP_K15>(
                 load_esc_val(d, e), SRC == kBytesplit ? uint32_t(d.raw[pos]) : 0u);
-            const uint4* xr = reinterpret_cast<const uint4*>(xtb + uint64_t(uint64_t(pos) - rowbase) * XB);
+            const uint16_t* xr = xtb + uint64_t(uint64_t(pos) - rowbase) * W;
+            uint32_t wv[W / 2 > 0 ? W / 2 : 1];
+            if (W == 2) {
+              wv[0] = *reinterpret_cast<const uint32_t*>(xr);
+            } else if (W == 4) {
+              const uint2 v = *reinterpret_cast<const uint2*>(xr);
+              wv[0] = v.x;
+              wv[1 % (W / 2 > 0 ? W / 2 : 1)] = v.y;
+            } else {
 #pragma unroll
-            for (int q = 0; q < XB / 8; ++q) {
-              const uint4 v = xr[q];
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                cs[8 * q + 2 * h] = fmaf(bf16_lo(w4[h]), delta, cs[8 * q + 2 * h]);
-                cs[8 * q + 2 * h + 1] = fmaf(bf16_hi(w4[h]), delta, cs[8 * q + 2 * h + 1]);
+              for (int q = 0; q < W / 8; ++q) {
+                const uint4 v = reinterpret_cast<const uint4*>(xr)[q];
+                wv[4 * q] = v.x; wv[4 * q + 1] = v.y; wv[4 * q + 2] = v.z; wv[4 * q + 3] = v.w;
               }
+            }
+#pragma unroll
+            for (int h = 0; h < W / 2; ++h) {
+              cs[2 * h] = fmaf(bf16_lo(wv[h]), delta, cs[2 * h]);
+              cs[2 * h + 1] = fmaf(bf16_hi(wv[h]), delta, cs[2 * h + 1]);
             }
           }
         }
 #pragma unroll
-        for (int b = 0; b < XB; ++b) {
+        for (int b = 0; b < W; ++b) {
           cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 8);
           cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 16);
         }
         if (lane < 8) {
 #pragma unroll
-          for (int b = 0; b < XB; ++b) corr[par][(warp * 16 + b) * 8 + lane] = cs[b];
+          for (int b = 0; b < W; ++b) corr[par][(warp * 16 + b) * 8 + lane] = cs[b];
         }
       } else {
         float c = 0.f;
@@ -1543,13 +1563,19 @@ int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
 #ifndef WCOMP_GEMV_XT
 #define WCOMP_GEMV_XT 1  // K15's escape corrections read a transposed copy of x
 #endif
+#ifndef WCOMP_GEMV_XT_MIN_B
+#define WCOMP_GEMV_XT_MIN_B 3
+#endif
 
 // With the transposed x a thread reads all batch rows of an escape's column
-// at once: K15 (escape rate 1.7-3 %) gains from B = 3 (B = 8: 164 -> 131 us,
-// B = 16: 251 -> 167 us on the dense-layer set); at B = 2 the padded copy
-// costs more than it saves, and byte-split's few escapes gain nothing.
-template <int SRC, int XB, int MINB, bool kXt>
+// at once (the copy is as wide as the batch: 4, 8 or 16 values per column):
+// K15 (escape rate 1.7-3 %) gains from B = 3 (dense-layer set: B = 4 128 ->
+// 121.5 us, B = 8 164 -> 131 us, B = 16 251 -> 167 us); at B = 2 the extra
+// launch and copy cost more than they save (112 -> 116.5 us), and
+// byte-split's few escapes gain nothing.
+template <int SRC, int XB, int MINB, int XW>
 int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
+  constexpr bool kXt = XW > 0;
   uint32_t units = 0;
   for (int j = 0; j < b.count; ++j) {
     b.set_prefix[j] = units;
@@ -1559,7 +1585,7 @@ int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cuda
   uint32_t* slot = nullptr;
   int st = counter_slot(dev, &slot);
   if (st != WCOMP_OK) return st;
-  auto kern = gemv_mma_kernel<SRC, XB, MINB, kXt>;
+  auto kern = gemv_mma_kernel<SRC, XB, MINB, XW>;
   static int per_sm_cache = 0;
   if (!per_sm_cache) {
     int per_sm = 0;
@@ -1580,11 +1606,11 @@ int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cuda
     if (cols >= (uint64_t(1) << 32)) return WCOMP_EUNSUPPORTED;
     xt.kprefix[b.count] = uint32_t(cols);
     xt.count = b.count;
-    cudaError_t e = pool_alloc(reinterpret_cast<void**>(&xt_mem), cols * XB * sizeof(uint16_t), s);
+    cudaError_t e = pool_alloc(reinterpret_cast<void**>(&xt_mem), cols * (kXt ? XW : 1) * sizeof(uint16_t), s);
     if (e != cudaSuccess) return map_cuda(e);
-    for (int j = 0; j < b.count; ++j) xt.p[j] = xt_mem + uint64_t(xt.kprefix[j]) * XB;
+    for (int j = 0; j < b.count; ++j) xt.p[j] = xt_mem + uint64_t(xt.kprefix[j]) * (kXt ? XW : 1);
     const uint32_t blocks = uint32_t(std::min<uint64_t>(cdiv(cols, 256), uint64_t(sms) * 8));
-    transpose_x_kernel<XB><<<blocks, 256, 0, s>>>(b, xt, B);
+    transpose_x_kernel<kXt ? XW : 2><<<blocks, 256, 0, s>>>(b, xt, B);
     count_launches(1);
   }
   kern<<<per_sm_cache * sms, kMmaThreads, 0, s>>>(b, units, B, slot, xt);
@@ -1596,8 +1622,12 @@ int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cuda
 
 template <int SRC, int XB, int MINB>
 int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
-  if (SRC == kK15 && WCOMP_GEMV_XT && B >= 3) return launch_mma_xt<SRC, XB, MINB, SRC == kK15>(b, Ns, B, dev, sms, s);
-  return launch_mma_xt<SRC, XB, MINB, false>(b, Ns, B, dev, sms, s);
+  if (SRC == kK15 && WCOMP_GEMV_XT && B >= WCOMP_GEMV_XT_MIN_B) {
+    if (B <= 2) return launch_mma_xt<SRC, XB, MINB, 2>(b, Ns, B, dev, sms, s);
+    if (B <= 4) return launch_mma_xt<SRC, XB, MINB, 4>(b, Ns, B, dev, sms, s);
+    return launch_mma_xt<SRC, XB, MINB, XB>(b, Ns, B, dev, sms, s);
+  }
+  return launch_mma_xt<SRC, XB, MINB, 0>(b, Ns, B, dev, sms, s);
 }
 
 // Batches from this size up take the tensor-core kernel (measured on the
