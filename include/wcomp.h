@@ -136,8 +136,14 @@ WCOMP_API int wcomp_decode(const wcomp_container* c, uint16_t* d_out, void* stre
  *   d_y     device, float[B*N], row-major; overwritten.
  * W is rebuilt in registers from the codes and raw bits; escaped weights are
  * corrected inside the same kernel (y += x * (w_true - w_placeholder)).
- * Products and sums are fp32; the summation order is fixed (no atomics), so
- * repeated calls give identical bits.
+ * Products and sums are fp32 (CUDA-core FMAs for small batches, BF16 tensor
+ * core MMAs with fp32 accumulation for larger ones); the summation order is
+ * fixed (no atomics), so repeated calls give identical bits.
+ * Memory: the work counters live in a device buffer the library allocates
+ * with cudaMalloc on first use per device; a K15 container at B >= 3 also
+ * takes a transposed copy of x (K * 4..16 * 2 bytes) from the library's
+ * stream-ordered pool for the duration of the call.  wcomp_gemv_noalloc
+ * allocates nothing.
  * Definition: forgeeks page, "Qué queda por demostrar" (GEMV on codes rebuilt
  * in registers, escape correction); wavect page on rebuilding exact BF16 in
  * registers for the matmul.
