@@ -75,7 +75,7 @@ def test_host_validation_matches_oracle(lib, scheme):
     w = synth.gen_weights_np(synth.WeightSpec("t", 16, 1000, "t4", 0.02, 0.02, "normal", 1.0, seed=5))
     buf = bytearray(O.serialize(O.encode(w, scheme)))
     ok = _deser_status(lib, bytes(buf))
-    assert ok != wcomp.ECORRUPT  # OK on a GPU machine, a CUDA error without a device
+    assert ok != wcomp.ECORRUPT  # OK with a GPU present, a CUDA error without one
     rng = np.random.default_rng(1)
     for off in [0, 4, 6, 8, 24, 32, 40, 72, 80, 92] + list(rng.integers(96, len(buf), size=16)):
         bad = bytearray(buf)
