@@ -83,6 +83,12 @@ def test_pack_bits9_hand_example():
     got = O.pack_bits9(np.array([0x1FF, 0x000, 0x155, 0x0AA]))
     assert got.tolist() == [0xFF, 0x01, 0x54, 0x55, 0x05]
     assert O.unpack_bits9(got, 4).tolist() == [0x1FF, 0x000, 0x155, 0x0AA]
+    # the values above read the same in either bit order; these do not:
+    # 0x001 sets stream bit 0; 0x100 sets bit 9 + 8 = 17; 0x003 sets bits 18 and 19
+    # -> byte 0 = 0x01, byte 2 = bits 1, 2, 3 = 0x0E, 27 bits in 4 bytes
+    got = O.pack_bits9(np.array([0x001, 0x100, 0x003]))
+    assert got.tolist() == [0x01, 0x00, 0x0E, 0x00]
+    assert O.unpack_bits9(got, 3).tolist() == [0x001, 0x100, 0x003]
     vals = np.random.default_rng(3).integers(0, 512, 1001)
     assert np.array_equal(O.unpack_bits9(O.pack_bits9(vals), vals.size), vals)
     assert O.pack_bits9(np.zeros(0)).size == 0

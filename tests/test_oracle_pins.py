@@ -148,6 +148,8 @@ def test_histogram_and_table_brute_force(scheme):
     h = O.histogram(sym, scheme)
     table, counts = _brute_table(w, scheme)
     assert h.sum() == w.size
+    # one bin per possible symbol: 2^8 high bytes, 2^9 sign+exponent values
+    assert h.size == (256 if scheme == 0 else 512)
     assert all(h[s] == counts.get(s, 0) for s in range(h.size))
     assert list(O.select_table(h)) == table
 
@@ -263,6 +265,28 @@ def test_escape_stream_and_indexes(scheme):
         assert c.row_index[r] == sum(1 for p in c.esc_pos if p < r * c.K)
 
 
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_indexes_with_escapes_on_boundaries(scheme):
+    # 3 rows of K = 8192 + 5: escapes placed exactly on row starts, on tile
+    # boundaries (multiples of 8192), on the element before each, and last.
+    N, K = 3, 8197
+    n = N * K
+    shift = 8 if scheme == 0 else 7
+    i = np.arange(n)
+    # 15 common symbols in turn fill the table; the raw bits count up
+    w = (((0x30 + i % 15) << 8) | (i & ((1 << shift) - 1))).astype(np.uint16)
+    spots = [0, 8191, 8192, K - 1, K, 16383, 16384, 2 * K - 1, 2 * K, 24575, 24576, n - 1]
+    w[spots] = 0x7F00  # a symbol seen only at these spots
+    c = O.encode(w, scheme, N, K)
+    assert c.E == len(spots) and c.esc_pos.tolist() == spots
+    # entry j counts escapes strictly below boundary j
+    assert c.tile_index.tolist() == [sum(p < t * 8192 for p in spots) for t in range(c.n_tiles + 1)]
+    assert c.row_index.tolist() == [sum(p < r * K for p in spots) for r in range(N + 1)]
+    assert c.row_index.tolist() == [0, 4, 8, len(spots)]
+    # row 1 starts with an escape and row 0 ends with one: both stay in their rows
+    assert np.array_equal(O.decode_rows(c, np.array([1])), w.reshape(N, K)[[1]])
+
+
 # ---------------------------------------------------------------------------
 # Corruption is detected.
 # ---------------------------------------------------------------------------
@@ -337,6 +361,17 @@ def test_gemv_brute_force_tiny():
         for r in range(3):
             ref = sum(_f(X[b, k]) * _f(W[r, k]) for k in range(5))
             assert abs(y[b, r] - ref) <= 1e-15 * max(1.0, abs(ref))
+
+
+def test_gemv_is_exact_where_fp32_accumulation_is_not():
+    # 1 + 2^-30 needs 31 significant bits: exact in fp64, rounded to 1 by any
+    # fp32 sum in any order.  Row 2: 1 + 2^-30 - 1 = 2^-30 exactly.
+    W = np.array([[0x3F80, 0x3080, 0x0000], [0x3F80, 0x3080, 0xBF80]], np.uint16)  # 1, 2^-30, 0 / -1
+    X = np.array([[0x3F80, 0x3F80, 0x3F80]], np.uint16)
+    assert _f(0x3080) == 2.0 ** -30
+    y = O.gemv(W, X)
+    assert y[0, 0] == 1.0 + 2.0 ** -30
+    assert y[0, 1] == 2.0 ** -30
 
 
 @pytest.mark.parametrize("scheme", O.SCHEMES)
