@@ -180,6 +180,44 @@ def test_gemv_ragged_k_element_path(W, scheme, B):
     c.free()
 
 
+def _escapes_on_boundaries(N, K, scheme):
+    """W[N, K] of 15 common symbols in turn (magnitudes 2^-15 .. 2), with a
+    rare symbol (2.0 .. 4.0) on every row start and row end and on both sides
+    of every 8192-element tile boundary; the raw bits count up."""
+    n = N * K
+    i = np.arange(n)
+    mask = 0xFF if scheme == O.BYTESPLIT else 0x7F
+    common = np.array([0x3C, 0x3D, 0x3E, 0x3F, 0xBC, 0xBD, 0xBE, 0xBF, 0x3B, 0xBB, 0x3A, 0xBA, 0x39, 0xB9, 0x38])
+    w = ((common[i % 15] << 8) | (i & mask)).astype(np.uint16)
+    spots = set()
+    for r in range(N):
+        spots |= {r * K, r * K + K - 1}
+    for t in range(1, -(-n // O.TILE)):
+        spots |= {t * O.TILE - 1, t * O.TILE}
+    spots = sorted(spots)
+    w[spots] = 0x4000 | (i[spots] & mask)
+    return w.reshape(N, K), spots
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+@pytest.mark.parametrize("shape", [(3, 8197), (6, 8192), (40, 1024)])
+def test_escapes_on_row_and_tile_boundaries(W, scheme, shape):
+    """Escapes exactly where rows and tiles begin and end: containers and
+    decode bit-exact, GEMV within tolerance for a ragged K (element path) and
+    aligned K (FMA and tensor-core kernels)."""
+    w, spots = _escapes_on_boundaries(*shape, scheme)
+    ref = O.encode(w, scheme)
+    assert ref.esc_pos.tolist() == spots
+    c = W.encode(dev(w), scheme)
+    assert W.serialize(c) == O.serialize(ref)
+    assert W.serialize(c, compact=True) == O.serialize_compact(ref)
+    assert np.array_equal(host(W.decode(c)).reshape(w.shape), w)
+    for B in (1, 4, 16):
+        x = synth.gen_x_np(B, shape[1], 40 + B)
+        check_gemv(W.gemv(c, dev(x)), O.gemv(w, x))
+    c.free()
+
+
 @pytest.mark.parametrize("scheme", O.SCHEMES)
 def test_gemv_one_hot_exact_and_zero(W, scheme):
     spec = synth.WeightSpec("o", 64, 256, "normal", 0.02, 0.05, "normal", 1.0, seed=5)
