@@ -438,57 +438,92 @@ __global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncB
 // group, a block scan gives each escape its place, and the values are read
 // back from the source.  Either way the stream ends up in ascending position
 // order.
+//
+// A CTA covers kCompactTiles consecutive tiles of one tensor: warp w copies
+// tile w's stash (a stash copy is a few hundred bytes, so one CTA per tile
+// would spend its life waiting on launch and load latency), then the whole
+// CTA ranks the overflowing tiles among them one after another.
 // ---------------------------------------------------------------------------
-// Both schemes in one launch: the scheme is uniform per CTA (one tile of one tensor).
+constexpr uint32_t kCompactTiles = kThreads / 32;
+
+// Both schemes in one launch: the scheme is uniform per CTA (tiles of one tensor).
 __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t sm[kThreads / 32];
+  __shared__ uint32_t overflow;
   const int ti = find_owner(bt, blockIdx.x);
   const EncDesc& d = bt.d[ti];
   const int SCHEME = d.scheme;
-  const uint32_t t = blockIdx.x - bt.prefix[ti];
+  const uint32_t t0 = (blockIdx.x - bt.prefix[ti]) * kCompactTiles;
+  const uint32_t nt = min(kCompactTiles, d.n_tiles - t0);
   const uint32_t* tile_index = reinterpret_cast<const uint32_t*>(d.main + d.off_tile);
-  const uint32_t first = tile_index[t], count = tile_index[t + 1] - first;
-  if (count == 0) return;  // uniform
-  if (count <= d.stash_cap) {
-    uint32_t* pos = reinterpret_cast<uint32_t*>(d.esc + d.off_pos);
-    uint8_t* val = d.esc + d.off_val;
-    for (uint32_t i = threadIdx.x; i < count; i += kThreads) {
-      const uint64_t s = uint64_t(t) * d.stash_cap + i;
-      pos[first + i] = d.stash_pos[s];
-      if (SCHEME == WCOMP_BYTESPLIT)
-        val[first + i] = uint8_t(d.stash_val[s]);
-      else
-        reinterpret_cast<uint16_t*>(val)[first + i] = d.stash_val[s];
-    }
-    return;
-  }
-  const uint64_t G = cdiv(d.n, kGroup);
-  const uint64_t g = uint64_t(t) * kThreads + threadIdx.x;
-  uint4 c4 = make_uint4(0, 0, 0, 0);
-  if (g < G) c4 = *reinterpret_cast<const uint4*>(d.main + d.off_codes + 16 * g);
-  const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
-  uint32_t cnt = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t x = cw[i] & (cw[i] >> 1) & (cw[i] >> 2) & (cw[i] >> 3) & 0x11111111u;
-    cnt += __popc(x);
-  }
-  uint32_t o = tile_index[t] + block_exclusive_256(cnt, sm);
-  if (!cnt) return;
   uint32_t* pos = reinterpret_cast<uint32_t*>(d.esc + d.off_pos);
   uint8_t* val = d.esc + d.off_val;
-  const uint64_t base = g * kGroup;
-  for (int e = 0; e < kGroup; ++e) {
-    if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape) {
-      const uint32_t p = uint32_t(base + e);
-      const uint32_t v = d.w[p];
-      pos[o] = p;
-      if (SCHEME == WCOMP_BYTESPLIT)
-        val[o] = uint8_t(v >> 8);
-      else
-        reinterpret_cast<uint16_t*>(val)[o] = uint16_t(v);
-      ++o;
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) overflow = 0;
+  __syncthreads();
+  if (warp < nt) {
+    const uint32_t t = t0 + warp;
+    const uint32_t first = tile_index[t], count = tile_index[t + 1] - first;
+    if (count > d.stash_cap) {
+      if (lane == 0) atomicOr(&overflow, 1u << warp);
+    } else {
+      const uint64_t s0 = uint64_t(t) * d.stash_cap;
+      // four entries per lane in flight before any is stored
+      for (uint32_t i0 = 0; i0 < count; i0 += 128) {
+        uint32_t p[4], v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t i = i0 + 32 * k + lane;
+          if (i < count) {
+            p[k] = d.stash_pos[s0 + i];
+            v[k] = d.stash_val[s0 + i];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t i = i0 + 32 * k + lane;
+          if (i < count) {
+            pos[first + i] = p[k];
+            if (SCHEME == WCOMP_BYTESPLIT)
+              val[first + i] = uint8_t(v[k]);
+            else
+              reinterpret_cast<uint16_t*>(val)[first + i] = uint16_t(v[k]);
+          }
+        }
+      }
     }
+  }
+  __syncthreads();
+  const uint64_t G = cdiv(d.n, kGroup);
+  for (uint32_t m = overflow; m; m &= m - 1) {  // uniform across the CTA
+    const uint32_t t = t0 + uint32_t(__ffs(m) - 1);
+    const uint64_t g = uint64_t(t) * kThreads + threadIdx.x;
+    uint4 c4 = make_uint4(0, 0, 0, 0);
+    if (g < G) c4 = *reinterpret_cast<const uint4*>(d.main + d.off_codes + 16 * g);
+    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = cw[i] & (cw[i] >> 1) & (cw[i] >> 2) & (cw[i] >> 3) & 0x11111111u;
+      cnt += __popc(x);
+    }
+    uint32_t o = tile_index[t] + block_exclusive_256(cnt, sm);
+    if (cnt) {
+      const uint64_t base = g * kGroup;
+      for (int e = 0; e < kGroup; ++e) {
+        if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape) {
+          const uint32_t p = uint32_t(base + e);
+          const uint32_t v = d.w[p];
+          pos[o] = p;
+          if (SCHEME == WCOMP_BYTESPLIT)
+            val[o] = uint8_t(v >> 8);
+          else
+            reinterpret_cast<uint16_t*>(val)[o] = uint16_t(v);
+          ++o;
+        }
+      }
+    }
+    __syncthreads();  // sm is rewritten by the next overflowing tile's scan
   }
 }
 
@@ -807,7 +842,13 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   for (auto& j : jobs)
     if (j.d.E) with_esc.push_back(j);
   e = for_chunks(with_esc, -1, [&](EncBatch& b) {
-    compact_kernel<<<tiles_prefix(b), kThreads, 0, s>>>(b);
+    uint32_t blocks = 0;
+    for (int j = 0; j < b.count; ++j) {
+      b.prefix[j] = blocks;
+      blocks += uint32_t(cdiv(b.d[j].n_tiles, kCompactTiles));
+    }
+    b.prefix[b.count] = blocks;
+    compact_kernel<<<blocks, kThreads, 0, s>>>(b);
     count_launches(1);
   });
   if (e != cudaSuccess) return fail2(e);
