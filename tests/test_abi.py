@@ -62,6 +62,64 @@ def test_argument_errors_without_gpu(lib):
     lib.wcomp_free(None, None)  # no-op
 
 
+def _ptrs(*vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def test_batched_and_remaining_argument_errors_without_gpu(lib):
+    """Every entry point rejects bad arguments on the host, before any CUDA call."""
+    h = ctypes.c_void_p()
+    P = ctypes.c_void_p
+    n1 = (ctypes.c_int64 * 1)(4)
+    k1 = (ctypes.c_int64 * 1)(4)
+    s1 = (ctypes.c_int * 1)(0)
+    ok = _ptrs(256)
+    # batched encode: null arrays, empty batch, null entry, bad scheme, zero size, null output
+    assert lib.wcomp_encode_batched(None, n1, k1, s1, 1, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_encode_batched(ok, n1, k1, s1, 0, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_encode_batched(ok, n1, k1, s1, 1, None, None) == wcomp.EINVAL
+    # batched decode and GEMV: null arrays and empty batches
+    assert lib.wcomp_decode_batched(None, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_decode_batched(ok, None, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_decode_batched(ok, ok, 0, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_batched(None, ok, 1, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_batched(ok, ok, 1, ok, 0, None) == wcomp.EINVAL
+    # containers' GEMV with a null entry inside the arrays
+    assert lib.wcomp_gemv_batched(_ptrs(None), ok, 1, ok, 1, None) == wcomp.EINVAL
+    # no-allocation GEMV: null pointers and B outside 1..16
+    assert lib.wcomp_gemv_noalloc(None, P(256), 1, P(256), None) == wcomp.EINVAL
+    # plain GEMV, batched: B outside 1..16, zero sizes, null entries, rows beyond 2^31
+    for B in (0, 17):
+        assert lib.wcomp_gemv_bf16_batched(ok, n1, k1, ok, B, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16_batched(ok, (ctypes.c_int64 * 1)(0), k1, ok, 1, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16_batched(ok, n1, (ctypes.c_int64 * 1)(-1), ok, 1, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16_batched(_ptrs(None), n1, k1, ok, 1, ok, 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16_batched(ok, n1, k1, ok, 1, _ptrs(None), 1, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16_batched(ok, n1, k1, ok, 1, ok, 0, None) == wcomp.EINVAL
+    assert lib.wcomp_gemv_bf16(P(256), 1 << 31, 4, P(256), 1, P(256), None) == wcomp.EUNSUPPORTED
+    assert lib.wcomp_gemv_bf16(P(256), 4, 0, P(256), 1, P(256), None) == wcomp.EINVAL
+    # (de)serialization: null container, null length, null buffer, null output
+    n = ctypes.c_uint64()
+    assert lib.wcomp_serialize(None, None, 0, ctypes.byref(n), None) == wcomp.EINVAL
+    assert lib.wcomp_serialize_compact(None, None, 0, ctypes.byref(n), None) == wcomp.EINVAL
+    assert lib.wcomp_deserialize(None, 96, None, ctypes.byref(h)) == wcomp.EINVAL
+    assert lib.wcomp_deserialize(ctypes.create_string_buffer(96), 96, None, None) == wcomp.EINVAL
+    assert lib.wcomp_info(P(256), None) == wcomp.EINVAL
+
+
+def test_every_status_has_its_own_message(lib):
+    codes = [wcomp.OK, wcomp.EINVAL, wcomp.ENOMEM, wcomp.ECORRUPT, wcomp.ECUDA, wcomp.EUNSUPPORTED, wcomp.ETIMEOUT]
+    msgs = [lib.wcomp_strerror(c) for c in codes]
+    assert all(msgs) and len(set(msgs)) == len(codes)
+    assert lib.wcomp_strerror(-99) == b"unknown status"
+    # the header's enum and the binding agree
+    src = open(HEADER).read()
+    enum = dict((k, int(v)) for k, v in re.findall(r"WCOMP_(OK|E[A-Z]+)\s*=\s*(-?\d+)", src))
+    assert enum == {"OK": 0, "EINVAL": -1, "ENOMEM": -2, "ECORRUPT": -3, "ECUDA": -4, "EUNSUPPORTED": -5,
+                    "ETIMEOUT": -6}
+    assert [enum[k] for k in ("OK", "EINVAL", "ENOMEM", "ECORRUPT", "ECUDA", "EUNSUPPORTED", "ETIMEOUT")] == codes
+
+
 def _deser_status(lib, buf: bytes) -> int:
     h = ctypes.c_void_p()
     b = ctypes.create_string_buffer(buf, len(buf))
