@@ -479,11 +479,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(t_ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u16 codec / fp32 GEMV accumulate",
         "data": "synthetic (seeded N(0,0.02) BF16 weights with 0.1% N(0,0.5) outliers, x ~ N(0,1) BF16)",
-        "config": {"workload": "dense layer set: 4 x 4096x4096 + 3 x 4096x11008 BF16, both schemes, "
-                               "encode + batched decode + fused GEMV B=1,4 + plain GEMV B=1,4",
-                   "tensors": len(specs), "elements": int(sum(s.n for s in specs)), "batches": list(BATCHES),
-                   "l2": "inputs larger than L2 (386 MB BF16, ~580 MB containers), swept in order",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(specs, world),
         "rows": rows,
         "kernels": kernels,
         "fused_over_plain_time": ratio,
@@ -608,6 +604,15 @@ def load_traffic(key: str):
     return None
 
 
+def workload_config(specs, world: int) -> dict:
+    """The `config` of both arms' lines: the workload a step covers."""
+    return {"workload": "dense layer set: 4 x 4096x4096 + 3 x 4096x11008 BF16, both schemes, "
+                        "encode + batched decode + fused GEMV B=1,4 + plain GEMV B=1,4",
+            "tensors": len(specs), "elements": int(sum(s.n for s in specs)), "batches": list(BATCHES),
+            "l2": "inputs larger than L2 (386 MB BF16, ~580 MB containers), swept in order",
+            "parallelism": f"replicas x{world}"}
+
+
 # ---------------------------------------------------------------------------
 # The reference arm: the CPU oracle, timed on the host cores.
 # ---------------------------------------------------------------------------
@@ -615,6 +620,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    from decode_gemv_sign_gb300 import synth
     vals = []
     for _ in range(args.warmup):
         cpu_baseline()
@@ -634,7 +640,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16 codec / f64 GEMV",
         "data": "synthetic (seeded numpy draw of the same workload recipe)",
-        "config": {"workload": "dense layer set sample (" + CPU_SAMPLE + ")", "parallelism": "1 host core"},
+        # the same workload as our arm's line; each step times a bounded sample of it (cpu_baseline)
+        "config": workload_config(synth.workload_dense_layers(), world),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": CPU_SAMPLE},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
