@@ -1634,7 +1634,7 @@ int launch_mma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
 // dense-layer set): the plain GEMV at every B (its wide per-lane loads and
 // x read by a quarter of the lanes beat the FMA kernel even at B = 1), K15
 // from B = 2, byte-split from B = 4 (its decode is cheap enough that the FMA
-// kernel keeps B = 1..2).  WCOMP_GEMV_MMA_MIN_B overrides all.
+// kernel keeps B = 1..3).  WCOMP_GEMV_MMA_MIN_B overrides all.
 #ifndef WCOMP_GEMV_MMA_MIN_B
 #define WCOMP_GEMV_MMA_MIN_B 0
 #endif
