@@ -1505,16 +1505,17 @@ int launch_vec(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   uint32_t* slot = nullptr;
   int st = counter_slot(dev, &slot);
   if (st != WCOMP_OK) return st;
-  static int per_sm_cache = 0;
-  if (!per_sm_cache) {
-    int per_sm = 0;
+  // resident CTAs per SM, asked once per instantiation (every thread computes the same value)
+  static std::atomic<int> per_sm_cache{0};
+  int per_sm = per_sm_cache.load(std::memory_order_relaxed);
+  if (!per_sm) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<SRC, BT, R, MINB, MODE, ESC>, kThreads, 0) !=
             cudaSuccess ||
         per_sm <= 0)
       per_sm = 1;
-    per_sm_cache = per_sm;
+    per_sm_cache.store(per_sm, std::memory_order_relaxed);
   }
-  const int blocks = per_sm_cache * sms;
+  const int blocks = per_sm * sms;
   gemv_kernel<SRC, BT, R, MINB, MODE, ESC><<<blocks, kThreads, 0, s>>>(b, units, B, slot);
   count_launches(1);
   return map_cuda(cudaGetLastError());
@@ -1547,15 +1548,17 @@ int launch_tma(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cudaStr
   uint32_t* slot = nullptr;
   if ((st = counter_slot(dev, &slot)) != WCOMP_OK) return st;
   auto kern = gemv_tma_kernel<SRC, BT, R, MODE, S, MINB>;
-  static int per_sm_cache = 0;
-  if (!per_sm_cache) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    int per_sm = 0;
+  // the shared-memory limit is an attribute of the function in the current device's context
+  cudaError_t ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (ae != cudaSuccess) return map_cuda(ae);
+  static std::atomic<int> per_sm_cache{0};
+  int per_sm = per_sm_cache.load(std::memory_order_relaxed);
+  if (!per_sm) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm <= 0)
       per_sm = 1;
-    per_sm_cache = per_sm;
+    per_sm_cache.store(per_sm, std::memory_order_relaxed);
   }
-  kern<<<per_sm_cache * sms, kThreads, smem, s>>>(b, units, B, slot, base + 2 * kSlots);
+  kern<<<per_sm * sms, kThreads, smem, s>>>(b, units, B, slot, base + 2 * kSlots);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }
@@ -1586,12 +1589,12 @@ int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cuda
   int st = counter_slot(dev, &slot);
   if (st != WCOMP_OK) return st;
   auto kern = gemv_mma_kernel<SRC, XB, MINB, XW>;
-  static int per_sm_cache = 0;
-  if (!per_sm_cache) {
-    int per_sm = 0;
+  static std::atomic<int> per_sm_cache{0};
+  int per_sm = per_sm_cache.load(std::memory_order_relaxed);
+  if (!per_sm) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaThreads, 0) != cudaSuccess || per_sm <= 0)
       per_sm = 1;
-    per_sm_cache = per_sm;
+    per_sm_cache.store(per_sm, std::memory_order_relaxed);
   }
   XtBatch xt;
   memset(&xt, 0, sizeof(xt));
@@ -1613,7 +1616,7 @@ int launch_mma_xt(GemvBatch& b, const int64_t* Ns, int B, int dev, int sms, cuda
     transpose_x_kernel<kXt ? XW : 2><<<blocks, 256, 0, s>>>(b, xt, B);
     count_launches(1);
   }
-  kern<<<per_sm_cache * sms, kMmaThreads, 0, s>>>(b, units, B, slot, xt);
+  kern<<<per_sm * sms, kMmaThreads, 0, s>>>(b, units, B, slot, xt);
   count_launches(1);
   const cudaError_t e = cudaGetLastError();
   if (xt_mem) cudaFreeAsync(xt_mem, s);
