@@ -110,6 +110,11 @@ def split_symbols(w: np.ndarray, scheme: int) -> Tuple[np.ndarray, np.ndarray]:
 # Step 2 - histogram of symbols over the tensor.
 # ---------------------------------------------------------------------------
 def histogram(sym: np.ndarray, scheme: int) -> np.ndarray:
+    """Count of every possible symbol (256 high bytes / 512 sign+exponent values).
+
+    forgeeks page, "Cómo funciona la compresión": the table holds the most reused sign+exponent
+    combinations, which is a count over the tensor (one table per tensor is
+    the reading taken where the page does not say)."""
     return np.bincount(sym, minlength=NBINS[scheme]).astype(np.int64)
 
 
@@ -117,7 +122,11 @@ def histogram(sym: np.ndarray, scheme: int) -> np.ndarray:
 # Step 3 - the 15-entry table: most frequent symbols first.
 # ---------------------------------------------------------------------------
 def select_table(hist: np.ndarray) -> np.ndarray:
-    """Order all bins by (count descending, symbol ascending); keep the first 15."""
+    """Order all bins by (count descending, symbol ascending); keep the first 15.
+
+    forgeeks page, "Cómo funciona la compresión": 15 table entries addressed by a
+    4-bit code.  The tie-break and the filling with unseen symbols are the
+    readings taken where the page is silent."""
     syms = np.arange(hist.size)
     order = np.lexsort((syms, -hist))  # last key is primary
     return order[:TABLE_SIZE].astype(np.uint32)
@@ -127,6 +136,10 @@ def select_table(hist: np.ndarray) -> np.ndarray:
 # Step 4 - codes: table index of each symbol, 15 (escape) when absent.
 # ---------------------------------------------------------------------------
 def assign_codes(sym: np.ndarray, table: np.ndarray, scheme: int) -> np.ndarray:
+    """Code of every element: its table index, or 15 (escape) for a symbol
+    outside the table.  forgeeks page, "Cómo funciona la compresión": a 4-bit code
+    into a 15-entry table, rare symbols to an exact escape stream (code 15 as
+    the escape marker is the reading of a 4-bit code that addresses 15 entries)."""
     lut = np.full(NBINS[scheme], ESCAPE, dtype=np.uint8)
     lut[table] = np.arange(TABLE_SIZE, dtype=np.uint8)
     return lut[sym]
@@ -136,7 +149,10 @@ def assign_codes(sym: np.ndarray, table: np.ndarray, scheme: int) -> np.ndarray:
 # Step 5 - streams.
 # ---------------------------------------------------------------------------
 def pack_nibbles(codes: np.ndarray) -> np.ndarray:
-    """Two codes per byte: element 2j in the low nibble, 2j+1 in the high nibble."""
+    """Two codes per byte: element 2j in the low nibble, 2j+1 in the high nibble.
+
+    The 4-bit code stream of the forgeeks page ("Cómo funciona la compresión");
+    the nibble order is this library's layout."""
     c = codes.astype(np.uint8)
     if c.size % 2:
         c = np.concatenate([c, np.zeros(1, np.uint8)])
@@ -203,7 +219,12 @@ def unpack_k15_planes(pa: np.ndarray, pb: np.ndarray, pc: np.ndarray, n: int) ->
 
 
 def escape_index(pos: np.ndarray, bounds: np.ndarray) -> np.ndarray:
-    """entry j = number of escapes whose position is below bounds[j]."""
+    """entry j = number of escapes whose position is below bounds[j].
+
+    Not part of the method's definition: an index over the escape stream so a
+    decoder finds a tile's or a row's escapes without a search (layout of
+    this library; the escape stream itself is the forgeeks page's, "Cómo
+    funciona la compresión")."""
     return np.searchsorted(pos, bounds, side="left").astype(np.uint32)
 
 
@@ -241,7 +262,12 @@ class Container:
 
 
 def encode(w: np.ndarray, scheme: int, N: Optional[int] = None, K: Optional[int] = None) -> Container:
-    """Encode BF16 bits w (any shape; read as W[N, K], default N=1 row if 1-D)."""
+    """Encode BF16 bits w (any shape; read as W[N, K], default N=1 row if 1-D).
+
+    The steps of forgeeks page, "Cómo funciona la compresión", in its order: split
+    each weight into the coded symbol and the raw bits, count the symbols, keep
+    the 15 most frequent as the table, code every element (15 = escape), and
+    keep the escaped symbols exactly in their own stream."""
     w = np.asarray(w, dtype=np.uint16)
     if N is None or K is None:
         if w.ndim == 2:
@@ -279,6 +305,7 @@ def encode(w: np.ndarray, scheme: int, N: Optional[int] = None, K: Optional[int]
 # Decode.
 # ---------------------------------------------------------------------------
 def unpack_codes(packed: np.ndarray, n: int) -> np.ndarray:
+    """Inverse of :func:`pack_nibbles`."""
     c = np.empty(2 * packed.size, dtype=np.uint8)
     c[0::2] = packed & 0xF
     c[1::2] = packed >> 4
@@ -286,7 +313,12 @@ def unpack_codes(packed: np.ndarray, n: int) -> np.ndarray:
 
 
 def decode(c: Container) -> np.ndarray:
-    """Rebuild the exact BF16 bits, shape [N, K]."""
+    """Rebuild the exact BF16 bits, shape [N, K].
+
+    Table symbol (or the escape stream's symbol) above the raw bits: the
+    forgeeks page, "Cómo funciona la compresión"; lossless means every bit
+    comes back (wavect page, "¿Qué significa “sin pérdida” para los pesos de
+    un LLM?")."""
     n = c.n
     codes = unpack_codes(c.codes, n)
     table = c.table.astype(np.uint32)
@@ -347,6 +379,9 @@ def section_sizes(scheme: int, N: int, K: int, E: int) -> list:
 
 
 def serialize(c: Container) -> bytes:
+    """Container version 1: header, then codes, raw bytes or K15 planes, both
+    indexes, escape positions and values, each section padded to 32 bytes.
+    The pages define no file format; this layout is the library's own."""
     parts = [("codes", c.codes)]
     if c.scheme == BYTESPLIT:
         parts.append(("raw", c.raw))
@@ -371,6 +406,11 @@ class CorruptContainer(ValueError):
 
 
 def deserialize(buf: bytes) -> Container:
+    """Parse and fully validate either serialized form (checksums, sizes, the
+    table, ascending in-range positions, indexes and codes agreeing with the
+    escape stream); raise CorruptContainer on any mismatch.  The wavect page
+    ("Un piloto de producción de 14 días") asks for corruption to be caught
+    before use."""
     if len(buf) < HEADER_BYTES:
         raise CorruptContainer("short header")
     head = buf[:HEADER_BYTES]
@@ -445,6 +485,7 @@ def pack_bits9(vals: np.ndarray) -> np.ndarray:
 
 
 def unpack_bits9(buf: np.ndarray, count: int) -> np.ndarray:
+    """Inverse of :func:`pack_bits9`: the first ``count`` 9-bit values."""
     bits = np.unpackbits(np.asarray(buf, dtype=np.uint8), bitorder="little")[: 9 * count]
     return (bits.reshape(count, 9).astype(np.uint32) << np.arange(9, dtype=np.uint32)).sum(axis=1).astype(np.uint32)
 
@@ -532,6 +573,7 @@ def _deserialize_compact(buf: bytes, scheme: int, N: int, K: int, E: int, table:
 
 
 def serialized_len_compact(scheme: int, N: int, K: int, E: int) -> int:
+    """Byte length of the compact form for these sizes."""
     return HEADER_BYTES + sum(_pad(s) for _, s in section_sizes_compact(scheme, N, K, E))
 
 
@@ -539,12 +581,18 @@ def serialized_len_compact(scheme: int, N: int, K: int, E: int) -> int:
 # GEMV in float64 from the exact BF16 values.
 # ---------------------------------------------------------------------------
 def bf16_to_f64(b: np.ndarray) -> np.ndarray:
+    """Exact value of BF16 bits (BF16 is the top half of an fp32 word)."""
     b = np.ascontiguousarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def gemv(w_bits: np.ndarray, x_bits: np.ndarray) -> np.ndarray:
-    """y[B, N] = x[B, K] @ W[N, K].T in float64."""
+    """y[B, N] = x[B, K] @ W[N, K].T in float64.
+
+    The product the fused kernel computes with W rebuilt from the codes
+    (forgeeks page, "Qué queda por demostrar"), stated on the exact BF16
+    values; every product of two BF16 numbers and every partial sum here is
+    far more precise than the fp32 arithmetic it is compared with."""
     W = bf16_to_f64(w_bits)
     X = bf16_to_f64(x_bits)
     return X @ W.T
@@ -568,10 +616,12 @@ def entropy_bpw(scheme: int, n: int, E: int) -> float:
 
 
 def physical_bpw(serialized_len: int, n: int) -> float:
+    """Bits per weight of a serialized container, every byte counted."""
     return 8.0 * serialized_len / n
 
 
 def serialized_len(scheme: int, N: int, K: int, E: int) -> int:
+    """Byte length of container version 1 for these sizes."""
     return HEADER_BYTES + sum(_pad(s) for _, s in section_sizes(scheme, N, K, E))
 
 
