@@ -46,16 +46,35 @@ def _batches(specs, batch_bytes: int):
 
 
 def _read_log(path: Optional[str]) -> Dict[tuple, dict]:
+    """Finished (tensor, scheme) records of a JSON-lines log.
+
+    Only newline-terminated lines count: text after the last newline is a
+    record an interruption cut short, and its tensor is validated again.  A
+    malformed line before that is an error (the log was damaged otherwise).
+    """
     done = {}
     if path and os.path.exists(path):
         with open(path) as f:
-            for line in f:
-                line = line.strip()
-                if not line:
-                    continue
-                r = json.loads(line)
-                done[(r["name"], r["scheme"])] = r
+            complete = f.read().split("\n")[:-1]
+        for line in complete:
+            line = line.strip()
+            if not line:
+                continue
+            r = json.loads(line)
+            done[(r["name"], r["scheme"])] = r
     return done
+
+
+def _open_log(path: str):
+    """Open the log for appending, after dropping an unterminated last line
+    (see _read_log) so the next record starts on a line of its own."""
+    if os.path.exists(path):
+        with open(path, "r+b") as f:
+            data = f.read()
+            keep = data.rfind(b"\n") + 1
+            if keep != len(data):
+                f.truncate(keep)
+    return open(path, "a")
 
 
 def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int = 16 << 30,
@@ -74,7 +93,7 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
 
     dev = torch.device(device)
     done = _read_log(log_path)
-    log = open(log_path, "a") if log_path else None
+    log = _open_log(log_path) if log_path else None
     t0 = time.perf_counter()
     try:
         for batch in _batches(specs, batch_bytes):
