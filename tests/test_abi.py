@@ -226,3 +226,33 @@ def test_host_validation_of_compact_form(lib, scheme):
     struct.pack_into("<H", bad, off["tile_count"] + 2, struct.unpack_from("<H", bad, off["tile_count"] + 2)[0] - 1)
     _recrc(bad)
     assert _deser_status(lib, bytes(bad)) == wcomp.ECORRUPT
+
+
+def test_info_struct_layout_matches_the_header(tmp_path):
+    """The binding's Info mirrors wcomp_info_t field for field: same names in
+    the same order, and the C compiler's offsets and size equal ctypes'."""
+    import shutil
+    import subprocess
+
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} wcomp_info_t;", src, re.S).group(1)
+    names = []
+    for decl in re.sub(r"/\*.*?\*/", "", body, flags=re.S).split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        for part in decl.split(None, 1)[1].split(","):
+            names.append(part.strip().split("[")[0])
+    assert names == [f for f, _ in wcomp.Info._fields_]
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "off.c"
+    prog.write_text('#include <stdio.h>\n#include "wcomp.h"\nint main(void){\n' +
+                    "".join(f'printf("%zu\\n", offsetof(wcomp_info_t, {n}));\n' for n in names) +
+                    'printf("%zu\\n", sizeof(wcomp_info_t)); return 0; }\n')
+    exe = tmp_path / "off"
+    subprocess.run([cc, "-std=c99", "-I", os.path.dirname(HEADER), str(prog), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [getattr(wcomp.Info, n).offset for n in names] + [ctypes.sizeof(wcomp.Info)]
+    assert got == want
