@@ -256,3 +256,39 @@ def test_info_struct_layout_matches_the_header(tmp_path):
     got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     want = [getattr(wcomp.Info, n).offset for n in names] + [ctypes.sizeof(wcomp.Info)]
     assert got == want
+
+
+def _c_kind(decl: str):
+    if "*" in decl:
+        return "ptr"
+    base = decl.replace("const", "").split()[0]
+    return {"int": ("int", 4), "int32_t": ("int", 4), "int64_t": ("int", 8), "uint64_t": ("uint", 8),
+            "uint32_t": ("uint", 4)}[base]
+
+
+def _py_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    return ("int" if t(-1).value < 0 else "uint", ctypes.sizeof(t))
+
+
+def test_binding_prototypes_match_the_header(lib):
+    """Every declared entry point: the binding passes as many arguments as the
+    header declares, each a pointer or an integer of the declared width and
+    signedness, and reads the declared return type."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = re.findall(r"WCOMP_API\s+([\w\s\*]+?)\s*\b(wcomp_\w+)\s*\(([^)]*)\)\s*;", src)
+    assert sorted(name for _, name, _ in protos) == declared()
+    for ret, name, params in protos:
+        fn = getattr(lib, name)
+        params = params.strip()
+        want = [] if params in ("", "void") else [_c_kind(p) for p in params.split(",")]
+        assert fn.argtypes is not None, name
+        assert [_py_kind(t) for t in fn.argtypes] == want, name
+        ret = ret.strip()
+        if ret == "void":
+            assert fn.restype is None, name
+        elif "*" in ret:
+            assert _py_kind(fn.restype) == "ptr", name
+        else:
+            assert _py_kind(fn.restype) == _c_kind(ret), name
