@@ -5,7 +5,8 @@ symbols at their symbol width, with every position implied by its code 15
 (forgeeks page "Prueba de GLM-5.2 reduce la memoria BF16 en casi un 25%",
 section "Cómo funciona la compresión").  Pinned here by a hand-derived bit
 packing example, closed-form sizes, an independent pure-Python reader that
-walks the bytes element by element (escape symbols consumed in order), the
+walks the bytes element by element (escape symbols consumed in order, and
+each tile's stored count checked against the escapes met in that tile), the
 bits/weight bound against the entropy accounting, and corruption cases.
 """
 import struct
@@ -44,13 +45,17 @@ def read_all_compact_pure(buf: bytes) -> list:
         p += _pad(8 * groups)
         c_off = p
         p += _pad(4 * groups)
-    p += _pad(2 * ((n + 8191) // 8192))
+    tc_off = p
+    n_tiles = (n + 8191) // 8192
+    p += _pad(2 * n_tiles)
     sym_off = p
     out = []
     r = 0
+    per_tile = [0] * n_tiles
     for i in range(n):
         byte = buf[codes_off + i // 2]
         code = (byte >> 4) if i % 2 else (byte & 15)
+        per_tile[i // 8192] += code == 15
         if scheme == 0:
             low = buf[raw_off + i]
         else:
@@ -73,6 +78,8 @@ def read_all_compact_pure(buf: bytes) -> list:
             r += 1
         out.append((sym << 8) | low if scheme == 0 else (sym << 7) | low)
     assert r == E
+    # the count section holds each 8192-element tile's own number of escapes
+    assert list(struct.unpack_from(f"<{n_tiles}H", buf, tc_off)) == per_tile
     return out
 
 

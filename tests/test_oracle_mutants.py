@@ -225,7 +225,63 @@ def _payload_checksum_unchecked():
     return {"zlib": Z}
 
 
+def _compact_k15_escape_without_mantissa():
+    orig = O._deserialize_compact
+
+    def _deserialize_compact(buf, scheme, N, K, E, table, plen, pcrc):
+        c = orig(buf, scheme, N, K, E, table, plen, pcrc)
+        if scheme == O.K15:
+            c.esc_val = (c.esc_val & 0xFF80).astype(np.uint16)
+        return c
+    return {"_deserialize_compact": _deserialize_compact}
+
+
+def _compact_tile_counts_cumulative():
+    # consistent on both sides: the counts section holds each tile's running
+    # total (escapes up to the tile's end) instead of the tile's own count
+    orig_ser, orig_des = O.serialize_compact, O._deserialize_compact
+
+    def serialize_compact(c):
+        saved = c.tile_index
+        try:
+            # diff of this index is saved[1:], the running totals
+            c.tile_index = np.concatenate([[0], np.cumsum(saved[1:].astype(np.int64))]).astype(np.uint32)
+            return orig_ser(c)
+        finally:
+            c.tile_index = saved
+
+    def _deserialize_compact(buf, scheme, N, K, E, table, plen, pcrc):
+        off = O.HEADER_BYTES
+        for name, size in O.section_sizes_compact(scheme, N, K, E):
+            if name == "tile_count":
+                break
+            off += O._pad(size)
+        n_tiles = -(-N * K // O.TILE)
+        raw = bytearray(buf)
+        running = np.frombuffer(bytes(raw[off: off + 2 * n_tiles]), "<u2").astype(np.int64)
+        counts = np.diff(np.concatenate([[0], running]))
+        raw[off: off + 2 * n_tiles] = counts.astype("<u2").tobytes()
+        payload = bytes(raw[O.HEADER_BYTES:])
+        return orig_des(bytes(raw[:O.HEADER_BYTES]) + payload, scheme, N, K, E, table, plen, O.zlib.crc32(payload))
+    return {"serialize_compact": serialize_compact, "_deserialize_compact": _deserialize_compact}
+
+
+def _decode_skips_bytesplit_escapes():
+    orig = O.decode
+
+    def decode(c):
+        w = orig(c)
+        if c.scheme == O.BYTESPLIT and c.E:
+            flat = w.reshape(-1)
+            flat[c.esc_pos] &= 0x00FF
+        return w
+    return {"decode": decode}
+
+
 MUTANTS = {
+    "compact_k15_escape_without_mantissa": _compact_k15_escape_without_mantissa,
+    "compact_tile_counts_cumulative": _compact_tile_counts_cumulative,
+    "decode_skips_bytesplit_escapes": _decode_skips_bytesplit_escapes,
     "tie_break_descending": _tie_break_descending,
     "least_frequent_first": _least_frequent_first,
     "codes_off_by_one": _codes_off_by_one,
