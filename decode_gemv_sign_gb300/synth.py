@@ -13,7 +13,7 @@ Two generators are provided:
   host in seconds (hundreds of millions of weights).  The bits it produces
   are copied to the host whenever the oracle has to look at them.
 
-Distributions follow the five workloads of the benchmark suite (weights
+Distributions follow the five workloads defined below (weights
 drawn N(0, sigma) or Student-t(4) scaled to sigma, with a fixed fraction of
 outlier positions taken from a seeded permutation).  Heavy Student-t tails
 are the shape the quantization-survey page on weight distributions reports
