@@ -13,7 +13,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
+import pytest  # noqa: E402
 from decode_gemv_sign_gb300 import synth  # noqa: E402
+from oracle import wcomp_oracle as O  # noqa: E402
 
 
 def test_reference_arm_line_matches_our_terms():
@@ -41,3 +43,36 @@ def test_workload_config_counts_the_dense_layer_set():
     assert cfg["tensors"] == 7
     assert cfg["elements"] == 4 * 4096 * 4096 + 3 * 4096 * 11008 == 202375168
     assert cfg["batches"] == [1, 4] and cfg["parallelism"] == "replicas x4"
+
+
+def _info(c) -> dict:
+    """The fields of wcomp_info that the byte counts use, for an oracle container
+    (section sizes padded to 32 bytes, as the library reports them)."""
+    pad = lambda x: (x + 31) // 32 * 32  # noqa: E731
+    sec = dict(O.section_sizes(c.scheme, c.N, c.K, c.E))
+    raw = pad(sec["raw"]) if c.scheme == O.BYTESPLIT else sum(pad(sec[k]) for k in ("plane_a", "plane_b", "plane_c"))
+    return {"scheme": c.scheme, "N": c.N, "K": c.K, "n": c.n, "n_tiles": c.n_tiles, "n_escapes": c.E,
+            "bytes_codes": pad(sec["codes"]), "bytes_raw": raw, "serialized_bytes": len(O.serialize(c))}
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+def test_algorithmic_bytes_per_weight(scheme):
+    """The roofline numerator against the format's per-weight sizes: a 4-bit code,
+    8 raw bits (byte-split) or 7 (K15), 16 bits written by decode, and per escape
+    a 4-byte position plus its 1- or 2-byte value."""
+    spec = synth.WeightSpec("d", 1024, 2048, "normal", 0.02, 0.001, "normal", 0.5, seed=3)
+    c = O.encode(synth.gen_weights_np(spec), scheme)
+    inf = _info(c)
+    n, E = c.n, c.E
+    assert E > 0
+    raw = 1.0 if scheme == O.BYTESPLIT else 7 / 8
+    esc = 5 if scheme == O.BYTESPLIT else 6
+    tiles = 4 * (c.n_tiles + 1) / n
+    rows = 4 * (c.N + 1) / n
+    assert bench.decode_bytes(inf) / n == pytest.approx(0.5 + raw + 2 + esc * E / n + tiles, abs=1e-12)
+    for B in (1, 4, 16):
+        io = (2 * B * c.K + 4 * B * c.N) / n
+        assert bench.gemv_bytes(inf, B) / n == pytest.approx(0.5 + raw + esc * E / n + rows + io, abs=1e-12)
+        assert bench.plain_bytes(c.N, c.K, B) / n == pytest.approx(2 + io, abs=1e-12)
+    # encode reads the source once and writes the container once (header excluded)
+    assert bench.encode_bytes(inf) == 2 * n + len(O.serialize(c)) - 96
