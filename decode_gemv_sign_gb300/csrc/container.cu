@@ -112,6 +112,7 @@ extern "C" const char* wcomp_strerror(int s) {
     case WCOMP_ECUDA: return "CUDA error";
     case WCOMP_EUNSUPPORTED: return "unsupported size";
     case WCOMP_ETIMEOUT: return "a device wait timed out";
+    case WCOMP_EINTERNAL: return "internal consistency check failed";
     default: return "unknown status";
   }
 }

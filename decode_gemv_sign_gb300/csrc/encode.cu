@@ -26,9 +26,10 @@ namespace {
 constexpr int kThreads = 256;  // pack / compact: one 8192-element tile per CTA
 
 struct Summary {
-  uint32_t E;
+  uint32_t E;         // escapes implied by the histogram: n minus the table symbols' counts
   uint16_t table[16];
-  uint32_t pad[3];
+  uint32_t scanned;   // escapes the pack pass actually found (the tile scan's total)
+  uint32_t pad[2];
 };
 
 struct EncDesc {
@@ -80,9 +81,15 @@ __global__ void __launch_bounds__(256) zero_kernel(const __grid_constant__ ZeroL
 // a1: per-tensor histogram.  Counters live in shared memory as [bins][16]
 // words; lane l owns the low half of column l (l < 16) or the high half of
 // column l - 16, so the lanes of a warp touch 16 distinct banks and two lanes
-// share a word only as its two halves.  The host sizes the grid so that no
-// 16-bit half can exceed 65535 (at most 8191 elements per thread).
+// share a word only as its two halves.  A half therefore collects the counts
+// of 8 threads (one lane of each warp).  Work is dealt out in 8-element
+// chunks, so a thread meets at most 8 x (its chunk count) elements; the host
+// (hist_blocks) sizes the grid so that no thread gets more than
+// kHistMaxChunks chunks: 8 threads x 8 x 1023 = 65472 < 65536, so a half
+// cannot wrap even when every element has the same symbol.
 // ---------------------------------------------------------------------------
+constexpr uint64_t kHistMaxChunks = 1023;
+constexpr uint32_t kHistThreads = 256;
 template <int SHIFT, int NB>
 __global__ void __launch_bounds__(256) hist_kernel(const __grid_constant__ EncBatch bt) {
   __shared__ uint32_t h[NB * 16];
@@ -428,7 +435,10 @@ __global__ void __launch_bounds__(1024) scan_kernel(const __grid_constant__ EncB
     idx[i] = run;
     run += v;
   }
-  if (threadIdx.x == 1023) idx[n_tiles] = part[1023];
+  if (threadIdx.x == 1023) {
+    idx[n_tiles] = part[1023];
+    d.summary->scanned = part[1023];  // checked on the host against the histogram's E
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -482,7 +492,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t i = i0 + 32 * k + lane;
-          if (i < count) {
+          if (i < count && first + i < d.E) {  // a count that disagrees with E is reported by the host
             pos[first + i] = p[k];
             if (SCHEME == WCOMP_BYTESPLIT)
               val[first + i] = uint8_t(v[k]);
@@ -511,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
     if (cnt) {
       const uint64_t base = g * kGroup;
       for (int e = 0; e < kGroup; ++e) {
-        if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape) {
+        if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape && o < d.E) {
           const uint32_t p = uint32_t(base + e);
           const uint32_t v = d.w[p];
           pos[o] = p;
@@ -551,6 +561,18 @@ struct Job {
   wcomp_container* c;
   EncDesc d;
 };
+
+// Histogram blocks for a tensor of n elements in a batch whose histogrammed
+// tensors hold total_n elements: about six blocks per SM spread over the
+// batch in proportion to size, but never fewer than keep every thread at or
+// below kHistMaxChunks 8-element chunks (the 16-bit counter bound in
+// hist_kernel), and never more than one chunk per thread.
+uint32_t hist_blocks(uint64_t n, uint64_t total_n, int sms) {
+  const uint64_t chunks = cdiv(n, 8);
+  const uint64_t want = std::max<uint64_t>(1, (uint64_t(sms) * 6 * n + total_n - 1) / total_n);
+  const uint64_t need = cdiv(chunks, kHistMaxChunks * kHistThreads);
+  return uint32_t(std::min<uint64_t>(std::max(want, need), cdiv(chunks, kHistThreads)));
+}
 
 void add_pad(ZeroList& z, uint8_t* base, uint64_t off, uint64_t sz) {
   const uint64_t p = padsec(sz);
@@ -694,9 +716,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
       uint32_t blocks = 0;
       for (int j = 0; j < b.count; ++j) {
         b.prefix[j] = blocks;
-        const uint64_t want = std::max<uint64_t>(1, (uint64_t(sms) * 6 * b.d[j].n + total_n - 1) / total_n);
-        const uint64_t need = cdiv(b.d[j].n, uint64_t(8191) * 256);
-        blocks += uint32_t(std::min<uint64_t>(std::max(want, need), cdiv(b.d[j].n, 8 * 256)));
+        blocks += hist_blocks(b.d[j].n, total_n, sms);
       }
       b.prefix[b.count] = blocks;
       if (scheme == WCOMP_BYTESPLIT)
@@ -746,23 +766,34 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     if (stash) cudaFreeAsync(stash, s);
     return fail(err);
   };
-  // escape counts and tables to pinned host memory, then the event the host waits on
-  Summary* hs = pinned_summaries(count);
+  // escape counts and tables to pinned host memory, then the event the host
+  // waits on; the second half of the buffer receives the summaries again
+  // after the tile scan (the escapes actually found)
+  Summary* hs = pinned_summaries(2 * count);
   if (!hs) return fail2(cudaErrorMemoryAllocation);
-  cudaEvent_t ready = nullptr;
+  Summary* hs2 = hs + count;
+  cudaEvent_t ready = nullptr, scanned = nullptr;
   e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&scanned, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemcpyAsync(hs, d_sum, sizeof(Summary) * count, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaEventRecord(ready, s);
   if (e != cudaSuccess) {
     if (ready) cudaEventDestroy(ready);
+    if (scanned) cudaEventDestroy(scanned);
     return fail2(e);
   }
-  cudaFreeAsync(d_sum, s);
-  d_sum = nullptr;
-  // past this point the copy into the pinned buffer may be in flight: wait for it before leaving
-  auto fail3 = [&](cudaError_t err) -> int {
+  // past this point copies into the pinned buffer may be in flight: wait for them before leaving
+  bool scanned_recorded = false;
+  auto drain = [&]() {
     cudaEventSynchronize(ready);
     cudaEventDestroy(ready);
+    ready = nullptr;
+    if (scanned_recorded) cudaEventSynchronize(scanned);
+    cudaEventDestroy(scanned);
+    scanned = nullptr;
+  };
+  auto fail3 = [&](cudaError_t err) -> int {
+    drain();
     return fail2(err);
   };
   // a3: pack (with the stash), then the tile scan.  A byte-split job and a
@@ -814,10 +845,15 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     count_launches(1);
   });
   if (e != cudaSuccess) return fail3(e);
-  // the one synchronization: escape counts and tables
+  e = cudaMemcpyAsync(hs2, d_sum, sizeof(Summary) * count, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaEventRecord(scanned, s);
+  if (e != cudaSuccess) return fail3(e);
+  scanned_recorded = true;
+  cudaFreeAsync(d_sum, s);
+  d_sum = nullptr;
+  // first wait: escape counts and tables (pack and the scan keep running)
   e = cudaEventSynchronize(ready);
-  cudaEventDestroy(ready);
-  if (e != cudaSuccess) return fail2(e);
+  if (e != cudaSuccess) return fail3(e);
   for (int i = 0; i < count; ++i) {
     wcomp_container* c = jobs[i].c;
     memcpy(c->table, hs[i].table, sizeof(c->table));
@@ -829,14 +865,14 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     d.off_val = L.off_val;
     if (L.E) {
       e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
-      if (e != cudaSuccess) return fail2(e);
+      if (e != cudaSuccess) return fail3(e);
       d.esc = c->d_esc;
       add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
       add_pad(z, c->d_esc, L.off_val, L.sz_val);
-      if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
+      if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail3(e);
     }
   }
-  if ((e = launch_zero(z, s)) != cudaSuccess) return fail2(e);
+  if ((e = launch_zero(z, s)) != cudaSuccess) return fail3(e);
   // a4: compaction for tensors with escapes; row indexes for all
   std::vector<Job> with_esc;
   for (auto& j : jobs)
@@ -851,7 +887,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     compact_kernel<<<blocks, kThreads, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail2(e);
+  if (e != cudaSuccess) return fail3(e);
   e = for_chunks(jobs, -1, [&](EncBatch& b) {
     uint32_t rows = 0;
     for (int j = 0; j < b.count; ++j) {
@@ -862,8 +898,23 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     row_index_kernel<<<unsigned(cdiv(rows, 256)), 256, 0, s>>>(b);
     count_launches(1);
   });
-  if (e != cudaSuccess) return fail2(e);
+  if (e != cudaSuccess) return fail3(e);
   if (stash) cudaFreeAsync(stash, s);
+  stash = nullptr;
+  // second wait, for the tile scan (the compaction and the row indexes queued
+  // above keep running): the escapes pack found must number the E the
+  // histogram implied, which sized the escape streams.  A mismatch means a
+  // wrong histogram; the compaction wrote nothing past E, and no container is
+  // returned.
+  e = cudaEventSynchronize(scanned);
+  drain();
+  if (e != cudaSuccess) return fail2(e);
+  for (int i = 0; i < count; ++i)
+    if (hs2[i].scanned != hs[i].E) {
+      for (auto& j : jobs)
+        if (j.c) wcomp_free(j.c, s);
+      return WCOMP_EINTERNAL;
+    }
   for (int i = 0; i < count; ++i) out[i] = jobs[i].c;
   return WCOMP_OK;
 }
@@ -879,6 +930,17 @@ extern "C" int wcomp_encode(const uint16_t* d_w, int64_t N, int64_t K, int schem
   *out = nullptr;
   if (!d_w || N <= 0 || K <= 0) return WCOMP_EINVAL;
   return encode_many(&d_w, &N, &K, &scheme, 1, static_cast<cudaStream_t>(stream), out);
+}
+
+extern "C" int wcomp_encode_hist_grid(const uint64_t* n, int count, int sms, uint32_t* blocks) {
+  if (!n || !blocks || count <= 0 || sms <= 0) return WCOMP_EINVAL;
+  uint64_t total_n = 0;
+  for (int i = 0; i < count; ++i) {
+    if (n[i] == 0 || n[i] >= (uint64_t(1) << 32)) return WCOMP_EINVAL;
+    total_n += n[i];
+  }
+  for (int i = 0; i < count; ++i) blocks[i] = hist_blocks(n[i], total_n, sms);
+  return WCOMP_OK;
 }
 
 extern "C" int wcomp_encode_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,

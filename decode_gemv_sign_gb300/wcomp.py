@@ -20,7 +20,7 @@ BYTESPLIT = 0
 K15 = 1
 SCHEMES = {"bytesplit": BYTESPLIT, "byte-split": BYTESPLIT, "k15": K15, BYTESPLIT: BYTESPLIT, K15: K15}
 
-OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED, ETIMEOUT, EINTERNAL = 0, -1, -2, -3, -4, -5, -6, -7
 
 
 class WcompError(RuntimeError):
@@ -68,6 +68,8 @@ def lib():
     L.wcomp_encode_batched.argtypes = [ctypes.POINTER(P), ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int), ctypes.c_int,
                                        P, ctypes.POINTER(P)]
+    L.wcomp_encode_hist_grid.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_uint32)]
     L.wcomp_decode.argtypes = [P, P, P]
     L.wcomp_gemv.argtypes = [P, P, ctypes.c_int, P, P]
     L.wcomp_gemv_noalloc.argtypes = [P, P, ctypes.c_int, P, P]
@@ -91,7 +93,7 @@ def lib():
     L.wcomp_device_check.restype = ctypes.c_int
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
-    for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
+    for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_encode_hist_grid", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
                  "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
                  "wcomp_decode_batched",
                  "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_serialize_compact",

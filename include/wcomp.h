@@ -68,7 +68,8 @@ typedef enum {
   WCOMP_ECORRUPT = -3,      /* serialized container failed validation */
   WCOMP_ECUDA = -4,         /* a CUDA runtime call failed */
   WCOMP_EUNSUPPORTED = -5,  /* size outside the supported range */
-  WCOMP_ETIMEOUT = -6       /* a kernel's bounded wait on its own copies ran out */
+  WCOMP_ETIMEOUT = -6,      /* a kernel's bounded wait on its own copies ran out */
+  WCOMP_EINTERNAL = -7      /* an internal consistency check failed; no result was returned */
 } wcomp_status;
 
 typedef struct wcomp_container wcomp_container;
@@ -104,17 +105,42 @@ typedef struct {
  * table of the 15 most frequent symbols (count descending, symbol ascending),
  * 4-bit packing of codes and raw bits, per-tile escape counts and their scan,
  * escape compaction in ascending position order, tile and row escape indexes.
- * Synchronizes `stream` once to learn the escape count, which sizes the
- * escape stream.  Output is deterministic and byte-identical to the CPU oracle.
+ * Waits on `stream` twice: once for the escape count the histogram implies,
+ * which sizes the escape stream (the pack and scan kernels keep running
+ * meanwhile), and once for the tile scan, whose total must equal that count
+ * (else WCOMP_EINTERNAL and no container).  The escape compaction and the row
+ * index are still running on `stream` when the call returns.  Output is
+ * deterministic and byte-identical to the CPU oracle.
+ * Definition: forgeeks page "Prueba de GLM-5.2 reduce la memoria BF16 en casi
+ * un 25%", section "Cómo funciona la compresión": the sign+exponent symbol
+ * (8 bits for byte-split, 9 for K15) gets a 4-bit code into the tensor's
+ * table of 15 symbols, code 15 marks an escape kept exactly, the low byte or
+ * 7-bit mantissa is stored as is.
  */
 WCOMP_API int wcomp_encode(const uint16_t* d_w, int64_t N, int64_t K, int scheme, void* stream,
                  wcomp_container** out);
 
 /*
+ * How wcomp_encode_batched sizes its histogram grid (host-side, no device
+ * work; exposed so the sizing can be checked without a GPU).  n[i] is the
+ * element count of tensor i of a batch whose tensors are all histogrammed,
+ * sms the device's SM count; blocks[i] receives the number of 256-thread
+ * blocks tensor i gets.  Thread t of block b counts the 8-element chunks
+ * b * 256 + t, b * 256 + t + 256 * blocks[i], ...; the counters are 16-bit
+ * halves shared by 8 threads, so no thread may be given more than 1023
+ * chunks (8 x 8 x 1023 = 65472 elements per half).  Returns WCOMP_EINVAL for
+ * a null pointer, count or sms <= 0, or an n outside [1, 2^32).
+ */
+WCOMP_API int wcomp_encode_hist_grid(const uint64_t* n, int count, int sms, uint32_t* blocks);
+
+/*
  * Encode `count` tensors in one pass: tensor i is W_i[N[i], K[i]] at d_w[i],
  * coded with schemes[i]; out[i] receives its container.  The same steps as
- * wcomp_encode run as batched launches over all tensors, with one stream
- * synchronization for the whole batch.  On failure every out[i] is NULL.
+ * wcomp_encode run as batched launches over all tensors, with the same two
+ * waits on `stream` for the whole batch (escape counts, then the scan check).
+ * On failure every out[i] is NULL.
+ * Definition: as wcomp_encode (forgeeks page, "Cómo funciona la compresión";
+ * one table per tensor).
  */
 WCOMP_API int wcomp_encode_batched(const uint16_t* const* d_w, const int64_t* N, const int64_t* K,
                                    const int* schemes, int count, void* stream, wcomp_container** out);
