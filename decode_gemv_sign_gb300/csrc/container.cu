@@ -311,17 +311,19 @@ static int validate(const uint8_t* b, uint64_t len, const Layout& L) {
   return WCOMP_OK;
 }
 
-// K15 mantissa of element i from the three planes (a 32-element group holds
-// 16 bytes of plane A, 8 of plane B, 4 of plane C; element 4q + l of the
-// group sits in byte l of its words, bit field q of the quad order).
+// K15 mantissa of element i.  A 32-element group keeps 28 mantissa bytes: 16
+// in plane A, 8 in plane B, 4 in plane C.  Byte j < 28 holds element j in
+// bits 0..6; bit 7 of byte 4 q + l holds bit q of element 28 + l.
 static uint32_t k15_mantissa(const uint8_t* pa, const uint8_t* pb, const uint8_t* pc, uint64_t i) {
   const uint64_t g = i >> 5;
-  const uint32_t e = uint32_t(i & 31), q = e >> 2, lane = e & 3;
-  const uint32_t wa = get32(pa + 16 * g + 4 * (q >> 1));
-  const uint32_t wb = get32(pb + 8 * g + 4 * (q >> 2));
-  const uint32_t wc = get32(pc + 4 * g);
-  return ((wa >> (8 * lane + 4 * (q & 1))) & 15u) | (((wb >> (8 * lane + 2 * (q & 3))) & 3u) << 4) |
-         (((wc >> (8 * lane + q)) & 1u) << 6);
+  const uint32_t e = uint32_t(i & 31);
+  auto byte_at = [&](uint32_t j) -> uint32_t {
+    return j < 16 ? pa[16 * g + j] : j < 24 ? pb[8 * g + (j - 16)] : pc[4 * g + (j - 24)];
+  };
+  if (e < 28) return byte_at(e) & 0x7Fu;
+  uint32_t m = 0;
+  for (uint32_t q = 0; q < 7; ++q) m |= ((byte_at(4 * q + (e - 28)) >> 7) & 1u) << q;
+  return m;
 }
 
 // Compact form: check the payload and rebuild the version-1 sections

@@ -9,9 +9,10 @@
 // One CTA of 256 threads decodes one 8192-element tile: thread j expands the
 // 32 codes of its group through the register table (prmt lookups), joins the
 // raw bytes / mantissa planes, and writes 64 bytes with two 256-bit stores.
-// Escaped elements first receive the placeholder symbol 0; then every warp
-// writes the escapes of its own 1024 elements over them, taken from the
-// tile's escape slice (found in O(1) through the tile index).
+// Escaped elements first receive the placeholder symbol 0; after a CTA
+// barrier the threads write the tile's escapes over them, one entry each,
+// from the tile's slice of the escape stream (found in O(1) through the tile
+// index).
 #include <string.h>
 
 #include <algorithm>
@@ -40,17 +41,12 @@ __device__ __forceinline__ void decode_tile(const TensorDesc& d, uint16_t* __res
     }
   }
   const uint32_t e0 = d.tile_index[tile], e1 = d.tile_index[tile + 1];
-  if (e0 == e1) return;
-  // Each warp patches the escapes of its own 1024 elements: the lanes walk the
-  // tile's escape slice and keep the positions in the warp's range.  A warp
-  // barrier orders the placeholder stores above before the patches; no CTA
-  // barrier is needed.
-  __syncwarp();
-  const uint64_t lo = uint64_t(tile) * kTile + (threadIdx.x >> 5) * (kTile / (kThreads / 32));
-  const uint64_t hi = lo + kTile / (kThreads / 32);
-  for (uint32_t e = e0 + (threadIdx.x & 31); e < e1; e += 32) {
+  if (e0 == e1) return;  // the same for every thread of the CTA
+  // The CTA's threads share the tile's escape slice, one entry each: a CTA
+  // barrier orders every placeholder store of the tile before the patches.
+  __syncthreads();
+  for (uint32_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
     const uint32_t p = d.esc_pos[e];
-    if (p < lo || p >= hi) continue;
     if (SCHEME == WCOMP_BYTESPLIT)
       reinterpret_cast<uint8_t*>(out)[2 * uint64_t(p) + 1] = d.esc_val[e];  // high byte only
     else

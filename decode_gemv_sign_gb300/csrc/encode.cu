@@ -280,20 +280,16 @@ __device__ __forceinline__ uint32_t pack_group(const EncDesc& d, uint64_t g, con
     *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     if (base + 16 < n) *reinterpret_cast<uint4*>(m + d.off_raw + 32 * g + 16) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   } else {
-    // K15 planes from the mantissa bytes (bit 7 of a low byte is exponent
-    // bit 0 and is never selected): plane A word q/2 takes bits 0..3 of
-    // quad q (high nibble for odd q), plane B word q/4 bits 4..5 at bit
-    // offset 2 (q mod 4), plane C bit 6 at bit offset q of every byte
-    uint32_t a[4], b[2] = {0u, 0u}, c = 0u;
+    // K15 mantissa bytes from the low bytes (bit 7 of a low byte is the
+    // exponent bit and is dropped): word q < 7 is quad q's four mantissas
+    // with bit 7 of byte lane i carrying bit q of element 28 + i's mantissa
+    uint32_t a[4], b[2], c;
+    uint32_t wq[7];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = (lo[2 * i] & 0x0F0F0F0Fu) | ((lo[2 * i + 1] << 4) & 0xF0F0F0F0u);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = q & 3;
-      b[q >> 2] |= j <= 2 ? ((lo[q] >> (4 - 2 * j)) & (0x03030303u << (2 * j)))
-                          : ((lo[q] << 2) & 0xC0C0C0C0u);
-      c |= q <= 6 ? ((lo[q] >> (6 - q)) & (0x01010101u << q)) : ((lo[q] << 1) & 0x80808080u);
-    }
+    for (int q = 0; q < 7; ++q) wq[q] = (lo[q] & 0x7F7F7F7Fu) | (((lo[7] >> q) << 7) & 0x80808080u);
+    a[0] = wq[0]; a[1] = wq[1]; a[2] = wq[2]; a[3] = wq[3];
+    b[0] = wq[4]; b[1] = wq[5];
+    c = wq[6];
     *reinterpret_cast<uint4*>(m + d.off_a + 16 * g) = make_uint4(a[0], a[1], a[2], a[3]);
     *reinterpret_cast<uint2*>(m + d.off_b + 8 * g) = make_uint2(b[0], b[1]);
     *reinterpret_cast<uint32_t*>(m + d.off_c + 4 * g) = c;

@@ -3,8 +3,11 @@
 // the register-level decode helpers.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is reached through the runtime)
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "../../include/wcomp.h"
 
@@ -85,6 +88,11 @@ struct wcomp_container {
   uint8_t* d_main = nullptr;
   uint8_t* d_esc = nullptr;
   int device = 0;
+  // TMA descriptors of the code and raw / mantissa streams, made on the
+  // first fused GEMV (tmap_ok: 1 made, 0 not applicable to this shape)
+  CUtensorMap tmap[4];
+  int tmap_ok = 0;
+  std::once_flag tmap_once;
 };
 
 namespace wc {
@@ -204,14 +212,16 @@ __device__ __forceinline__ void lookup8(const uint32_t* t4, uint32_t m7, const Q
   q1 = lop_select(prmt(t4[0], t4[1], h), prmt(t4[2], t4[3], h), m.m1);
 }
 
-// K15 mantissa of quad q (4 elements) of a 32-element group, one byte each.
-template <int Q>
-__device__ __forceinline__ uint32_t k15_mant(const uint32_t* a, const uint32_t* b, uint32_t c) {
-  uint32_t ma = (Q & 1) ? ((a[Q >> 1] >> 4) & 0x0F0F0F0Fu) : (a[Q >> 1] & 0x0F0F0F0Fu);
-  constexpr int sb = 2 * (Q & 3);
-  uint32_t mb = sb <= 4 ? ((b[Q >> 2] << (4 - sb)) & 0x30303030u) : ((b[Q >> 2] >> (sb - 4)) & 0x30303030u);
-  uint32_t mc = Q <= 6 ? ((c << (6 - Q)) & 0x40404040u) : ((c >> (Q - 6)) & 0x40404040u);
-  return ma | mb | mc;
+// K15 mantissas.  A 32-element group keeps its 7-bit mantissas in 28 bytes,
+// seen as seven 32-bit words W0..W6 (W0..W3 in plane A, W4..W5 in plane B,
+// W6 in plane C): byte lane i of W_q holds element 4q + i in bits 0..6, and
+// its bit 7 holds bit q of the mantissa of element 28 + i.  Quad q < 7 is
+// therefore W_q with bit 7 cleared; quad 7 gathers bit 7 of every word.
+__device__ __forceinline__ uint32_t k15_tail(const uint32_t (&w)[7]) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int q = 0; q < 7; ++q) r |= (w[q] >> (7 - q)) & (0x01010101u << q);
+  return r;
 }
 
 // Decode one 32-element group into 16 words of BF16 pairs (element 2j in the
@@ -242,17 +252,14 @@ __device__ __forceinline__ void decode_group(const RegTable& t, const uint32_t (
   }
 }
 
-// K15: the 8 mantissa quads of a group from its plane words.
+// K15: the 8 mantissa quads of a group from its plane words (bit 7 of every
+// byte cleared; the exponent bit is added by the caller).
 __device__ __forceinline__ void k15_mantissas(const uint32_t (&a)[4], const uint32_t (&b)[2], uint32_t c,
                                               uint32_t (&r)[8]) {
-  r[0] = k15_mant<0>(a, b, c);
-  r[1] = k15_mant<1>(a, b, c);
-  r[2] = k15_mant<2>(a, b, c);
-  r[3] = k15_mant<3>(a, b, c);
-  r[4] = k15_mant<4>(a, b, c);
-  r[5] = k15_mant<5>(a, b, c);
-  r[6] = k15_mant<6>(a, b, c);
-  r[7] = k15_mant<7>(a, b, c);
+  const uint32_t w[7] = {a[0], a[1], a[2], a[3], b[0], b[1], c};
+#pragma unroll
+  for (int q = 0; q < 7; ++q) r[q] = w[q] & 0x7F7F7F7Fu;
+  r[7] = k15_tail(w);
 }
 
 // Streaming loads that do not keep the weights in L1.
@@ -303,6 +310,22 @@ __device__ __forceinline__ void load_group(const TensorDesc& d, uint64_t g, uint
   }
 }
 
+// Byte j (0..27) of the mantissa bytes of group g: plane A bytes 0..15,
+// plane B bytes 16..23, plane C bytes 24..27.
+__device__ __forceinline__ uint32_t k15_mant_byte(const TensorDesc& d, uint64_t g, uint32_t j) {
+  return j < 16 ? d.pa[16 * g + j] : j < 24 ? d.pb[8 * g + (j - 16)] : d.pc[4 * g + (j - 24)];
+}
+
+// The 7-bit mantissa of element i.
+__device__ __forceinline__ uint32_t k15_mant_elem(const TensorDesc& d, uint64_t i) {
+  const uint64_t g = i >> 5;
+  const uint32_t e = uint32_t(i & 31);
+  if (e < 28) return k15_mant_byte(d, g, e) & 0x7F;
+  uint32_t m = 0;
+  for (uint32_t q = 0; q < 7; ++q) m |= ((k15_mant_byte(d, g, 4 * q + (e - 28)) >> 7) & 1u) << q;
+  return m;
+}
+
 // Element-wise decode of element i (any alignment; escapes give the placeholder).
 __device__ __forceinline__ uint32_t decode_elem_placeholder(const TensorDesc& d, uint64_t i) {
   uint32_t code = (d.codes[i >> 1] >> (4 * (i & 1))) & 0xF;
@@ -312,12 +335,7 @@ __device__ __forceinline__ uint32_t decode_elem_placeholder(const TensorDesc& d,
     lo = d.raw[i];
   } else {
     uint32_t e0 = (d.t.e0[code >> 2] >> (8 * (code & 3))) & 0x80;
-    uint64_t g = i >> 5;
-    uint32_t e = uint32_t(i & 31), q = e >> 2, lane = e & 3;
-    uint32_t a = (d.pa[16 * g + 4 * (q >> 1) + lane] >> (4 * (q & 1))) & 0xF;
-    uint32_t b = (d.pb[8 * g + 4 * (q >> 2) + lane] >> (2 * (q & 3))) & 0x3;
-    uint32_t c = (d.pc[4 * g + lane] >> q) & 0x1;
-    lo = e0 | a | (b << 4) | (c << 6);
+    lo = e0 | k15_mant_elem(d, i);
   }
   return (hi << 8) | lo;
 }

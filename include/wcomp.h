@@ -162,14 +162,19 @@ WCOMP_API int wcomp_decode(const wcomp_container* c, uint16_t* d_out, void* stre
  *   d_y     device, float[B*N], row-major; overwritten.
  * W is rebuilt in registers from the codes and raw bits; escaped weights are
  * corrected inside the same kernel (y += x * (w_true - w_placeholder)).
- * Products and sums are fp32 (CUDA-core FMAs for small batches, BF16 tensor
- * core MMAs with fp32 accumulation for larger ones); the summation order is
- * fixed (no atomics), so repeated calls give identical bits.
+ * Products run on the tensor cores (BF16 MMAs with fp32 accumulation); the
+ * summation order is fixed (no atomics), so repeated calls give identical
+ * bits.  Shapes with K % 32 != 0 (K15: K % 128 != 0) or an x that is not
+ * 16-byte aligned take a slower element-by-element path with the same result
+ * contract.
  * Memory: the work counters live in a device buffer the library allocates
  * with cudaMalloc on first use per device; a K15 container at B >= 3 also
  * takes a transposed copy of x (K * 4..16 * 2 bytes) from the library's
  * stream-ordered pool for the duration of the call.  wcomp_gemv_noalloc
  * allocates nothing.
+ * Errors found on the device (a copy that never completed) do not fail the
+ * call: the kernel records them and stops waiting; wcomp_device_check
+ * reports them.
  * Definition: forgeeks page, "Qué queda por demostrar" (GEMV on codes rebuilt
  * in registers, escape correction); wavect page on rebuilding exact BF16 in
  * registers for the matmul.
@@ -229,9 +234,12 @@ WCOMP_API int wcomp_gemv_batched(const wcomp_container* const* containers, const
                        int B, float* const* d_y, int count, void* stream);
 
 /*
- * Report and clear the device error word of the current device: kernels
- * whose bounded waits run out record it there and stop early instead of
- * hanging.  Synchronizes `stream`.  Returns WCOMP_OK or WCOMP_ETIMEOUT.
+ * Report and clear the device error words of the current device (the one
+ * wcomp_gemv and the batched GEMVs use, and the one in wcomp_gemv_noalloc's
+ * static array).  A GEMV kernel whose bounded wait on its own tensor copies
+ * runs out records it there and finishes without waiting instead of hanging;
+ * its outputs are then undefined.  Synchronizes `stream`.  Returns WCOMP_OK
+ * or WCOMP_ETIMEOUT.
  */
 WCOMP_API int wcomp_device_check(void* stream);
 

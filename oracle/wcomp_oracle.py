@@ -34,7 +34,7 @@ Readings where the pages are silent (each is listed in the design notes):
   for byte-split the value is the high byte, for K15 the value is the whole
   16-bit word (its top 9 bits are the symbol, the low 7 repeat the raw
   mantissa so the weight can be rebuilt from the entry alone);
-* the physical container layout (nibble order, K15 bit planes, indexes,
+* the physical container layout (nibble order, K15 mantissa bytes, indexes,
   header, checksums) is this library's own and is defined here; it has two
   serialized forms: version 1 keeps the (position, value) escape stream and
   both indexes, version 2 (compact) keeps only what the pages count: the
@@ -72,7 +72,7 @@ SCHEMES = (BYTESPLIT, K15)
 TABLE_SIZE = 15
 ESCAPE = 15
 TILE = 8192  # elements per decode tile (granule of the tile escape index)
-GROUP = 32  # elements per K15 raw-plane group
+GROUP = 32  # elements per K15 mantissa group (28 bytes)
 HEADER_BYTES = 96
 ALIGN = 32  # every payload section starts on a 32-byte boundary (256-bit loads)
 
@@ -160,61 +160,42 @@ def pack_nibbles(codes: np.ndarray) -> np.ndarray:
 
 
 def pack_k15_planes(raw7: np.ndarray) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
-    """The 7 mantissa bits of every element in three planes of 4, 2 and 1 bits.
+    """The 7 mantissa bits of every element, 28 bytes per 32-element group.
 
-    Elements are taken in groups of 32 (the last group zero padded).  Inside
-    a group, element e = 4 q + i belongs to quad q (0..7) at lane i (0..3).
+    The pages store the K15 mantissa uncompressed at 7 bits per weight but
+    give it no physical layout; this is the library's own.  Elements are taken
+    in groups of 32 (the last group zero padded).  Byte j (j < 28) of a group
+    holds element j's mantissa in bits 0..6; bit 7 of byte j holds bit
+    j // 4 of the mantissa of element 28 + j % 4.  So element 28 + i is spread
+    over bit 7 of bytes i, 4 + i, ..., 24 + i (its bits 0 .. 6), and byte j
+    sits in byte lane j % 4 of 32-bit word j // 4.
 
-    * plane A (mantissa bits 0..3), 16 bytes per group: 32-bit word q // 2,
-      byte i holds quad q's lane-i nibble in its low half when q is even and
-      in its high half when q is odd;
-    * plane B (mantissa bits 4..5), 8 bytes per group: 32-bit word q // 4,
-      bits 8 i + 2 (q % 4) .. +1;
-    * plane C (mantissa bit 6), 4 bytes per group: bit 8 i + q.
-
-    Each quad therefore sits in the same byte lanes of all three planes, so a
-    decoder rebuilds four mantissas with word-wide shifts and masks.
+    The 28 bytes are split into three sections with power-of-two strides:
+    ``plane_a`` bytes 0..15 (16 per group), ``plane_b`` bytes 16..23 (8 per
+    group) and ``plane_c`` bytes 24..27 (4 per group).
     """
     n = raw7.size
     groups = _cdiv(n, GROUP)
     m = np.zeros(groups * GROUP, dtype=np.uint32)
     m[:n] = raw7
-    m = m.reshape(groups, 8, 4)  # [group, quad q, lane i]
-    a = m & 0xF
-    b = (m >> 4) & 0x3
-    c = (m >> 6) & 0x1
-    q = np.arange(8, dtype=np.uint32).reshape(1, 8, 1)
-    i = np.arange(4, dtype=np.uint32).reshape(1, 1, 4)
-    # plane A: word q//2, bit position 8 i + 4 (q % 2)
-    wa = np.zeros((groups, 4), dtype=np.uint32)
-    contrib_a = a << (8 * i + 4 * (q % 2))
-    for qq in range(8):
-        wa[:, qq // 2] |= np.bitwise_or.reduce(contrib_a[:, qq, :], axis=1)
-    # plane B: word q//4, bit position 8 i + 2 (q % 4)
-    wb = np.zeros((groups, 2), dtype=np.uint32)
-    contrib_b = b << (8 * i + 2 * (q % 4))
-    for qq in range(8):
-        wb[:, qq // 4] |= np.bitwise_or.reduce(contrib_b[:, qq, :], axis=1)
-    # plane C: one word, bit position 8 i + q
-    contrib_c = c << (8 * i + q)
-    wc = np.bitwise_or.reduce(contrib_c.reshape(groups, 32), axis=1).astype(np.uint32)
-    return (wa.astype("<u4").reshape(-1).view(np.uint8),
-            wb.astype("<u4").reshape(-1).view(np.uint8),
-            wc.astype("<u4").reshape(-1).view(np.uint8))
+    m = m.reshape(groups, GROUP)
+    j = np.arange(28)
+    tail_bit = (m[:, 28 + (j % 4)] >> (j // 4)) & 1  # [group, byte j]
+    mb = (m[:, :28] | (tail_bit << 7)).astype(np.uint8)
+    return (mb[:, :16].reshape(-1).copy(), mb[:, 16:24].reshape(-1).copy(), mb[:, 24:28].reshape(-1).copy())
 
 
 def unpack_k15_planes(pa: np.ndarray, pb: np.ndarray, pc: np.ndarray, n: int) -> np.ndarray:
     """Inverse of :func:`pack_k15_planes` (returns the n 7-bit mantissas)."""
     groups = _cdiv(n, GROUP)
-    wa = np.frombuffer(pa[: 16 * groups].tobytes(), dtype="<u4").reshape(groups, 4).astype(np.uint32)
-    wb = np.frombuffer(pb[: 8 * groups].tobytes(), dtype="<u4").reshape(groups, 2).astype(np.uint32)
-    wc = np.frombuffer(pc[: 4 * groups].tobytes(), dtype="<u4").reshape(groups).astype(np.uint32)
-    q = np.arange(8, dtype=np.uint32).reshape(1, 8, 1)
-    i = np.arange(4, dtype=np.uint32).reshape(1, 1, 4)
-    a = (wa[:, (q // 2).reshape(8)].reshape(groups, 8, 1) >> (8 * i + 4 * (q % 2))) & 0xF
-    b = (wb[:, (q // 4).reshape(8)].reshape(groups, 8, 1) >> (8 * i + 2 * (q % 4))) & 0x3
-    c = (wc.reshape(groups, 1, 1) >> (8 * i + q)) & 0x1
-    m = (a | (b << 4) | (c << 6)).reshape(-1)
+    mb = np.concatenate([np.asarray(pa[: 16 * groups], np.uint8).reshape(groups, 16),
+                         np.asarray(pb[: 8 * groups], np.uint8).reshape(groups, 8),
+                         np.asarray(pc[: 4 * groups], np.uint8).reshape(groups, 4)], axis=1).astype(np.uint32)
+    head = mb & 0x7F  # elements 0..27
+    tail = np.zeros((groups, 4), dtype=np.uint32)  # elements 28..31
+    for b in range(7):
+        tail |= ((mb[:, 4 * b:4 * b + 4] >> 7) & 1) << b
+    m = np.concatenate([head, tail], axis=1).reshape(-1)
     return m[:n].astype(np.uint32)
 
 

@@ -60,12 +60,13 @@ def read_all_compact_pure(buf: bytes) -> list:
             low = buf[raw_off + i]
         else:
             g, e = divmod(i, 32)
-            q, lane = divmod(e, 4)
-            wa = struct.unpack_from("<I", buf, a_off + 16 * g + 4 * (q // 2))[0]
-            wb = struct.unpack_from("<I", buf, b_off + 8 * g + 4 * (q // 4))[0]
-            wc = struct.unpack_from("<I", buf, c_off + 4 * g)[0]
-            low = (((wa >> (8 * lane + 4 * (q % 2))) & 15) + 16 * ((wb >> (8 * lane + 2 * (q % 4))) & 3) +
-                   64 * ((wc >> (8 * lane + q)) & 1))
+            def mbyte(j):
+                if j < 16:
+                    return buf[a_off + 16 * g + j]
+                if j < 24:
+                    return buf[b_off + 8 * g + j - 16]
+                return buf[c_off + 4 * g + j - 24]
+            low = (mbyte(e) & 0x7F) if e < 28 else sum(((mbyte(4 * b + e - 28) >> 7) & 1) << b for b in range(7))
         if code != 15:
             sym = table[code]
         elif scheme == 0:

@@ -135,6 +135,32 @@ def _k15_planes_neighbours_swapped():
                                                             -(-n // 32) * 32)[:n]}
 
 
+def _k15_tail_bits_reversed():
+    # consistent on both sides: bit b of a tail element goes to byte 4 (6 - b) + i
+    # instead of byte 4 b + i, so everything still round-trips
+    def pack(raw7):
+        n = raw7.size
+        groups = -(-n // 32)
+        m = np.zeros(groups * 32, dtype=np.uint32)
+        m[:n] = raw7
+        m = m.reshape(groups, 32)
+        j = np.arange(28)
+        tail_bit = (m[:, 28 + (j % 4)] >> (6 - j // 4)) & 1
+        mb = (m[:, :28] | (tail_bit << 7)).astype(np.uint8)
+        return mb[:, :16].reshape(-1).copy(), mb[:, 16:24].reshape(-1).copy(), mb[:, 24:28].reshape(-1).copy()
+
+    def unpack(pa, pb, pc, n):
+        groups = -(-n // 32)
+        mb = np.concatenate([pa[:16 * groups].reshape(groups, 16), pb[:8 * groups].reshape(groups, 8),
+                             pc[:4 * groups].reshape(groups, 4)], axis=1).astype(np.uint32)
+        tail = np.zeros((groups, 4), dtype=np.uint32)
+        for b in range(7):
+            tail |= ((mb[:, 4 * (6 - b):4 * (6 - b) + 4] >> 7) & 1) << b
+        return np.concatenate([mb & 0x7F, tail], axis=1).reshape(-1)[:n].astype(np.uint32)
+
+    return {"pack_k15_planes": pack, "unpack_k15_planes": unpack}
+
+
 def _index_counts_at_or_below():
     return {"escape_index": lambda pos, bounds: np.searchsorted(pos, bounds, side="right").astype(np.uint32)}
 
@@ -289,6 +315,7 @@ MUTANTS = {
     "k15_symbol_width_8": _k15_symbol_width_8,
     "nibbles_high_first": _nibbles_high_first,
     "k15_planes_neighbours_swapped": _k15_planes_neighbours_swapped,
+    "k15_tail_bits_reversed": _k15_tail_bits_reversed,
     "index_counts_at_or_below": _index_counts_at_or_below,
     "k15_escape_keeps_symbol_only": _k15_escape_keeps_symbol_only,
     "decode_rows_ignores_escapes": _decode_rows_ignores_escapes,

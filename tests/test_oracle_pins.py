@@ -62,14 +62,17 @@ def read_element_pure(buf: bytes, i: int) -> int:
         low = buf[raw_off + i]
     else:
         g, e = divmod(i, 32)
-        q, lane = divmod(e, 4)
-        wa = struct.unpack_from("<I", buf, a_off + 16 * g + 4 * (q // 2))[0]
-        wb = struct.unpack_from("<I", buf, b_off + 8 * g + 4 * (q // 4))[0]
-        wc = struct.unpack_from("<I", buf, c_off + 4 * g)[0]
-        m0 = (wa >> (8 * lane + 4 * (q % 2))) & 15
-        m1 = (wb >> (8 * lane + 2 * (q % 4))) & 3
-        m2 = (wc >> (8 * lane + q)) & 1
-        low = m0 + 16 * m1 + 64 * m2
+        # byte j of the group's 28 mantissa bytes: 16 in section A, 8 in B, 4 in C
+        def mbyte(j):
+            if j < 16:
+                return buf[a_off + 16 * g + j]
+            if j < 24:
+                return buf[b_off + 8 * g + j - 16]
+            return buf[c_off + 4 * g + j - 24]
+        if e < 28:
+            low = mbyte(e) & 0x7F
+        else:
+            low = sum(((mbyte(4 * b + e - 28) >> 7) & 1) << b for b in range(7))
     if code != 15:
         sym = table[code]
         return (sym << 8) | low if scheme == 0 else (sym << 7) | low
@@ -199,26 +202,37 @@ def test_nibble_order_fixture():
 
 
 def test_k15_plane_bit_positions():
-    # one element with mantissa 0b1011011 at e = 13 (group 0, quad 3, lane 1)
-    m = np.zeros(40, dtype=np.uint32)
+    # group 0: element 13 (a head element) has mantissa 0b1011011, element 30
+    # (tail element 2) has 0b1000101; group 1: element 32 + 5 = 0b1000001,
+    # tail element 32 + 31 (tail 3) = 0b0000011
+    m = np.zeros(64, dtype=np.uint32)
     m[13] = 0b1011011
-    m[32 + 5] = 0b1000001  # group 1, quad 1, lane 1
+    m[30] = 0b1000101
+    m[32 + 5] = 0b1000001
+    m[32 + 31] = 0b0000011
     pa, pb, pc = O.pack_k15_planes(m)
+    assert pa.size == 32 and pb.size == 16 and pc.size == 8  # 16 + 8 + 4 bytes per group
+    mb0 = np.concatenate([pa[:16], pb[:8], pc[:4]])
+    mb1 = np.concatenate([pa[16:], pb[8:], pc[4:]])
+    # head element 13: byte 13, bits 0..6 (plane A, word 3, byte lane 1)
+    expect0 = np.zeros(28, dtype=np.uint8)
+    expect0[13] = 0b1011011
+    # tail element 30 = 28 + 2: bit b in bit 7 of byte 4 b + 2; its bits 0, 2 and 6 are set
+    for b in (0, 2, 6):
+        expect0[4 * b + 2] |= 0x80
+    assert np.array_equal(mb0, expect0)
+    expect1 = np.zeros(28, dtype=np.uint8)
+    expect1[5] = 0b1000001
+    for b in (0, 1):  # tail element 3 of group 1 (element 63): bits 0 and 1
+        expect1[4 * b + 3] |= 0x80
+    assert np.array_equal(mb1, expect1)
+    # the three sections as little-endian words: byte 13 is lane 1 of word 3 of plane A
     a = np.frombuffer(pa.tobytes(), "<u4")
-    b = np.frombuffer(pb.tobytes(), "<u4")
+    assert a[3] == 0b1011011 << 8 and a[1] == 0
+    assert a[0] == 0x80 << 16 and a[2] == 0x80 << 16  # bits 0 and 2 of element 30 (lane 2 of words 0 and 2)
     cc = np.frombuffer(pc.tobytes(), "<u4")
-    # bits 0..3 = 0b1011 -> plane A word 1 (q // 2), byte 1, high half (q odd)
-    assert a[1] == 0b1011 << (8 * 1 + 4)
-    assert a[0] == a[2] == a[3] == 0
-    # bits 4..5 = 0b01 -> plane B word 0, bit 8*1 + 2*3
-    assert b[0] == 0b01 << (8 + 6) and b[1] == 0
-    # bit 6 = 1 -> plane C bit 8*1 + 3
-    assert cc[0] == 1 << 11
-    # two groups for 40 elements; the second group's words follow the first
-    assert pa.size == 32 and pb.size == 16 and pc.size == 8
-    assert a[4] == 1 << (8 + 4) and a[5] == a[6] == a[7] == 0
-    assert b[2] == 0 and b[3] == 0 and cc[1] == 1 << (8 + 1)
-    back = O.unpack_k15_planes(pa, pb, pc, 40)
+    assert cc[0] == 0x80 << 16  # bit 6 of element 30: byte 26 = plane C byte 2
+    back = O.unpack_k15_planes(pa, pb, pc, 64)
     assert np.array_equal(back, m)
 
 
