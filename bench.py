@@ -1,22 +1,24 @@
 """Benchmark of the lossless BF16 weight-coding hot path on one GB300 (or N replicas).
 
-One step = one pass of the whole hot path over the dense-layer workload
-(4 x 4096x4096 and 3 x 4096x11008 BF16 weights, N(0, 0.02) with 0.1%
-N(0, 0.5) outliers), in both schemes (byte-split and K15):
+Workload: the checkpoint-shaped set (1,923 BF16 tensors, 120 GiB; hidden 6144,
+vocabulary 151552) and its 16384x53248 GEMV.  One step is one pass of the
+whole hot path over one HBM-sized batch of that set:
 
-  1. encode every tensor (histogram, top-15 table, pack, tile scan, escape
-     compaction, row index)
-  2. decode all 14 containers to exact BF16 in one batched launch
-  3. fused decode-GEMV over all 14 containers at batch 1 and batch 4
-  4. plain BF16 GEMV over the 7 raw tensors at batch 1 and batch 4 (one
-     batched launch each, the same launch structure as the fused GEMV)
+  1. encode the batch's 208 tensors (16 GiB of BF16, both embeddings and the
+     first layers) in both schemes: histogram, top-15 table, pack, tile scan,
+     escape compaction, row index
+  2. decode all 416 containers to exact BF16 (batched launches)
+  3. fused decode-GEMV on the 16384x53248 weight (byte-split and K15
+     containers, encoded once before timing) at batch 1, 4, 8 and 16
+  4. plain BF16 GEMV on the same weight at the same batches
 
 `value` is the step's algorithmic HBM bytes (the minimum each launch must
-move, see `bytes_*` below) divided by the device time of the step, in GB/s.
-Per-row rates, the fused / plain GEMV time ratio and the roofline of the
-dominant kernel are reported beside it.  Inputs (386 MB of BF16 weights plus
-~580 MB of containers) are larger than the 129 MB L2 and are swept in order,
-so successive launches do not find their inputs in L2.
+move, see `*_bytes` below) divided by the device time of the step, in GB/s.
+Each row is also reported as decoded GB/s (2n / t, BF16 produced or
+consumed) and compressed-read GB/s (container bytes read / t), with the
+fused / plain GEMV time ratio per batch.  Inputs (17 GB of BF16 plus ~24 GB of
+containers) are far larger than the 129 MB L2 and are swept in order, so no
+launch finds its inputs in L2.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun every rank runs the same workload on its own GPU (replicas,
@@ -37,10 +39,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused decode-GEMV & decode HBM GB/s (% of GB300 peak); GEMV time vs plain BF16"
-WORKLOAD = "dense_layers"
-BATCHES = (1, 4)
+BATCHES = (1, 4, 8, 16)
+BATCH_BYTES = 16 << 30
 SCHEME_NAMES = {0: "bytesplit", 1: "k15"}
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
 
 # ---------------------------------------------------------------------------
 # Algorithmic bytes per launch (the minimum traffic each operation implies).
@@ -163,20 +166,30 @@ def measured_peaks() -> dict:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on a bounded sample of the workload.
 # ---------------------------------------------------------------------------
-CPU_SAMPLE = "one 4096x4096 tensor of the dense-layer workload: encode, decode, GEMV B=1,4, plain GEMV B=1,4, both schemes"
+CPU_SAMPLE = ("per process: one 2048x6144 tensor of the batch (each process its own): encode, decode, fused "
+              "GEMV B=1,4,8,16 and plain GEMV B=1,4,8,16, both schemes")
 
 
-def oracle_sample_run() -> dict:
-    """Runs in a child process with BLAS limited to one thread."""
+def _sample_spec(i: int):
+    from decode_gemv_sign_gb300 import synth
+
+    # the batch's 2048x6144 tensors, taken in turn
+    sq = [s for s in synth.checkpoint_batch(0, BATCH_BYTES) if (s.N, s.K) == (2048, 6144)]
+    return sq[i % len(sq)]
+
+
+def oracle_sample(i: int) -> dict:
+    """One bounded sample of the workload through the oracle (runs in a worker
+    process with BLAS limited to one thread)."""
     import numpy as np
 
     from decode_gemv_sign_gb300 import synth
     from oracle import wcomp_oracle as O
 
-    spec = synth.workload_dense_layers()[0]
+    spec = _sample_spec(i)
     w = synth.gen_weights_np(spec)
     xs = {B: synth.gen_x_np(B, spec.K, 77 + B) for B in BATCHES}
-    total_bytes = 0
+    total = 0
     t0 = time.perf_counter()
     for scheme in (0, 1):
         c = O.encode(w, scheme)
@@ -186,35 +199,67 @@ def oracle_sample_run() -> dict:
         sizes = dict(O.section_sizes(scheme, c.N, c.K, c.E))
         info["bytes_codes"] = O._pad(sizes["codes"])
         info["bytes_raw"] = sum(O._pad(sizes[k]) for k in ("raw", "plane_a", "plane_b", "plane_c") if k in sizes)
-        total_bytes += encode_bytes(info)
+        total += encode_bytes(info)
         d = O.decode(O.deserialize(buf))
         assert np.array_equal(d, w)
-        total_bytes += decode_bytes(info)
+        total += decode_bytes(info)
         for B in BATCHES:
             O.gemv_container(c, xs[B])
-            total_bytes += gemv_bytes(info, B)
+            total += gemv_bytes(info, B)
     for B in BATCHES:
         O.gemv(w, xs[B])
-        total_bytes += plain_bytes(spec.N, spec.K, B)
-    dt = time.perf_counter() - t0
-    return {"bytes": total_bytes, "seconds": dt}
+        total += plain_bytes(spec.N, spec.K, B)
+    return {"bytes": total, "seconds": time.perf_counter() - t0}
 
 
-def cpu_baseline(repeats: int = 1) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    tot_b, tot_s = 0.0, 0.0
-    for _ in range(repeats):
-        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample"], env=env,
-                           capture_output=True, text=True, timeout=900)
-        if r.returncode != 0:
-            return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": CPU_SAMPLE,
-                    "error": r.stderr.strip().splitlines()[-1:] or ["failed"]}
-        d = json.loads(r.stdout.strip().splitlines()[-1])
-        tot_b += d["bytes"]
-        tot_s += d["seconds"]
-    return {"value": tot_b / tot_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{repeats} x " + CPU_SAMPLE, "seconds": round(tot_s, 2)}
+def _pool_init():
+    os.environ["CUDA_VISIBLE_DEVICES"] = ""
+
+
+class OraclePool:
+    """Worker processes (spawned, one BLAS thread each) that run oracle samples."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs, initializer=_pool_init)
+
+    def run(self, first: int) -> dict:
+        """One sample per process, all at once; bytes over wall time."""
+        t0 = time.perf_counter()
+        res = self.pool.map(oracle_sample, range(first, first + self.procs))
+        wall = time.perf_counter() - t0
+        return {"bytes": sum(r["bytes"] for r in res), "seconds": wall,
+                "busy_seconds": sum(r["seconds"] for r in res)}
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline() -> dict:
+    """The oracle on one core and on every host core (one process per core)."""
+    one = OraclePool(1)
+    r1 = one.run(0)
+    one.close()
+    cores = host_cores()
+    allp = OraclePool(cores)
+    ra = allp.run(0)
+    allp.close()
+    return {"value": round(ra["bytes"] / ra["seconds"] / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes at once, " + CPU_SAMPLE, "seconds": round(ra["seconds"], 2),
+            "single_core": {"value": round(r1["bytes"] / r1["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+                            "sample": "1 process, " + CPU_SAMPLE, "seconds": round(r1["seconds"], 2)}}
 
 
 # ---------------------------------------------------------------------------
@@ -269,25 +314,55 @@ def aggregate_rate(dist, local_bytes: float, local_ms: float) -> tuple:
 # ---------------------------------------------------------------------------
 # The GPU arm.
 # ---------------------------------------------------------------------------
-class HotPath:
-    def __init__(self, W, weights, specs, xs, stream):
-        import torch
+def workload_config(batch_specs, gemv_spec, world: int) -> dict:
+    """The `config` of both arms' lines: the workload a step covers."""
+    return {"workload": (f"checkpoint-shaped set (1,923 BF16 tensors, 120 GiB), one HBM-sized batch of "
+                         f"{len(batch_specs)} tensors (the first 16 GiB: both 151552x6144 embeddings and the first "
+                         f"layers), both schemes: encode + batched decode; GEMV {gemv_spec.N}x{gemv_spec.K} "
+                         f"fused (byte-split, K15) and plain BF16 at B=1,4,8,16"),
+            "tensors": len(batch_specs), "elements": int(sum(s.n for s in batch_specs)),
+            "gemv": [gemv_spec.N, gemv_spec.K], "batches": list(BATCHES),
+            "l2": "inputs far larger than L2 (17 GB BF16 batch, ~24 GB containers, 1.7 GB GEMV weight), swept in order",
+            "parallelism": f"replicas x{world}"}
 
+
+def alloc_batch(specs, dev):
+    """One flat device buffer holding the batch's tensors back to back (16-byte aligned views)."""
+    import torch
+
+    offs, total = [], 0
+    for s in specs:
+        offs.append(total)
+        total += (s.n + 7) // 8 * 8
+    flat = torch.empty(total, dtype=torch.int16, device=dev)
+    views = [flat[o:o + s.n].view(s.N, s.K) for o, s in zip(offs, specs)]
+    return flat, views
+
+
+class HotPath:
+    """The step's device state: batch sources, decode outputs, GEMV inputs and outputs."""
+
+    def __init__(self, W, torch, src_views, specs, gemv_w, gemv_cs, xs, stream):
         self.W = W
         self.torch = torch
-        self.weights = weights
+        self.src = src_views
         self.specs = specs
-        self.xs = xs  # {B: [x per tensor]}
+        self.gemv_w = gemv_w
+        self.gemv_cs = gemv_cs
+        self.xs = xs
         self.stream = stream
-        self.outs = [torch.empty((s.N, s.K), dtype=torch.int16, device="cuda") for s in specs for _ in (0, 1)]
-        self.ys = {B: [torch.empty((B, s.N), dtype=torch.float32, device="cuda") for s in specs for _ in (0, 1)]
-                   for B in BATCHES}
-        self.yp = {B: [torch.empty((B, s.N), dtype=torch.float32, device="cuda") for s in specs] for B in BATCHES}
+        dev = gemv_w.device
+        self.out_flat, self.outs0 = alloc_batch(specs, dev)
+        self.out_flat1, self.outs1 = alloc_batch(specs, dev)
+        self.outs = [o for pair in zip(self.outs0, self.outs1) for o in pair]
+        N = gemv_w.shape[0]
+        self.yf = {(s, B): torch.empty((B, N), dtype=torch.float32, device=dev) for s in (0, 1) for B in BATCHES}
+        self.yp = {B: torch.empty((B, N), dtype=torch.float32, device=dev) for B in BATCHES}
         self.containers = []
         self.infos = None
 
-    def step(self, ev=None):
-        """One pass of the hot path; `ev` (list) receives (name, start, end) events."""
+    def step(self, marks=None):
+        """One pass of the hot path; `marks` (list) receives (name, start event, end event)."""
         W, torch = self.W, self.torch
 
         def mark():
@@ -297,51 +372,48 @@ class HotPath:
 
         for c in self.containers:
             c.free(self.stream)
-        t0 = mark() if ev is not None else None
-        cs = W.encode_batched([w for w in self.weights for _ in (0, 1)], [0, 1] * len(self.weights),
-                              stream=self.stream)
+        prev = mark() if marks is not None else None
+        cs = W.encode_batched([w for w in self.src for _ in (0, 1)], [0, 1] * len(self.src), stream=self.stream)
         self.containers = cs
-        t1 = mark() if ev is not None else None
+        if marks is not None:
+            e = mark()
+            marks.append(("encode", prev, e))
+            prev = e
         W.decode_batched(cs, self.outs, stream=self.stream)
-        t2 = mark() if ev is not None else None
-        marks = [("encode", t0, t1), ("decode", t1, t2)]
-        prev = t2
-        for B in BATCHES:
-            xs2 = [x for x in self.xs[B] for _ in (0, 1)]
-            W.gemv_batched(cs, xs2, self.ys[B], stream=self.stream)
-            e = mark() if ev is not None else None
-            marks.append((f"gemv_fused_b{B}", prev, e))
+        if marks is not None:
+            e = mark()
+            marks.append(("decode", prev, e))
             prev = e
         for B in BATCHES:
-            W.gemv_bf16_batched(self.weights, self.xs[B], self.yp[B], stream=self.stream)
-            e = mark() if ev is not None else None
-            marks.append((f"gemv_plain_b{B}", prev, e))
-            prev = e
-        if ev is not None:
-            ev.append(marks)
+            for s in (0, 1):
+                W.gemv(self.gemv_cs[s], self.xs[B], self.yf[(s, B)], stream=self.stream)
+                if marks is not None:
+                    e = mark()
+                    marks.append((f"gemv_fused_{SCHEME_NAMES[s]}_b{B}", prev, e))
+                    prev = e
+            W.gemv_bf16(self.gemv_w, self.xs[B], self.yp[B], stream=self.stream)
+            if marks is not None:
+                e = mark()
+                marks.append((f"gemv_plain_b{B}", prev, e))
+                prev = e
         if self.infos is None:
             self.infos = [c.info() for c in cs]
 
-    def algorithmic_bytes(self) -> dict:
-        out = {"encode": 0, "decode": 0}
+    def row_bytes(self) -> dict:
+        """Algorithmic bytes of every row of the step, with the bytes of
+        BF16 produced / consumed and the container bytes read."""
+        out = {"encode": {"bytes": sum(encode_bytes(i) for i in self.infos), "bf16": sum(2 * i["n"] for i in self.infos),
+                          "compressed": sum(i["serialized_bytes"] - 96 for i in self.infos)},
+               "decode": {"bytes": sum(decode_bytes(i) for i in self.infos), "bf16": sum(2 * i["n"] for i in self.infos),
+                          "compressed": sum(container_read_bytes(i, "decode") for i in self.infos)}}
+        gi = {s: self.gemv_cs[s].info() for s in (0, 1)}
+        N, K = self.gemv_w.shape
         for B in BATCHES:
-            out[f"gemv_fused_b{B}"] = 0
-            out[f"gemv_plain_b{B}"] = 0
-        for inf in self.infos:
-            out["encode"] += encode_bytes(inf)
-            out["decode"] += decode_bytes(inf)
-            for B in BATCHES:
-                out[f"gemv_fused_b{B}"] += gemv_bytes(inf, B)
-        for s in self.specs:
-            for B in BATCHES:
-                out[f"gemv_plain_b{B}"] += plain_bytes(s.N, s.K, B)
+            for s in (0, 1):
+                out[f"gemv_fused_{SCHEME_NAMES[s]}_b{B}"] = {"bytes": gemv_bytes(gi[s], B), "bf16": 2 * N * K,
+                                                             "compressed": container_read_bytes(gi[s], "gemv")}
+            out[f"gemv_plain_b{B}"] = {"bytes": plain_bytes(N, K, B), "bf16": 2 * N * K, "compressed": 2 * N * K}
         return out
-
-    def per_scheme_bytes(self, B: int) -> dict:
-        d = {0: 0, 1: 0}
-        for inf in self.infos:
-            d[inf["scheme"]] += gemv_bytes(inf, B)
-        return d
 
 
 def time_launches(fn, stream, reps: int = 10) -> float:
@@ -362,28 +434,18 @@ def time_launches(fn, stream, reps: int = 10) -> float:
     return a.elapsed_time(b) / reps
 
 
-def time_kernels(hp, W, torch) -> dict:
-    """Per-launch device time of each kernel kind of the step (ms)."""
-    res = {}
-    # the step's decode launch: all containers of both schemes in one batch
-    res["decode_all"] = time_launches(lambda: W.decode_batched(hp.containers, hp.outs, stream=hp.stream), hp.stream)
-    by = {s: [c for c in hp.containers if c.scheme == s] for s in (0, 1)}
-    outs = {s: [o for o, c in zip(hp.outs, hp.containers) if c.scheme == s] for s in (0, 1)}
-    for s in (0, 1):
-        nm = SCHEME_NAMES[s]
-        res[f"decode_{nm}"] = time_launches(lambda: W.decode_batched(by[s], outs[s], stream=hp.stream), hp.stream)
-        for B in BATCHES:
-            ys = [torch.empty((B, c.N), dtype=torch.float32, device="cuda") for c in by[s]]
-            res[f"gemv_fused_{nm}_b{B}"] = time_launches(
-                lambda: W.gemv_batched(by[s], hp.xs[B], ys, stream=hp.stream), hp.stream)
-    for B in BATCHES:
-        res[f"gemv_plain_b{B}"] = time_launches(
-            lambda: W.gemv_bf16_batched(hp.weights, hp.xs[B], hp.yp[B], stream=hp.stream), hp.stream)
-    return res
+def make_gemv(W, torch, dev):
+    """The 16384x53248 GEMV weight, its containers and x per batch size."""
+    from decode_gemv_sign_gb300 import synth
+
+    spec = synth.checkpoint_gemv_spec()
+    w = synth.gen_weights_torch(spec, dev)
+    cs = {s: W.encode(w, s) for s in (0, 1)}
+    xs = {B: synth.gen_x_torch(B, spec.K, 9000 + B, dev) for B in BATCHES}
+    return spec, w, cs, xs
 
 
 def run_ours(args):
-    import numpy as np
     import torch
 
     from decode_gemv_sign_gb300 import build, synth
@@ -394,20 +456,24 @@ def run_ours(args):
     dist = init_dist(world)
     build.build()
     W.lib()
-    specs = synth.WORKLOADS[WORKLOAD]()
     dev = torch.device("cuda", local)
-    weights = [synth.gen_weights_torch(s, dev) for s in specs]
-    xs = {B: [synth.gen_x_torch(B, s.K, 9000 + 10 * B + i, dev) for i, s in enumerate(specs)] for B in BATCHES}
+    specs = synth.checkpoint_batch(0, BATCH_BYTES)
+    src_flat, src = alloc_batch(specs, dev)
+    for s, v in zip(specs, src):
+        v.copy_(synth.gen_weights_torch(s, dev))
+    gspec, gw, gcs, xs = make_gemv(W, torch, dev)
     stream = torch.cuda.current_stream()
-    hp = HotPath(W, weights, specs, xs, stream)
+    hp = HotPath(W, torch, src, specs, gw, gcs, xs, stream)
     for _ in range(args.warmup):
         hp.step()
     torch.cuda.synchronize()
+    # every decode of the warm-up steps was bit-exact
+    exact = all(bool(torch.equal(a, w) and torch.equal(b, w)) for a, b, w in zip(hp.outs0, hp.outs1, src))
 
     # ---- timed region: K steps, device time, clocks sampled meanwhile
     clocks = ClockSampler(local)
     clocks.start()
-    ev = []
+    marks = []
     barrier(dist)
     torch.cuda.synchronize()
     clocks.mark_start()
@@ -416,7 +482,7 @@ def run_ours(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(args.steps):
-        hp.step(ev)
+        hp.step(marks)
     end.record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
@@ -424,118 +490,145 @@ def run_ours(args):
     launches = W.launch_count() - n0
     clk = clocks.stop()
     t_ms = start.elapsed_time(end)
+    dev_check = W.lib().wcomp_device_check(None)
 
     phase_ms = {}
-    for marks in ev:
-        for name, a, b in marks:
-            phase_ms[name] = phase_ms.get(name, 0.0) + a.elapsed_time(b)
+    for name, a, b in marks:
+        phase_ms[name] = phase_ms.get(name, 0.0) + a.elapsed_time(b)
     phase_ms = {k: v / args.steps for k, v in phase_ms.items()}
-    bytes_ = hp.algorithmic_bytes()
-    step_bytes = sum(bytes_.values())
+    rb = hp.row_bytes()
+    step_bytes = sum(r["bytes"] for r in rb.values())
     value, t_ms_max = aggregate_rate(dist, step_bytes * args.steps, t_ms)
-
-    # ---- end to end through the public API with host buffers
-    e2e = run_e2e(args, W, torch, hp, specs, dist)
 
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"]
-    rows = {}
-    for k, ms in phase_ms.items():
-        gbs = bytes_[k] / (ms / 1e3) / 1e9
-        rows[k] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                   "frac_of_8TBps": round(gbs / 8000.0, 4), "bytes": bytes_[k]}
-    # per-launch kernel times (back-to-back launches, device clock)
-    kt = time_kernels(hp, W, torch)
-    kbytes = {"decode_all": sum(decode_bytes(i) for i in hp.infos)}
-    for s_ in (0, 1):
-        nm = SCHEME_NAMES[s_]
-        infos = [i for i in hp.infos if i["scheme"] == s_]
-        kbytes[f"decode_{nm}"] = sum(decode_bytes(i) for i in infos)
-        for B in BATCHES:
-            kbytes[f"gemv_fused_{nm}_b{B}"] = sum(gemv_bytes(i, B) for i in infos)
-    for B in BATCHES:
-        kbytes[f"gemv_plain_b{B}"] = sum(plain_bytes(sp.N, sp.K, B) for sp in specs)
-    kernels = {k: {"ms": round(v, 4), "GB/s": round(kbytes[k] / (v / 1e3) / 1e9, 1),
-                   "frac_of_peak": round(kbytes[k] / (v / 1e3) / 1e9 / peak, 4), "bytes": kbytes[k]}
-               for k, v in kt.items()}
-    ratio = {}
-    for B in BATCHES:
-        ratio[f"b{B}"] = {SCHEME_NAMES[s_]: round(kt[f"gemv_fused_{SCHEME_NAMES[s_]}_b{B}"] / kt[f"gemv_plain_b{B}"], 4)
-                          for s_ in (0, 1)}
-    # Dominant kernel: the single launch with the largest device time in the step
-    # (the batched decode of all 14 containers; the launch list in profiles/
-    # confirms it has the largest share of the library's GPU time).
-    dom = "decode_all"
-    dom_gbs = kbytes[dom] / (kt[dom] / 1e3) / 1e9
-    traffic = load_traffic("decode_kernel_both")
-    roofline = {"kernel": "decode_kernel (batched, 7 tensors x 2 schemes)", "bound": "hbm", "achieved": round(dom_gbs, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                "peak_source": peaks["source"] + " (hbm_gbs: read+write copy)",
-                "algorithmic_bytes_per_launch": kbytes[dom], "launch_ms": round(kt[dom], 4),
-                "traffic": traffic}
 
+    def rates(name, ms):
+        r = rb[name]
+        gbs = r["bytes"] / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                "frac_of_8TBps": round(gbs / NOMINAL_HBM_GBS, 4), "bytes": r["bytes"],
+                "decoded_GB/s": round(r["bf16"] / (ms / 1e3) / 1e9, 1),
+                "compressed_read_GB/s": round(r["compressed"] / (ms / 1e3) / 1e9, 1)}
+
+    rows = {k: rates(k, ms) for k, ms in phase_ms.items()}
+    # per-launch times (back-to-back calls of each operation, device clock)
+    kt = {"decode_batch": time_launches(lambda: W.decode_batched(hp.containers, hp.outs, stream=stream), stream, 5)}
+    for B in BATCHES:
+        for s in (0, 1):
+            kt[f"gemv_fused_{SCHEME_NAMES[s]}_b{B}"] = time_launches(
+                lambda: W.gemv(gcs[s], xs[B], hp.yf[(s, B)], stream=stream), stream)
+        kt[f"gemv_plain_b{B}"] = time_launches(lambda: W.gemv_bf16(gw, xs[B], hp.yp[B], stream=stream), stream)
+    rb["decode_batch"] = rb["decode"]
+    kernels = {k: rates(k, ms) for k, ms in kt.items()}
+    ratio = {f"b{B}": {SCHEME_NAMES[s]: round(kt[f"gemv_fused_{SCHEME_NAMES[s]}_b{B}"] / kt[f"gemv_plain_b{B}"], 4)
+                       for s in (0, 1)} for B in BATCHES}
+    # the dense 12-bit ablation: the same GEMV on an escape-free weight (byte-split E = 0)
+    ablation = dense12_rows(W, torch, dev, stream, peak)
+
+    # Dominant kernel: decode_kernel, the step's largest share of library GPU
+    # time (launch list in profiles/); its launches in the batched decode
+    # call carry the batch's 416 containers.
+    dom_ms = kt["decode_batch"]
+    dom_gbs = rb["decode"]["bytes"] / (dom_ms / 1e3) / 1e9
+    roofline = {"kernel": "decode_kernel (batched decode of the batch's 416 containers)", "bound": "hbm",
+                "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                "frac_of_8TBps": round(dom_gbs / NOMINAL_HBM_GBS, 4),
+                "peak_source": peaks["source"] + " (hbm_gbs: read+write copy)",
+                "algorithmic_bytes_per_call": rb["decode"]["bytes"], "call_ms": round(dom_ms, 4),
+                "traffic": load_traffic("decode_kernel_checkpoint_batch", rb["decode"]["bytes"])}
+
+    infos = hp.infos
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u16 codec / fp32 GEMV accumulate",
-        "data": "synthetic (seeded N(0,0.02) BF16 weights with 0.1% N(0,0.5) outliers, x ~ N(0,1) BF16)",
-        "config": workload_config(specs, world),
+        "data": "synthetic (seeded checkpoint-shaped BF16 tensors: Normal / Student-t(4), sigma ~ U(0.005, 0.05), "
+                "0.1% outliers; x ~ N(0,1) BF16)",
+        "config": workload_config(specs, gspec, world),
         "rows": rows,
         "kernels": kernels,
         "fused_over_plain_time": ratio,
-        "escape_rate": {SCHEME_NAMES[s]: round(sum(i["n_escapes"] for i in hp.infos if i["scheme"] == s) /
-                                               sum(i["n"] for i in hp.infos if i["scheme"] == s), 6) for s in (0, 1)},
-        "bpw": {SCHEME_NAMES[s]: {"entropy": round(sum(i["entropy_bpw"] * i["n"] for i in hp.infos if i["scheme"] == s) /
-                                                   sum(i["n"] for i in hp.infos if i["scheme"] == s), 4),
-                                  "physical": round(sum(8 * i["serialized_bytes"] for i in hp.infos if i["scheme"] == s) /
-                                                    sum(i["n"] for i in hp.infos if i["scheme"] == s), 4),
+        "dense12_ablation": ablation,
+        "decode_exact": exact,
+        "device_check": dev_check,
+        "escape_rate": {SCHEME_NAMES[s]: round(sum(i["n_escapes"] for i in infos if i["scheme"] == s) /
+                                               sum(i["n"] for i in infos if i["scheme"] == s), 6) for s in (0, 1)},
+        "gemv_escape_rate": {SCHEME_NAMES[s]: round(gcs[s].info()["n_escapes"] / gcs[s].info()["n"], 6)
+                             for s in (0, 1)},
+        "bpw": {SCHEME_NAMES[s]: {"entropy": round(sum(i["entropy_bpw"] * i["n"] for i in infos if i["scheme"] == s) /
+                                                   sum(i["n"] for i in infos if i["scheme"] == s), 4),
+                                  "physical": round(sum(8 * i["serialized_bytes"] for i in infos if i["scheme"] == s) /
+                                                    sum(i["n"] for i in infos if i["scheme"] == s), 4),
                                   "physical_compact": round(
-                                      sum(8 * i["serialized_compact_bytes"] for i in hp.infos if i["scheme"] == s) /
-                                      sum(i["n"] for i in hp.infos if i["scheme"] == s), 4)}
+                                      sum(8 * i["serialized_compact_bytes"] for i in infos if i["scheme"] == s) /
+                                      sum(i["n"] for i in infos if i["scheme"] == s), 4)}
                 for s in (0, 1)},
         "roofline": roofline,
         "clocks": clk,
         "gpu_launches": int(launches),
-        "e2e": e2e,
     }
+    # ---- end to end through the public API with host buffers
+    result["e2e"] = run_e2e(args, W, torch, hp, specs, src_flat, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(repeats=2)
+        result["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def run_e2e(args, W, torch, hp, specs, dist):
-    """Same hot path through the public API, inputs copied from pinned host memory each step
-    and every GEMV result read back to the host.  Two device input sets alternate: step k+1's
-    weights and x are copied on a second stream while step k computes (the copy of step 0
-    and every later one lies inside the timed region)."""
-    host_w = [w.cpu().pin_memory() for w in hp.weights]
-    host_x = {B: [x.cpu().pin_memory() for x in hp.xs[B]] for B in BATCHES}
-    host_y = {B: [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in hp.ys[B]] for B in BATCHES}
-    host_yp = {B: [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in hp.yp[B]] for B in BATCHES}
-    h2d = sum(w.numel() * 2 for w in host_w) + sum(x.numel() * 2 for B in BATCHES for x in host_x[B])
-    d2h = sum(y.numel() * 4 for B in BATCHES for y in host_y[B]) + sum(
-        y.numel() * 4 for B in BATCHES for y in host_yp[B])
-    sets = []
-    for _ in range(2):
-        dev_w = [torch.empty_like(w) for w in hp.weights]
-        dev_x = {B: [torch.empty_like(x) for x in hp.xs[B]] for B in BATCHES}
-        sets.append((dev_w, dev_x, HotPath(W, dev_w, specs, dev_x, hp.stream)))
+def dense12_rows(W, torch, dev, stream, peak) -> dict:
+    """Fused byte-split GEMV on an escape-free 16384x53248 weight (every high
+    byte in the table, so the kernel reads exactly 12 bits per weight and
+    corrects nothing) beside the plain GEMV, at B = 1 and 4."""
+    from decode_gemv_sign_gb300 import synth
+
+    spec = synth.dense12_spec()
+    w = synth.gen_weights_torch(spec, dev)
+    c = W.encode(w, 0)
+    inf = c.info()
+    out = {"weight": [spec.N, spec.K], "escapes": inf["n_escapes"]}
+    for B in (1, 4):
+        x = synth.gen_x_torch(B, spec.K, 9100 + B, dev)
+        y = torch.empty((B, spec.N), dtype=torch.float32, device=dev)
+        tf = time_launches(lambda: W.gemv(c, x, y, stream=stream), stream)
+        tp = time_launches(lambda: W.gemv_bf16(w, x, y, stream=stream), stream)
+        gbs = gemv_bytes(inf, B) / (tf / 1e3) / 1e9
+        out[f"b{B}"] = {"fused_ms": round(tf, 4), "plain_ms": round(tp, 4), "fused_over_plain": round(tf / tp, 4),
+                        "fused_GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    c.free(stream)
+    del w
+    return out
+
+
+def run_e2e(args, W, torch, hp, specs, src_flat, dist):
+    """The same step through the public API, its inputs copied from pinned host
+    memory every step (the batch's 16 GiB of BF16 and every x) and every GEMV
+    result read back.  Two device copies of the batch alternate, so step k+1's
+    inputs are copied on a second stream while step k computes (the copy of
+    the first timed step lies inside the timed region too)."""
+    host_src = torch.empty(src_flat.shape, dtype=src_flat.dtype).pin_memory()
+    host_src.copy_(src_flat)
+    host_x = {B: hp.xs[B].cpu().pin_memory() for B in BATCHES}
+    host_y = {k: torch.empty(y.shape, dtype=y.dtype).pin_memory() for k, y in hp.yf.items()}
+    host_yp = {B: torch.empty(y.shape, dtype=y.dtype).pin_memory() for B, y in hp.yp.items()}
+    h2d = host_src.numel() * 2 + sum(x.numel() * 2 for x in host_x.values())
+    d2h = sum(y.numel() * 4 for y in host_y.values()) + sum(y.numel() * 4 for y in host_yp.values())
+    sets = [(src_flat, hp.src, hp.xs)]
+    flat2, views2 = alloc_batch(specs, src_flat.device)
+    sets.append((flat2, views2, {B: torch.empty_like(hp.xs[B]) for B in BATCHES}))
     copy_stream = torch.cuda.Stream()
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
 
     def copy_in(i):
-        dev_w, dev_x, _ = sets[i]
+        flat, _, xs = sets[i]
         copy_stream.wait_event(done[i])  # the set's previous step has finished with it
         with torch.cuda.stream(copy_stream):
-            for d, h in zip(dev_w, host_w):
-                d.copy_(h, non_blocking=True)
+            flat.copy_(host_src, non_blocking=True)
             for B in BATCHES:
-                for d, h in zip(dev_x[B], host_x[B]):
-                    d.copy_(h, non_blocking=True)
+                xs[B].copy_(host_x[B], non_blocking=True)
         ready[i].record(copy_stream)
 
     def run(steps):
@@ -547,13 +640,12 @@ def run_e2e(args, W, torch, hp, specs, dist):
             if k + 1 < steps:
                 copy_in(1 - i)
             hp.stream.wait_event(ready[i])
-            e2e_hp = sets[i][2]
-            e2e_hp.step()
-            for B in BATCHES:
-                for h, d in zip(host_y[B], e2e_hp.ys[B]):
-                    h.copy_(d, non_blocking=True)
-                for h, d in zip(host_yp[B], e2e_hp.yp[B]):
-                    h.copy_(d, non_blocking=True)
+            hp.src, hp.xs = sets[i][1], sets[i][2]
+            hp.step()
+            for key, h in host_y.items():
+                h.copy_(hp.yf[key], non_blocking=True)
+            for B, h in host_yp.items():
+                h.copy_(hp.yp[B], non_blocking=True)
             done[i].record(hp.stream)
 
     run(max(2, args.warmup))
@@ -567,12 +659,11 @@ def run_e2e(args, W, torch, hp, specs, dist):
     b.record(hp.stream)
     torch.cuda.synchronize()
     barrier(dist)
+    hp.src, hp.xs = sets[0][1], sets[0][2]
     ms = allmax(dist, a.elapsed_time(b))
-    for _, _, e2e_hp in sets:
-        for c in e2e_hp.containers:
-            c.free(hp.stream)
-    step_bytes = sum(hp.algorithmic_bytes().values())
+    step_bytes = sum(r["bytes"] for r in hp.row_bytes().values())
     v = allsum(dist, step_bytes * args.steps) / (ms / 1e3) / 1e9
+    del flat2, views2
     return {"value": round(v, 1), "unit": "GB/s", "ms_per_step": round(ms / args.steps, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "step k+1's inputs are copied on a second stream while step k computes"}
@@ -588,10 +679,13 @@ def _source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(key: str):
-    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when
-    the summary has no such line or the kernel's sources changed since the capture."""
-    p = os.path.join(ROOT, "profiles", "traffic_dense_layers.md")
+def load_traffic(key: str, algorithmic_bytes: int):
+    """DRAM bytes (read + write) per call from the committed ncu summary, or None
+    when the summary has no such line or the kernel's sources changed since the
+    capture.  The summary stores DRAM bytes per algorithmic byte of a smaller
+    capture of the same kernel; the call's traffic is that ratio times its
+    algorithmic bytes."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
     for line in open(p):
@@ -600,17 +694,8 @@ def load_traffic(key: str):
             files, digest = parts[3].split("=")
             if _source_digest(files.split("+")) != digest:
                 return None
-            return int(parts[2])
+            return int(round(float(parts[2]) * algorithmic_bytes))
     return None
-
-
-def workload_config(specs, world: int) -> dict:
-    """The `config` of both arms' lines: the workload a step covers."""
-    return {"workload": "dense layer set: 4 x 4096x4096 + 3 x 4096x11008 BF16, both schemes, "
-                        "encode + batched decode + fused GEMV B=1,4 + plain GEMV B=1,4",
-            "tensors": len(specs), "elements": int(sum(s.n for s in specs)), "batches": list(BATCHES),
-            "l2": "inputs larger than L2 (386 MB BF16, ~580 MB containers), swept in order",
-            "parallelism": f"replicas x{world}"}
 
 
 # ---------------------------------------------------------------------------
@@ -621,28 +706,32 @@ def run_reference(args):
     if rank != 0:
         return
     from decode_gemv_sign_gb300 import synth
-    vals = []
-    for _ in range(args.warmup):
-        cpu_baseline()
-    t_total, b_total = 0.0, 0.0
-    last = None
-    for _ in range(args.steps):
-        last = cpu_baseline()
-        if last["value"] is None:
-            print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " + str(last.get("error"))}))
-            return
-        t_total += last["seconds"]
-        b_total += last["value"] * last["seconds"] * 1e9
-        vals.append(last["value"])
+
+    cores = host_cores()
+    pool = OraclePool(cores)
+    try:
+        for i in range(args.warmup):
+            pool.run(cores * i)
+        t_total, b_total = 0.0, 0.0
+        for i in range(args.steps):
+            r = pool.run(cores * (args.warmup + i))
+            t_total += r["seconds"]
+            b_total += r["bytes"]
+    except Exception as e:  # a failing oracle run is reported, not hidden
+        print(json.dumps({"impl": "reference", "unavailable": f"oracle run failed: {e}"}))
+        return
+    finally:
+        pool.close()
     v = b_total / t_total / 1e9
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16 codec / f64 GEMV",
         "data": "synthetic (seeded numpy draw of the same workload recipe)",
-        # the same workload as our arm's line; each step times a bounded sample of it (cpu_baseline)
-        "config": workload_config(synth.workload_dense_layers(), world),
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": CPU_SAMPLE},
+        # the same workload as our arm's line; each step times a bounded sample of it
+        "config": workload_config(synth.checkpoint_batch(0, BATCH_BYTES), synth.checkpoint_gemv_spec(), world),
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {cores} processes at once, " + CPU_SAMPLE},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -651,18 +740,16 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default 200 for ours, so the timed region spans several clock "
-                         "samples; 10 for the reference arm, whose steps take seconds each)")
-    ap.add_argument("--warmup", type=int, default=3)
+                    help="timed steps (default 20 for ours, about half a second of device time; 3 for the "
+                         "reference arm, whose steps take seconds each)")
+    ap.add_argument("--warmup", type=int, default=None, help="untimed steps first (default 3; ours takes at least 3)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    if args.oracle_sample:
-        print(json.dumps(oracle_sample_run()))
-        return
     if args.steps is None:
-        args.steps = 200 if args.impl == "ours" else 10
+        args.steps = 20 if args.impl == "ours" else 3
+    if args.warmup is None:
+        args.warmup = 3 if args.impl == "ours" else 1
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -81,8 +81,11 @@ def gen_weights_np(spec: WeightSpec) -> np.ndarray:
     """Draw ``spec`` with numpy's PCG64; return uint16 BF16 bits of shape [N, K]."""
     rng = np.random.Generator(np.random.PCG64(spec.seed))
     n = spec.n
-    if spec.dist == "normal":
+    if spec.dist in ("normal", "normal_clamped"):
         v = rng.standard_normal(n, dtype=np.float32) * np.float32(spec.sigma)
+        if spec.dist == "normal_clamped":
+            v = np.sign(v + np.float32(1e-30)) * np.clip(np.abs(v), np.float32(2.0**-14), np.float32(2.0**-2 * 0.99))
+            v = v.astype(np.float32)
     elif spec.dist == "t4":
         # Student-t with 4 degrees of freedom has variance 2: scale to std sigma.
         v = rng.standard_t(4, size=n).astype(np.float32) * np.float32(spec.sigma / math.sqrt(2.0))
@@ -114,8 +117,12 @@ def gen_weights_torch(spec: WeightSpec, device):
     g = torch.Generator(device=device)
     g.manual_seed(spec.seed)
     n = spec.n
-    if spec.dist == "normal":
+    if spec.dist in ("normal", "normal_clamped"):
         v = torch.randn(n, generator=g, device=device, dtype=torch.float32) * spec.sigma
+        if spec.dist == "normal_clamped":
+            sgn = torch.where(v < 0, -1.0, 1.0)
+            v = sgn * v.abs().clamp_(2.0**-14, 2.0**-2 * 0.99)
+            del sgn
     elif spec.dist == "t4":
         # t4 = Z / sqrt(chi2_4 / 4); chi2_4 = -2 log(U1 U2).
         z = torch.randn(n, generator=g, device=device, dtype=torch.float32)
@@ -231,9 +238,38 @@ def workload_checkpoint(layers: int = 113) -> List[WeightSpec]:
     return out
 
 
+def batches(specs: Sequence[WeightSpec], batch_bytes: int) -> List[List[WeightSpec]]:
+    """Consecutive groups of specs holding at most ``batch_bytes`` of BF16 each
+    (a tensor larger than the limit forms a group of its own)."""
+    out, cur, size = [], [], 0
+    for s in specs:
+        b = 2 * s.n
+        if cur and size + b > batch_bytes:
+            out.append(cur)
+            cur, size = [], 0
+        cur.append(s)
+        size += b
+    if cur:
+        out.append(cur)
+    return out
+
+
+def checkpoint_batch(index: int = 0, batch_bytes: int = 16 << 30) -> List[WeightSpec]:
+    """Batch ``index`` of the checkpoint-shaped set in HBM-sized groups."""
+    return batches(workload_checkpoint(), batch_bytes)[index]
+
+
 def checkpoint_gemv_spec() -> WeightSpec:
     """The single large GEMV weight of the checkpoint workload: 16384x53248."""
     return WeightSpec("gemv16384x53248", 16384, 53248, "t4", 0.02, 0.001, "normal", 0.1, seed=5999)
+
+
+def dense12_spec(N: int = 16384, K: int = 53248, seed: int = 6000) -> WeightSpec:
+    """Escape-free weights: N(0, 0.02) with every magnitude clamped into
+    [2^-14, 2^-2), so only 14 high bytes occur (sign x exponent bits 7..1 of
+    113..124) and byte-split needs no escape at all: exactly 4 code bits plus 8
+    raw bits per weight, the dense 12-bit form of the pages' GPU prototype."""
+    return WeightSpec("dense12", N, K, "normal_clamped", 0.02, seed=seed)
 
 
 WORKLOADS = {

@@ -30,19 +30,27 @@ def test_reference_arm_line_matches_our_terms():
     assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["ms_per_step"] > 0
-    assert d["config"] == bench.workload_config(synth.workload_dense_layers(), 1)
+    assert d["config"] == bench.workload_config(synth.checkpoint_batch(0, bench.BATCH_BYTES),
+                                                synth.checkpoint_gemv_spec(), 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["vs_baseline"] is None
 
 
-def test_workload_config_counts_the_dense_layer_set():
-    specs = synth.workload_dense_layers()
-    cfg = bench.workload_config(specs, 4)
-    assert cfg["tensors"] == 7
-    assert cfg["elements"] == 4 * 4096 * 4096 + 3 * 4096 * 11008 == 202375168
-    assert cfg["batches"] == [1, 4] and cfg["parallelism"] == "replicas x4"
+def test_workload_config_counts_the_checkpoint_batch():
+    """One step covers the first HBM-sized (16 GiB) batch of the checkpoint-shaped
+    set: both embeddings and the first layers, and the 16384x53248 GEMV."""
+    specs = synth.checkpoint_batch(0, bench.BATCH_BYTES)
+    cfg = bench.workload_config(specs, synth.checkpoint_gemv_spec(), 4)
+    assert cfg["tensors"] == len(specs) == 208
+    assert 2 * cfg["elements"] <= bench.BATCH_BYTES < 2 * cfg["elements"] + 2 * 16384 * 6144
+    assert [(s.N, s.K) for s in specs[:2]] == [(151552, 6144)] * 2
+    assert cfg["gemv"] == [16384, 53248]
+    assert cfg["batches"] == [1, 4, 8, 16] and cfg["parallelism"] == "replicas x4"
+    # the batches of the whole set cover all 1,923 tensors in order
+    groups = synth.batches(synth.workload_checkpoint(), bench.BATCH_BYTES)
+    assert groups[0] == specs and sum(len(g) for g in groups) == 1923
 
 
 def _info(c) -> dict:
