@@ -70,6 +70,7 @@ constexpr int kRows = 16;      // weight rows per unit (the MMA's M side)
 constexpr int kKBlock = 128;   // columns per k-block (4 lanes x 32)
 constexpr int kCtasPerSm = 2;
 constexpr int kEscDepth = 16;  // escape corrections with their loads in flight together
+constexpr int kEscQ = 2;       // escapes a thread moves along per k-block (no transposed x)
 
 enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
@@ -434,7 +435,7 @@ struct SmemAt {
   static constexpr uint32_t kBarOff = kRing;
   static constexpr uint32_t kPartOff = kBarOff + kWarps * ST * 8;
   static constexpr uint32_t kPart = 2 * kWarps * 32 * 4 * NT;                        // floats
-  static constexpr uint32_t kCorr = SRC == kPlain ? 0 : XW > 0 ? 2 * kWarps * 16 * kRows : 2 * kThreads;  // floats
+  static constexpr uint32_t kCorr = SRC == kPlain ? 0 : XW > 0 ? 2 * kRows * 16 : 2 * kThreads;  // floats
   static constexpr uint32_t kCorrOff = kPartOff + 4 * kPart;
   static constexpr uint32_t kLutOff = kCorrOff + 4 * kCorr;
   static constexpr uint32_t kLut = 256 * lut_rep<SRC>();  // words
@@ -502,11 +503,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     build_lut(owner(p.set_prefix, p.count, first_unit));
     __syncthreads();
   }
-  // This thread's share of the escape corrections: row cj of the unit, batch
-  // cb, part cq of cP (cbp batch slots; cP = threads / (16 cbp) parts).
+  // This thread's share of the escape corrections: row cj = tid / 16 of the
+  // unit, batch slot cb, part cq of cP (cbp batch slots, cP = 16 / cbp parts),
+  // so the 16 threads of a row read consecutive escapes of it.
   const int cbp = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
   const int cP = kThreads / (kRows * cbp);
-  const int cj = threadIdx.x & 15, cb = (threadIdx.x >> 4) % cbp, cq = (threadIdx.x >> 4) / cbp;
+  const int cj = threadIdx.x >> 4, cb = (threadIdx.x & 15) / cP, cq = (threadIdx.x & 15) % cP;
   uint32_t u = first_unit, u_next = next_unit[1];
   uint32_t issued = 0, done = 0;  // k-blocks copied / computed by this warp
   bool aborted = false;           // a wait ran out: stop waiting, finish the schedule
@@ -573,6 +575,94 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
       const TensorDesc& d = p.d[cur.ti];
+      // ---- escape corrections of this unit, run through the k-loop.  Thread
+      // (row cj, batch slot cb, part cq) owns the escapes e = ce0 + cq + j cP
+      // of row cj (with the transposed x: thread (cj, part tid % 16) owns
+      // e = ce0 + part + 16 j, every batch row at once).  Each k-block moves
+      // kEscQ of them one stage along: A requests the position and value, B
+      // (one k-block later) gathers x (and the raw byte), C (one more k-block
+      // later) accumulates, so every load has a k-block's compute to land.
+      // Escapes the loop does not reach are taken after it, kEscDepth at a
+      // time.
+      constexpr bool kXt = XW > 0;
+      constexpr int kQ = kXt ? 1 : kEscQ;
+      constexpr int kXWords = kXt ? XW / 2 : 1;
+      const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
+      const uint32_t e_step = kXt ? uint32_t(kThreads / 16) : uint32_t(cP);
+      uint32_t e_next = kXt ? ce0 + (threadIdx.x & 15) : ce0 + cq;
+      const uint32_t e_end = SRC != kPlain && cj < cur.rows && (kXt || cb < B) ? ce1 : 0;
+      const uint16_t* xrow = kXt ? xt.p[cur.ti] : p.x[cur.ti] + int64_t(cb) * d.K;
+      uint32_t posA[kQ], valA[kQ], okA = 0, okB = 0;  // stage masks: entries requested / gathered
+      uint32_t xB[kQ][kXWords], loB[kQ], valB[kQ];
+      float c = 0.f, cs[kXt ? XW : 1];
+#pragma unroll
+      for (int b = 0; b < (kXt ? XW : 1); ++b) cs[b] = 0.f;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        posA[q] = uint32_t(rowbase);
+        valA[q] = loB[q] = valB[q] = 0u;
+#pragma unroll
+        for (int w = 0; w < kXWords; ++w) xB[q][w] = 0u;
+      }
+      // stage A: request positions and values of the next kQ escapes
+      auto esc_request = [&]() {
+        okA = 0;
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const uint32_t i = e_next + q * e_step;
+          const bool ok = i < e_end;
+          okA |= uint32_t(ok) << q;
+          posA[q] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+          valA[q] = ok ? load_esc_val(d, i) : 0u;  // value 0 and x 0: contributes exactly 0
+        }
+        e_next += kQ * e_step;
+      };
+      // stage C then B: accumulate the gathered escapes, gather the requested ones
+      auto esc_advance = [&]() {
+        if constexpr (SRC != kPlain) {
+          if (!(okA | okB)) return;  // nothing in flight (most k-blocks for byte-split's rare escapes)
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            if constexpr (kXt) {
+              const float delta = esc_delta<WCOMP_K15>(valB[q], 0u);
+#pragma unroll
+              for (int h = 0; h < kXWords; ++h) {
+                cs[2 * h] = fmaf(bf16_lo(xB[q][h]), delta, cs[2 * h]);
+                cs[2 * h + 1] = fmaf(bf16_hi(xB[q][h]), delta, cs[2 * h + 1]);
+              }
+            } else {
+              c = fmaf(__uint_as_float(xB[q][0] << 16), esc_delta<SRC>(valB[q], loB[q]), c);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            const bool ok = (okA >> q) & 1;
+            const uint64_t k = uint64_t(posA[q]) - rowbase;
+            valB[q] = ok ? valA[q] : 0u;
+            loB[q] = SRC == kBytesplit && ok ? uint32_t(d.raw[posA[q]]) : 0u;
+            if constexpr (kXt) {
+              const uint16_t* xr = xrow + k * XW;
+              if (XW == 4) {
+                const uint2 v = ok ? *reinterpret_cast<const uint2*>(xr) : make_uint2(0u, 0u);
+                xB[q][0] = v.x;
+                xB[q][1 % kXWords] = v.y;
+              } else {
+#pragma unroll
+                for (int h = 0; h < XW / 8; ++h) {
+                  const uint4 v = ok ? reinterpret_cast<const uint4*>(xr)[h] : make_uint4(0u, 0u, 0u, 0u);
+                  xB[q][(4 * h) % kXWords] = v.x; xB[q][(4 * h + 1) % kXWords] = v.y;
+                  xB[q][(4 * h + 2) % kXWords] = v.z; xB[q][(4 * h + 3) % kXWords] = v.w;
+                }
+              }
+            } else {
+              xB[q][0] = ok ? uint32_t(xrow[k]) : 0u;
+            }
+          }
+          okB = okA;
+          okA = 0;
+        }
+      };
+      if (SRC != kPlain && e_next < e_end) esc_request();
       for (uint32_t kb = cur.kb0; kb < cur.kb1; ++kb) {
         // every lane is done with the stage of the previous k-block, which the
         // copies below may refill
@@ -592,6 +682,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         else
           compute_item<SRC, NT, false>(d.t, lut, st, lane, uint32_t(32 * (lane & 3)) < cur.kvalid, xv, acc);
         ++done;
+        if constexpr (SRC != kPlain) {
+          esc_advance();
+          // no new requests in the last k-block: what is left goes to the batches below
+          if (kb + 1 < cur.kb1 && e_next < e_end) esc_request();
+        }
       }
       // ---- unit end: partial tiles, escape corrections, fixed-order sums
       float* pp = part + ((par * kWarps + warp) * 32 + lane) * 4 * NT;
@@ -600,30 +695,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int r = 0; r < 4; ++r) pp[4 * nt + r] = acc[nt][r];
       if constexpr (SRC != kPlain) {
-        const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
+        // what the loop has in flight (a request made before a k-loop of no
+        // k-blocks too), then the escapes it did not reach
+        esc_advance();
+        esc_advance();
         if constexpr (XW > 0) {
-          // thread (row cj, part tid / 16 of 16): every batch row at once
-          // from the transposed x; the two parts of a warp are summed by a
-          // shuffle, the warps in order in the final sum
-          float cs[XW];
-#pragma unroll
-          for (int b = 0; b < XW; ++b) cs[b] = 0.f;
-          if (cj < cur.rows) {
-            const uint16_t* xtb = xt.p[cur.ti];
+          // thread (row cj, part tid % 16 of 16): every batch row at once
+          // from the transposed x; the 16 parts of a row (one half-warp) are
+          // summed by a fixed shuffle tree
+          {
             constexpr int D = XW >= 16 ? kEscDepth / 4 : kEscDepth / 2;
-            for (uint32_t e = ce0 + (threadIdx.x >> 4); e < ce1; e += D * (kThreads / 16)) {
+            for (uint32_t e = e_next; e < e_end; e += D * e_step) {
               uint32_t pos[D], val[D];
 #pragma unroll
               for (int v = 0; v < D; ++v) {
-                const uint32_t i = e + v * (kThreads / 16);
-                const bool ok = i < ce1;
+                const uint32_t i = e + v * e_step;
+                const bool ok = i < e_end;
                 pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
                 val[v] = ok ? load_esc_val(d, i) : 0u;  // value 0: delta 0
               }
               uint32_t wv[D][XW / 2];
 #pragma unroll
               for (int v = 0; v < D; ++v) {
-                const uint16_t* xr = xtb + uint64_t(uint64_t(pos[v]) - rowbase) * XW;
+                const uint16_t* xr = xrow + uint64_t(uint64_t(pos[v]) - rowbase) * XW;
                 if (XW == 4) {
                   const uint2 q2 = *reinterpret_cast<const uint2*>(xr);
                   wv[v][0] = q2.x;
@@ -649,37 +743,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             }
           }
 #pragma unroll
-          for (int b = 0; b < XW; ++b) cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], 16);
-          if (lane < 16) {
+          for (int b = 0; b < (kXt ? XW : 1); ++b) {
 #pragma unroll
-            for (int b = 0; b < XW; ++b) corr[((par * kWarps + warp) * 16 + b) * kRows + lane] = cs[b];
+            for (int o = 8; o; o >>= 1) cs[b] += __shfl_xor_sync(0xffffffffu, cs[b], o);
+          }
+          if ((lane & 15) == 0) {
+#pragma unroll
+            for (int b = 0; b < (kXt ? XW : 1); ++b) corr[(par * kRows + cj) * 16 + b] = cs[b];
           }
         } else {
-          float c = 0.f;
-          if (cj < cur.rows && cb < B) {
-            const uint16_t* xb = p.x[cur.ti] + int64_t(cb) * d.K;
-            // kEscDepth escapes at a time, all their loads in flight together
-            // (positions and values, then the x and raw-byte gathers); entries
-            // past the row's last escape contribute exactly zero
-            for (uint32_t e = ce0 + cq; e < ce1; e += kEscDepth * cP) {
-              uint32_t pos[kEscDepth], val[kEscDepth], lo[kEscDepth], xw[kEscDepth];
+          // kEscDepth escapes at a time, all their loads in flight together
+          // (positions and values, then the x and raw-byte gathers); entries
+          // past the row's last escape contribute exactly zero
+          for (uint32_t e = e_next; e < e_end; e += kEscDepth * e_step) {
+            uint32_t pos[kEscDepth], val[kEscDepth], lo[kEscDepth], xw[kEscDepth];
 #pragma unroll
-              for (int v = 0; v < kEscDepth; ++v) {
-                const uint32_t i = e + v * cP;
-                const bool ok = i < ce1;
-                pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
-                val[v] = ok ? load_esc_val(d, i) : 0u;
-              }
-#pragma unroll
-              for (int v = 0; v < kEscDepth; ++v) {
-                const bool ok = e + v * cP < ce1;
-                lo[v] = SRC == kBytesplit && ok ? uint32_t(d.raw[pos[v]]) : 0u;
-                xw[v] = ok ? uint32_t(xb[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
-              }
-#pragma unroll
-              for (int v = 0; v < kEscDepth; ++v)
-                c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v], lo[v]), c);
+            for (int v = 0; v < kEscDepth; ++v) {
+              const uint32_t i = e + v * e_step;
+              const bool ok = i < e_end;
+              pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+              val[v] = ok ? load_esc_val(d, i) : 0u;
             }
+#pragma unroll
+            for (int v = 0; v < kEscDepth; ++v) {
+              const bool ok = e + v * e_step < e_end;
+              lo[v] = SRC == kBytesplit && ok ? uint32_t(d.raw[pos[v]]) : 0u;
+              xw[v] = ok ? uint32_t(xrow[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
+            }
+#pragma unroll
+            for (int v = 0; v < kEscDepth; ++v)
+              c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v], lo[v]), c);
           }
           corr[par * kThreads + threadIdx.x] = c;
         }
@@ -697,10 +790,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int w = 0; w < kWarps; ++w) y += part[((par * kWarps + w) * 32 + src_lane) * 4 * NT + reg];
         if constexpr (SRC != kPlain) {
           if (XW > 0) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) y += corr[((par * kWarps + w) * 16 + b) * kRows + j];
+            y += corr[(par * kRows + j) * 16 + b];
           } else {
-            for (int q = 0; q < cP; ++q) y += corr[par * kThreads + (q * cbp + b) * kRows + j];
+            for (int q = 0; q < cP; ++q) y += corr[par * kThreads + j * 16 + b * cP + q];
           }
         }
         p.y[cur.ti][int64_t(b) * d.N + cur.r0 + j] = y;
@@ -968,14 +1060,14 @@ int launch(GemvBatch& b, const TmaBatch& tm, const int64_t* Ns, int B, int dev, 
   return map_cuda(e);
 }
 
-// K15 at B >= 3 corrects its escapes from a transposed copy of x, as wide as
-// the batch rounds up to (4, 8 or 16 values per column); at B <= 2 the extra
-// pass costs more than the gathers it saves, and byte-split's few escapes
-// gain nothing from it.
+// K15 at B >= 2 corrects its escapes from a transposed copy of x, as wide as
+// the batch rounds up to (4, 8 or 16 values per column), so one thread adds an
+// escape to every batch row with one or two 16-byte loads; byte-split's few
+// escapes gain nothing from it.
 template <int SRC>
 int dispatch_vec(GemvBatch& b, const TmaBatch& tm, const int64_t* Ns, int B, int dev, int sms, cudaStream_t s) {
   if constexpr (SRC == kK15) {
-    if (B >= 3) {
+    if (B >= 2) {
       if (B <= 4) return launch<SRC, 1, 4>(b, tm, Ns, B, dev, sms, s);
       if (B <= 8) return launch<SRC, 1, 8>(b, tm, Ns, B, dev, sms, s);
       return launch<SRC, 2, 16>(b, tm, Ns, B, dev, sms, s);
