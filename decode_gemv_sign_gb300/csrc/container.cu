@@ -113,6 +113,7 @@ extern "C" const char* wcomp_strerror(int s) {
     case WCOMP_EUNSUPPORTED: return "unsupported size";
     case WCOMP_ETIMEOUT: return "a device wait timed out";
     case WCOMP_EINTERNAL: return "internal consistency check failed";
+    case WCOMP_EBOUNDS: return "a kernel index check failed (debug build)";
     default: return "unknown status";
   }
 }

@@ -21,6 +21,7 @@
 
 namespace wc {
 namespace {
+WCOMP_DEBUG_WORD
 
 constexpr int kThreads = 256;
 
@@ -46,7 +47,9 @@ __device__ __forceinline__ void decode_tile(const TensorDesc& d, uint16_t* __res
   // barrier orders every placeholder store of the tile before the patches.
   __syncthreads();
   for (uint32_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    if (!WCOMP_DCHECK(e < d.E, 0)) continue;
     const uint32_t p = d.esc_pos[e];
+    if (!WCOMP_DCHECK(p < d.n && p / kTile == tile, 0)) continue;
     if (SCHEME == WCOMP_BYTESPLIT)
       reinterpret_cast<uint8_t*>(out)[2 * uint64_t(p) + 1] = d.esc_val[e];  // high byte only
     else
@@ -100,6 +103,8 @@ int launch_decode(const wcomp_container* const* cs, uint16_t* const* outs, int c
 }
 
 }  // namespace
+
+WCOMP_DEBUG_TAKE(debug_take_decode)
 }  // namespace wc
 
 using namespace wc;

@@ -22,6 +22,7 @@
 
 namespace wc {
 namespace {
+WCOMP_DEBUG_WORD
 
 constexpr int kThreads = 256;  // pack / compact: one 8192-element tile per CTA
 
@@ -315,6 +316,7 @@ __device__ __forceinline__ void stash_group(const EncDesc& d, uint32_t tile, uin
       const uint32_t pw = (j >> 1) == 0 ? wv[4 * k] : (j >> 1) == 1 ? wv[4 * k + 1]
                           : (j >> 1) == 2 ? wv[4 * k + 2] : wv[4 * k + 3];
       const uint32_t v = (pw >> (16 * (j & 1))) & 0xFFFF;
+      if (!WCOMP_DCHECK(o < uint64_t(tile + 1) * d.stash_cap && o < uint64_t(d.n_tiles) * d.stash_cap, 3)) break;
       d.stash_pos[o] = uint32_t(base + 8 * k + j);
       d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
       ++o;
@@ -519,6 +521,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
       for (int e = 0; e < kGroup; ++e) {
         if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape && o < d.E) {
           const uint32_t p = uint32_t(base + e);
+          if (!WCOMP_DCHECK(p < d.n, 3)) break;
           const uint32_t v = d.w[p];
           pos[o] = p;
           if (SCHEME == WCOMP_BYTESPLIT)
@@ -916,6 +919,8 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
 }
 
 }  // namespace
+
+WCOMP_DEBUG_TAKE(debug_take_encode)
 }  // namespace wc
 
 using namespace wc;

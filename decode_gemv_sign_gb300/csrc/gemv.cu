@@ -62,6 +62,7 @@
 
 namespace wc {
 namespace {
+WCOMP_DEBUG_WORD
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -373,7 +374,7 @@ __device__ __forceinline__ void load_x(const GemvBatch& p, const Unit& m, uint32
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int b = g + 8 * nt;
-    if (kok && b < B) {
+    if (kok && b < B && WCOMP_DCHECK(int64_t(kb) * kKBlock + 32 * t + 32 <= K, 2)) {
       const uint16_t* xr = p.x[m.ti] + int64_t(b) * K + int64_t(kb) * kKBlock + 32 * t;
 #pragma unroll
       for (int i = 0; i < 4; ++i) xv[nt][i] = ld_x_v4(xr + 8 * i);
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
           const uint32_t i = e_next + q * e_step;
-          const bool ok = i < e_end;
+          const bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
           okA |= uint32_t(ok) << q;
           posA[q] = ok ? d.esc_pos[i] : uint32_t(rowbase);
           valA[q] = ok ? load_esc_val(d, i) : 0u;  // value 0 and x 0: contributes exactly 0
@@ -636,8 +637,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
 #pragma unroll
           for (int q = 0; q < kQ; ++q) {
-            const bool ok = (okA >> q) & 1;
             const uint64_t k = uint64_t(posA[q]) - rowbase;
+            const bool ok = ((okA >> q) & 1) && WCOMP_DCHECK(k < uint64_t(d.K), 1);
             valB[q] = ok ? valA[q] : 0u;
             loB[q] = SRC == kBytesplit && ok ? uint32_t(d.raw[posA[q]]) : 0u;
             if constexpr (kXt) {
@@ -710,8 +711,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
               for (int v = 0; v < D; ++v) {
                 const uint32_t i = e + v * e_step;
-                const bool ok = i < e_end;
+                bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
                 pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+                ok = ok && WCOMP_DCHECK(uint64_t(pos[v]) - rowbase < uint64_t(d.K), 1);
+                if (!ok) pos[v] = uint32_t(rowbase);
                 val[v] = ok ? load_esc_val(d, i) : 0u;  // value 0: delta 0
               }
               uint32_t wv[D][XW / 2];
@@ -756,17 +759,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // (positions and values, then the x and raw-byte gathers); entries
           // past the row's last escape contribute exactly zero
           for (uint32_t e = e_next; e < e_end; e += kEscDepth * e_step) {
-            uint32_t pos[kEscDepth], val[kEscDepth], lo[kEscDepth], xw[kEscDepth];
+            uint32_t pos[kEscDepth], val[kEscDepth], lo[kEscDepth], xw[kEscDepth], okm = 0;
 #pragma unroll
             for (int v = 0; v < kEscDepth; ++v) {
               const uint32_t i = e + v * e_step;
-              const bool ok = i < e_end;
+              bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
               pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+              ok = ok && WCOMP_DCHECK(uint64_t(pos[v]) - rowbase < uint64_t(d.K), 1);
+              okm |= uint32_t(ok) << v;
               val[v] = ok ? load_esc_val(d, i) : 0u;
             }
 #pragma unroll
             for (int v = 0; v < kEscDepth; ++v) {
-              const bool ok = e + v * e_step < e_end;
+              const bool ok = (okm >> v) & 1;
               lo[v] = SRC == kBytesplit && ok ? uint32_t(d.raw[pos[v]]) : 0u;
               xw[v] = ok ? uint32_t(xrow[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
             }
@@ -795,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int q = 0; q < cP; ++q) y += corr[par * kThreads + j * 16 + b * cP + q];
           }
         }
-        p.y[cur.ti][int64_t(b) * d.N + cur.r0 + j] = y;
+        if (WCOMP_DCHECK(b < B && cur.r0 + j < d.N, 2)) p.y[cur.ti][int64_t(b) * d.N + cur.r0 + j] = y;
       }
       if (!have_next) break;
       // advance: the next unit becomes current, the copy cursor keeps its place.
@@ -1195,6 +1200,8 @@ int gemv_plain(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks, 
 }
 
 }  // namespace
+
+WCOMP_DEBUG_TAKE(debug_take_gemv)
 }  // namespace wc
 
 using namespace wc;
@@ -1227,7 +1234,9 @@ extern "C" int wcomp_device_check(void* stream) {
       if (e != cudaSuccess) return map_cuda(e);
     }
   }
-  return failed ? WCOMP_ETIMEOUT : WCOMP_OK;
+  if (failed) return WCOMP_ETIMEOUT;
+  const uint32_t dbg = debug_take_decode() | debug_take_encode() | debug_take_gemv();
+  return dbg ? WCOMP_EBOUNDS : WCOMP_OK;
 }
 
 extern "C" int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream) {

@@ -129,6 +129,7 @@ struct TensorDesc {
   const uint32_t* esc_pos;
   const uint8_t* esc_val;  // uint8 (byte-split) or uint16 (K15) entries
   uint64_t n;
+  uint64_t E;              // escapes
   int64_t N, K;
   RegTable t;
   int scheme;
@@ -148,6 +149,7 @@ inline TensorDesc make_desc(const wcomp_container* c) {
   d.esc_pos = reinterpret_cast<const uint32_t*>(c->d_esc + L.off_pos);
   d.esc_val = c->d_esc + L.off_val;
   d.n = L.n;
+  d.E = L.E;
   d.N = L.N;
   d.K = L.K;
   d.t = make_reg_table(c->table, L.scheme);
@@ -398,6 +400,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (WCOMP_MBAR_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   return false;
 }
+
+// ---------------------------------------------------------------------------
+// Debug builds (WCOMP_DEBUG=1): index checks before the kernels' memory
+// accesses.  A failed check sets a bit in the translation unit's error word
+// and the access is skipped, so the kernel finishes; wcomp_device_check
+// reports it as WCOMP_EBOUNDS.  Release builds compile the checks away.
+//   bit 0: decode output or escape position out of range
+//   bit 1: GEMV escape position, row or column out of range
+//   bit 2: GEMV output or x index out of range
+//   bit 3: encoder stash or escape stream index out of range
+// ---------------------------------------------------------------------------
+#ifndef WCOMP_DEBUG
+#define WCOMP_DEBUG 0
+#endif
+#if WCOMP_DEBUG
+#define WCOMP_DEBUG_WORD static __device__ uint32_t g_debug_err;
+#define WCOMP_DCHECK(cond, bit) ((cond) ? true : (atomicOr(&g_debug_err, 1u << (bit)), false))
+#define WCOMP_DEBUG_TAKE(fn)                                                          \
+  uint32_t fn() {                                                                     \
+    uint32_t v = 0, z = 0;                                                            \
+    if (cudaMemcpyFromSymbol(&v, g_debug_err, sizeof(v)) != cudaSuccess) return ~0u; \
+    cudaMemcpyToSymbol(g_debug_err, &z, sizeof(z));                                   \
+    return v;                                                                         \
+  }
+#else
+#define WCOMP_DEBUG_WORD
+#define WCOMP_DCHECK(cond, bit) true
+#define WCOMP_DEBUG_TAKE(fn) \
+  uint32_t fn() { return 0; }
+#endif
+// Each translation unit's debug error word, read and cleared (0 in release builds).
+uint32_t debug_take_decode();
+uint32_t debug_take_encode();
+uint32_t debug_take_gemv();
 
 // Host-side launch helpers (defined in container.cu).
 // Stream-ordered allocation from the library's own memory pool on the current

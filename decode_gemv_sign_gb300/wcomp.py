@@ -20,7 +20,7 @@ BYTESPLIT = 0
 K15 = 1
 SCHEMES = {"bytesplit": BYTESPLIT, "byte-split": BYTESPLIT, "k15": K15, BYTESPLIT: BYTESPLIT, K15: K15}
 
-OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED, ETIMEOUT, EINTERNAL = 0, -1, -2, -3, -4, -5, -6, -7
+OK, EINVAL, ENOMEM, ECORRUPT, ECUDA, EUNSUPPORTED, ETIMEOUT, EINTERNAL, EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7, -8
 
 
 class WcompError(RuntimeError):

@@ -69,7 +69,8 @@ typedef enum {
   WCOMP_ECUDA = -4,         /* a CUDA runtime call failed */
   WCOMP_EUNSUPPORTED = -5,  /* size outside the supported range */
   WCOMP_ETIMEOUT = -6,      /* a kernel's bounded wait on its own copies ran out */
-  WCOMP_EINTERNAL = -7      /* an internal consistency check failed; no result was returned */
+  WCOMP_EINTERNAL = -7,     /* an internal consistency check failed; no result was returned */
+  WCOMP_EBOUNDS = -8        /* a debug build's index check failed inside a kernel (the access was skipped) */
 } wcomp_status;
 
 typedef struct wcomp_container wcomp_container;
@@ -238,8 +239,10 @@ WCOMP_API int wcomp_gemv_batched(const wcomp_container* const* containers, const
  * wcomp_gemv and the batched GEMVs use, and the one in wcomp_gemv_noalloc's
  * static array).  A GEMV kernel whose bounded wait on its own tensor copies
  * runs out records it there and finishes without waiting instead of hanging;
- * its outputs are then undefined.  Synchronizes `stream`.  Returns WCOMP_OK
- * or WCOMP_ETIMEOUT.
+ * its outputs are then undefined.  In a debug build (compiled with
+ * WCOMP_DEBUG=1) the kernels also check their indexes before memory
+ * accesses, skip an access that fails and record it.  Synchronizes `stream`.
+ * Returns WCOMP_OK, WCOMP_ETIMEOUT or WCOMP_EBOUNDS.
  */
 WCOMP_API int wcomp_device_check(void* stream);
 

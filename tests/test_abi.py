@@ -109,7 +109,7 @@ def test_batched_and_remaining_argument_errors_without_gpu(lib):
 
 def test_every_status_has_its_own_message(lib):
     codes = [wcomp.OK, wcomp.EINVAL, wcomp.ENOMEM, wcomp.ECORRUPT, wcomp.ECUDA, wcomp.EUNSUPPORTED, wcomp.ETIMEOUT,
-             wcomp.EINTERNAL]
+             wcomp.EINTERNAL, wcomp.EBOUNDS]
     msgs = [lib.wcomp_strerror(c) for c in codes]
     assert all(msgs) and len(set(msgs)) == len(codes)
     assert lib.wcomp_strerror(-99) == b"unknown status"
@@ -117,9 +117,9 @@ def test_every_status_has_its_own_message(lib):
     src = open(HEADER).read()
     enum = dict((k, int(v)) for k, v in re.findall(r"WCOMP_(OK|E[A-Z]+)\s*=\s*(-?\d+)", src))
     assert enum == {"OK": 0, "EINVAL": -1, "ENOMEM": -2, "ECORRUPT": -3, "ECUDA": -4, "EUNSUPPORTED": -5,
-                    "ETIMEOUT": -6, "EINTERNAL": -7}
+                    "ETIMEOUT": -6, "EINTERNAL": -7, "EBOUNDS": -8}
     assert [enum[k] for k in ("OK", "EINVAL", "ENOMEM", "ECORRUPT", "ECUDA", "EUNSUPPORTED", "ETIMEOUT",
-                              "EINTERNAL")] == codes
+                              "EINTERNAL", "EBOUNDS")] == codes
 
 
 def _deser_status(lib, buf: bytes) -> int:

@@ -33,6 +33,27 @@ def host(t) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
+GUARD = 4096  # elements of pattern on each side of a guarded output
+
+
+class Guarded:
+    """A device output with guard regions before and after it, filled with a
+    known bit pattern: a store past either end of the output (which a kernel
+    writing exactly-sized buffers could otherwise make unseen) changes them."""
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape))
+        self.n = n
+        word = torch.int16 if dtype == torch.int16 else torch.int32
+        self.pattern = 0x5A5A if word == torch.int16 else 0x7FBADBAD
+        self.raw = torch.full((n + 2 * GUARD,), self.pattern, dtype=word, device="cuda")
+        self.out = self.raw.view(dtype)[GUARD:GUARD + n].view(*shape)
+
+    def check(self):
+        head, tail = self.raw[:GUARD], self.raw[GUARD + self.n:]
+        assert bool((head == self.pattern).all()) and bool((tail == self.pattern).all()), "guard region overwritten"
+
+
 def check_gemv(y_gpu, y_ref):
     y = y_gpu.cpu().numpy().astype(np.float64)
     scale = np.abs(y_ref).max()
@@ -71,8 +92,10 @@ def test_container_and_decode_bit_exact(W, case, scheme):
     compact = O.serialize_compact(ref)
     assert W.serialize(c, compact=True) == compact
     assert inf["serialized_compact_bytes"] == len(compact)
-    out = W.decode(c)
+    g = Guarded(w.shape, torch.int16)
+    out = W.decode(c, g.out)
     assert np.array_equal(host(out).reshape(w.shape), w)
+    g.check()
     c.free()
     # the compact bytes load back into the same device container
     c2 = W.deserialize(compact)
@@ -139,8 +162,10 @@ def test_gemv_matches_oracle(W, scheme, B):
     w = synth.gen_weights_np(spec)
     x = synth.gen_x_np(B, spec.K, 200 + B)
     c = W.encode(dev(w), scheme)
-    y = W.gemv(c, dev(x))
+    g = Guarded((B, spec.N), torch.float32)
+    y = W.gemv(c, dev(x), g.out)
     check_gemv(y, O.gemv(w, x))
+    g.check()
     # deterministic: same bits on a second call
     y2 = W.gemv(c, dev(x))
     assert torch.equal(y, y2)
@@ -160,13 +185,15 @@ def test_gemv_partial_blocks(W, scheme, shape, B):
     spec = synth.WeightSpec("p", N, K, "t4", 0.02, 0.01, "normal", 1.0, seed=31 * N + K)
     w = synth.gen_weights_np(spec)
     x = synth.gen_x_np(B, K, 17 * B + K)
+    g = Guarded((B, N), torch.float32)
     if scheme == 2:
-        y = W.gemv_bf16(dev(w), dev(x))
+        y = W.gemv_bf16(dev(w), dev(x), g.out)
     else:
         c = W.encode(dev(w), scheme)
-        y = W.gemv(c, dev(x))
+        y = W.gemv(c, dev(x), g.out)
         c.free()
     check_gemv(y, O.gemv(w, x))
+    g.check()
 
 
 @pytest.mark.parametrize("scheme", O.SCHEMES)
@@ -211,10 +238,14 @@ def test_escapes_on_row_and_tile_boundaries(W, scheme, shape):
     c = W.encode(dev(w), scheme)
     assert W.serialize(c) == O.serialize(ref)
     assert W.serialize(c, compact=True) == O.serialize_compact(ref)
-    assert np.array_equal(host(W.decode(c)).reshape(w.shape), w)
+    gd = Guarded(w.shape, torch.int16)
+    assert np.array_equal(host(W.decode(c, gd.out)).reshape(w.shape), w)
+    gd.check()
     for B in (1, 4, 16):
         x = synth.gen_x_np(B, shape[1], 40 + B)
-        check_gemv(W.gemv(c, dev(x)), O.gemv(w, x))
+        gy = Guarded((B, shape[0]), torch.float32)
+        check_gemv(W.gemv(c, dev(x), gy.out), O.gemv(w, x))
+        gy.check()
     c.free()
 
 
@@ -267,14 +298,18 @@ def test_batched_matches_single(W):
              for i, (N, K) in enumerate([(64, 1024), (200, 640), (33, 1000), (128, 2048), (1, 4096)])]
     ws = [synth.gen_weights_np(s) for s in specs]
     cs = [W.encode(dev(w), i % 2) for i, w in enumerate(ws)]
-    outs = W.decode_batched(cs)
-    for w, o in zip(ws, outs):
+    gd = [Guarded(w.shape, torch.int16) for w in ws]
+    outs = W.decode_batched(cs, [g.out for g in gd])
+    for w, o, g in zip(ws, outs, gd):
         assert np.array_equal(host(o).reshape(w.shape), w)
+        g.check()
     for B in (1, 4):
         xs = [synth.gen_x_np(B, s.K, 500 + i) for i, s in enumerate(specs)]
-        ys = W.gemv_batched(cs, [dev(x) for x in xs])
-        for c, w, x, y in zip(cs, ws, xs, ys):
+        gy = [Guarded((B, s.N), torch.float32) for s in specs]
+        ys = W.gemv_batched(cs, [dev(x) for x in xs], [g.out for g in gy])
+        for c, w, x, y, g in zip(cs, ws, xs, ys, gy):
             check_gemv(y, O.gemv(w, x))
+            g.check()
             assert torch.equal(y, W.gemv(c, dev(x)))
     for c in cs:
         c.free()

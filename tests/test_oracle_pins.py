@@ -423,3 +423,17 @@ def test_synth_rounding_matches_ieee_rne():
     for u, b in cases.items():
         f = struct.unpack("<f", struct.pack("<I", u))[0]
         assert int(synth.f32_to_bf16_bits(np.array([f], np.float32))[0]) == b
+
+
+def test_dense12_workload_has_no_byte_split_escape():
+    """The escape-free workload of the dense 12-bit ablation: every magnitude in
+    [2^-14, 2^-2) leaves 14 high bytes (two signs x exponent bits 7..1 of
+    113..124), fewer than the table's 15, so byte-split escapes nothing and
+    costs 4 + 8 + 15 * 8 / n bits per weight."""
+    w = synth.gen_weights_np(synth.dense12_spec(64, 2048, seed=3))
+    hi = np.unique(w >> 8)
+    assert len(hi) <= 14
+    c = O.encode(w, O.BYTESPLIT)
+    assert c.E == 0
+    assert O.entropy_bpw(O.BYTESPLIT, c.n, c.E) == pytest.approx(12 + 15 * 8 / c.n)
+    assert np.array_equal(O.decode(c).reshape(w.shape), w)

@@ -4,8 +4,9 @@ It serves callers that cannot let the library allocate device memory (a fixed
 memory budget, or no implicit synchronisation from cudaMalloc / cudaFree); its
 work counters live in a small static device array instead of a buffer the
 library allocates.  Checked through the C ABI against wcomp_gemv on the same
-container and input, on two calls in a row (the array keeps the previous
-call's contents, so the second call shows that the counters are cleared).
+container and input, and against the CPU oracle's float64 GEMV, on two calls
+in a row (the array keeps the previous call's contents, so the second call
+shows that the counters are cleared).
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has run every other test first; it also passes on its own in a fresh
@@ -15,6 +16,7 @@ import numpy as np
 import pytest
 
 from decode_gemv_sign_gb300 import synth
+from oracle import wcomp_oracle as O
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -44,13 +46,17 @@ def test_noalloc_matches_gemv_twice(W, scheme, B, shape):
     x = synth.gen_x_np(B, K, 7100 + B)
     c = W.encode(dev(w), scheme)
     xd = dev(x)
-    y_ref = W.gemv(c, xd).cpu().numpy().astype(np.float64)
-    scale = np.abs(y_ref).max()
+    y_lib = W.gemv(c, xd).cpu().numpy().astype(np.float64)
+    y_ora = O.gemv(w, x)
+    scale = np.abs(y_ora).max()
+    assert np.abs(y_lib - y_ora).max() <= GEMV_TOL * scale
     for _ in range(2):
         y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
         W.gemv_noalloc(c, xd, y)
         got = y.cpu().numpy().astype(np.float64)
-        assert np.abs(got - y_ref).max() <= GEMV_TOL * scale
+        assert np.abs(got - y_lib).max() <= GEMV_TOL * scale
+        assert np.abs(got - y_ora).max() <= GEMV_TOL * scale
+    W.device_check()
     c.free()
 
 
