@@ -422,10 +422,23 @@ extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* strea
   return WCOMP_OK;
 }
 
+// Release one container's hold on a block: its own allocation, or its share
+// of an arena (the arena's block goes back to the pool with the last share).
+static void release_block(Arena* a, void* own, cudaStream_t s) {
+  if (a) {
+    if (a->refs.fetch_sub(1, std::memory_order_acq_rel) == 1) {
+      cudaFreeAsync(a->block, s);
+      delete a;
+    }
+  } else if (own) {
+    cudaFreeAsync(own, s);
+  }
+}
+
 extern "C" void wcomp_free(wcomp_container* c, void* stream) {
   if (!c) return;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (c->d_main) cudaFreeAsync(c->d_main, s);
-  if (c->d_esc) cudaFreeAsync(c->d_esc, s);
+  release_block(c->main_arena, c->d_main, s);
+  release_block(c->esc_arena, c->d_esc, s);
   delete c;
 }

@@ -608,7 +608,7 @@ cudaError_t launch_zero(ZeroList& z, cudaStream_t s) {
 
 // Escapes a tile's stash holds (pack records them, compaction copies them;
 // a tile with more is ranked again from its codes).
-constexpr uint32_t kStashCap = 256;
+constexpr uint32_t kStashCap = 512;
 
 // Pinned host memory for one call's summaries, kept per host thread and
 // grown on demand.  A call returns only after its copy into it completed.
@@ -652,17 +652,43 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   };
   cudaError_t e = pool_alloc(reinterpret_cast<void**>(&d_sum), sizeof(Summary) * count, s);
   if (e != cudaSuccess) return map_cuda(e);
+  // the containers' main sections: one arena block for the whole batch, each
+  // container's part starting on a 256-byte boundary
+  Arena* main_arena = new (std::nothrow) Arena();
+  if (!main_arena) return fail(cudaErrorMemoryAllocation);
+  {
+    uint64_t total = 0;
+    for (int i = 0; i < count; ++i) {
+      Layout L;
+      L.compute(schemes[i], Ns[i], Ks[i], 0);
+      total += (L.main_alloc + 255) & ~uint64_t(255);
+    }
+    e = pool_alloc(&main_arena->block, total, s);
+    if (e != cudaSuccess) {
+      delete main_arena;
+      return fail(e);
+    }
+  }
+  uint64_t main_off = 0;
   ZeroList z;
   memset(&z, 0, sizeof(z));
   for (int i = 0; i < count; ++i) {
     wcomp_container* c = new (std::nothrow) wcomp_container();
-    if (!c) return fail(cudaErrorMemoryAllocation);
+    if (!c) {
+      if (main_arena->refs.load() == 0) {
+        cudaFreeAsync(main_arena->block, s);
+        delete main_arena;
+      }
+      return fail(cudaErrorMemoryAllocation);
+    }
     jobs[i].c = c;
     c->device = dev;
     Layout& L = c->L;
     L.compute(schemes[i], Ns[i], Ks[i], 0);
-    e = pool_alloc(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
-    if (e != cudaSuccess) return fail(e);
+    c->main_arena = main_arena;
+    main_arena->refs.fetch_add(1, std::memory_order_relaxed);
+    c->d_main = static_cast<uint8_t*>(main_arena->block) + main_off;
+    main_off += (L.main_alloc + 255) & ~uint64_t(255);
     EncDesc& d = jobs[i].d;
     memset(&d, 0, sizeof(d));
     d.w = ws[i];
@@ -853,6 +879,24 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   // first wait: escape counts and tables (pack and the scan keep running)
   e = cudaEventSynchronize(ready);
   if (e != cudaSuccess) return fail3(e);
+  // the escape streams, sized now that E is known: one arena block for the batch
+  uint64_t esc_total = 0;
+  for (int i = 0; i < count; ++i) {
+    Layout L = jobs[i].c->L;
+    L.compute(L.scheme, L.N, L.K, hs[i].E);
+    if (L.E) esc_total += (L.esc_payload + 255) & ~uint64_t(255);
+  }
+  Arena* esc_arena = nullptr;
+  if (esc_total) {
+    esc_arena = new (std::nothrow) Arena();
+    if (!esc_arena) return fail3(cudaErrorMemoryAllocation);
+    e = pool_alloc(&esc_arena->block, esc_total, s);
+    if (e != cudaSuccess) {
+      delete esc_arena;
+      return fail3(e);
+    }
+  }
+  uint64_t esc_off = 0;
   for (int i = 0; i < count; ++i) {
     wcomp_container* c = jobs[i].c;
     memcpy(c->table, hs[i].table, sizeof(c->table));
@@ -863,8 +907,10 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
     d.off_pos = L.off_pos;
     d.off_val = L.off_val;
     if (L.E) {
-      e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
-      if (e != cudaSuccess) return fail3(e);
+      c->esc_arena = esc_arena;
+      esc_arena->refs.fetch_add(1, std::memory_order_relaxed);
+      c->d_esc = static_cast<uint8_t*>(esc_arena->block) + esc_off;
+      esc_off += (L.esc_payload + 255) & ~uint64_t(255);
       d.esc = c->d_esc;
       add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
       add_pad(z, c->d_esc, L.off_val, L.sz_val);

@@ -63,6 +63,11 @@
 namespace wc {
 namespace {
 WCOMP_DEBUG_WORD
+#if WCOMP_DEBUG
+// Debug builds: when set, every warp of a GEMV launch leaves its first copy
+// unissued but waits for it, so that bounded wait runs out.
+__device__ uint32_t g_debug_skip_first_copy;
+#endif
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -146,7 +151,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // ---------------------------------------------------------------------------
 // TMA and mbarriers.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls of a stage's mbarrier before giving up (tenths of a second at least)
+constexpr uint64_t kWaitNs = 1000000000ull;  // how long a wait on a stage's copies may take (1 s)
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t x, uint32_t y,
                                             uint32_t bar) {
@@ -170,12 +175,21 @@ __device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase of the given parity; false if it did not complete
-// within kWaitLimit polls.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of the given parity; false if it has not completed by
+// `deadline` (global timer, ns).
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, uint64_t deadline) {
+  while (!mbar_done(bar, parity))
+    if (global_ns() > deadline) return false;
+  return true;
+}
+// The same with a deadline kWaitNs from the first poll that failed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_done(bar, parity)) return true;
-  return false;
+  return mbar_done(bar, parity) || mbar_wait_until(bar, parity, global_ns() + kWaitNs);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
@@ -512,7 +526,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int cj = threadIdx.x >> 4, cb = (threadIdx.x & 15) / cP, cq = (threadIdx.x & 15) % cP;
   uint32_t u = first_unit, u_next = next_unit[1];
   uint32_t issued = 0, done = 0;  // k-blocks copied / computed by this warp
-  bool aborted = false;           // a wait ran out: stop waiting, finish the schedule
+  bool aborted = false;           // a wait ran out (warp-uniform): no more copies or waits, finish the schedule
+#if WCOMP_DEBUG
+  const bool skip_first_copy = g_debug_skip_first_copy != 0;
+#else
+  constexpr bool skip_first_copy = false;
+#endif
   if (u < total_units) {
     Unit cur, nxt;
     uint32_t ce0 = 0, ce1 = 0, ne0 = 0, ne1 = 0;  // row cj's escapes in the current / next unit
@@ -545,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ckb = nxt.kb0;
       }
       if (ahead == 1 && ckb >= nxt.kb1) return false;
-      if (lane == 0) {
+      if (lane == 0 && !(skip_first_copy && issued == 0)) {
         const uint32_t sidx = issued % kStages;
         issue_item<SRC>(tm, ahead == 0 ? cur : nxt, ckb, ring + sidx * StageGeom<SRC>::kBytes, bars + 8 * sidx);
       }
@@ -668,14 +687,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // every lane is done with the stage of the previous k-block, which the
         // copies below may refill
         __syncwarp();
-        while (issued < done + kStages && issue_next()) {
+        while (!aborted && issued < done + kStages && issue_next()) {
         }
         uint4 xv[NT][4];
         load_x<NT>(p, cur, kb, B, lane, xv);
         const uint32_t sidx = done % kStages;
-        if (!aborted && !mbar_wait_bounded(bars + 8 * sidx, (done / kStages) & 1)) {
-          aborted = true;  // this lane stops waiting; the warp still runs the same instructions
-          atomicOr(err, 1u);
+        if (!aborted && __any_sync(0xffffffffu, !mbar_wait_bounded(bars + 8 * sidx, (done / kStages) & 1))) {
+          aborted = true;  // the warp stops copying and waiting, and still runs the same instructions
+          if (lane == 0) atomicOr(err, 1u);
         }
         const uint32_t st = ring + sidx * StageGeom<SRC>::kBytes;
         if (kb + 1 < cur.nkb || cur.kvalid == kKBlock)
@@ -831,9 +850,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   // A warp that gave up waiting lets its copies in flight land (bounded)
   // before the CTA exits; otherwise every copy it issued has been waited for.
-  if (__any_sync(0xffffffffu, aborted) && lane == 0) {
+  if (aborted && lane == 0) {
+    const uint64_t deadline = global_ns() + kWaitNs;
     for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-      mbar_wait_bounded(bars + 8 * (i % kStages), (i / kStages) & 1);
+      mbar_wait_until(bars + 8 * (i % kStages), (i / kStages) & 1, deadline);
   }
   __syncwarp();
   // The last CTA to finish returns the counter slot to zero for the next launch.
@@ -1237,6 +1257,21 @@ extern "C" int wcomp_device_check(void* stream) {
   if (failed) return WCOMP_ETIMEOUT;
   const uint32_t dbg = debug_take_decode() | debug_take_encode() | debug_take_gemv();
   return dbg ? WCOMP_EBOUNDS : WCOMP_OK;
+}
+
+extern "C" int wcomp_debug_skip_first_copy(int on) {
+#if WCOMP_DEBUG
+  const uint32_t v = on ? 1u : 0u;
+  const cudaError_t e = cudaMemcpyToSymbol(g_debug_skip_first_copy, &v, sizeof(v));
+  if (e == cudaSuccess) {
+    const cudaError_t e2 = cudaDeviceSynchronize();
+    if (e2 != cudaSuccess) return map_cuda(e2);
+  }
+  return e == cudaSuccess ? WCOMP_OK : map_cuda(e);
+#else
+  (void)on;
+  return WCOMP_EUNSUPPORTED;
+#endif
 }
 
 extern "C" int wcomp_gemv(const wcomp_container* c, const uint16_t* d_x, int B, float* d_y, void* stream) {

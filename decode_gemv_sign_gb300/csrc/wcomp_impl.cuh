@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/wcomp.h"
@@ -82,11 +83,23 @@ struct Scratch {
 
 }  // namespace wc
 
+namespace wc {
+// Device memory shared by the containers of one batched encode (one block for
+// their main sections, one for their escape streams): returned to the pool
+// when the last container using it is released.
+struct Arena {
+  void* block = nullptr;
+  std::atomic<int> refs{0};
+};
+}  // namespace wc
+
 struct wcomp_container {
   wc::Layout L;
   uint16_t table[wc::kTableSize];
-  uint8_t* d_main = nullptr;
-  uint8_t* d_esc = nullptr;
+  uint8_t* d_main = nullptr;       // inside main_arena when that is set, else its own allocation
+  uint8_t* d_esc = nullptr;        // inside esc_arena when that is set, else its own allocation
+  wc::Arena* main_arena = nullptr;
+  wc::Arena* esc_arena = nullptr;
   int device = 0;
   // TMA descriptors of the code and raw / mantissa streams, made on the
   // first fused GEMV (tmap_ok: 1 made, 0 not applicable to this shape)

@@ -91,13 +91,15 @@ def lib():
     L.wcomp_version.argtypes = []
     L.wcomp_device_check.argtypes = [P]
     L.wcomp_device_check.restype = ctypes.c_int
+    L.wcomp_debug_skip_first_copy.argtypes = [ctypes.c_int]
+    L.wcomp_debug_skip_first_copy.restype = ctypes.c_int
     L.wcomp_launch_count.argtypes = []
     L.wcomp_launch_count.restype = ctypes.c_uint64
     for name in ("wcomp_encode", "wcomp_encode_batched", "wcomp_encode_hist_grid", "wcomp_decode", "wcomp_gemv", "wcomp_gemv_noalloc",
                  "wcomp_gemv_bf16", "wcomp_gemv_bf16_batched",
                  "wcomp_decode_batched",
                  "wcomp_gemv_batched", "wcomp_info", "wcomp_serialize", "wcomp_serialize_compact",
-                 "wcomp_deserialize", "wcomp_version"):
+                 "wcomp_deserialize", "wcomp_version", "wcomp_debug_skip_first_copy"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

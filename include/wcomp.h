@@ -139,7 +139,10 @@ WCOMP_API int wcomp_encode_hist_grid(const uint64_t* n, int count, int sms, uint
  * coded with schemes[i]; out[i] receives its container.  The same steps as
  * wcomp_encode run as batched launches over all tensors, with the same two
  * waits on `stream` for the whole batch (escape counts, then the scan check).
- * On failure every out[i] is NULL.
+ * The batch's containers share two pool blocks (one for their code, raw and
+ * index sections, one for their escape streams); each container is still
+ * released on its own with wcomp_free, and a block returns to the pool with
+ * the last container that uses it.  On failure every out[i] is NULL.
  * Definition: as wcomp_encode (forgeeks page, "Cómo funciona la compresión";
  * one table per tensor).
  */
@@ -246,7 +249,29 @@ WCOMP_API int wcomp_gemv_batched(const wcomp_container* const* containers, const
  */
 WCOMP_API int wcomp_device_check(void* stream);
 
-/* Describe a container (host-side, no device work). */
+/*
+ * Test hook for the bounded waits, in debug builds only (compiled with
+ * WCOMP_DEBUG=1).  While `on` is non-zero, every warp of a GEMV launch
+ * (fused or plain) leaves the first of its tensor copies unissued but still
+ * waits for it: the wait runs out after about a second, the warp stops
+ * copying and waiting, lets the copies it has in flight land and finishes,
+ * and wcomp_device_check then reports WCOMP_ETIMEOUT.  The outputs of such a
+ * launch are undefined; the context stays usable.  Applies to the current
+ * device and synchronizes it.  Release builds do nothing and return
+ * WCOMP_EUNSUPPORTED.  (Library housekeeping; the pages define no
+ * counterpart.)
+ */
+WCOMP_API int wcomp_debug_skip_first_copy(int on);
+
+/*
+ * Describe a container (host-side, no device work): shape, table, section
+ * sizes, and the bits/weight accounting of forgeeks page "Prueba de GLM-5.2
+ * reduce la memoria BF16 en casi un 25%", section "Cómo funciona la
+ * compresión" (a 4-bit code plus 8 raw bits for byte-split or 7 for K15 per
+ * weight, plus each escape and each table entry at its symbol width), next to
+ * the physical bits/weight of both serialized forms.  Returns WCOMP_EINVAL
+ * for a NULL argument.
+ */
 WCOMP_API int wcomp_info(const wcomp_container* c, wcomp_info_t* info);
 
 /*
@@ -254,7 +279,11 @@ WCOMP_API int wcomp_info(const wcomp_container* c, wcomp_info_t* info);
  * scheme, N, K, E, tile size, table, payload length, CRC-32 of the payload,
  * CRC-32 of the header) followed by the payload sections, each padded to 32
  * bytes.  With host_buf == NULL only *len is set.  Returns WCOMP_EINVAL if
- * cap is too small.  Synchronizes `stream`.
+ * cap is too small.  Synchronizes `stream`.  The pages fix no file format;
+ * this one stores every section the device container holds, so that
+ * wcomp_deserialize rebuilds it without recomputation, and carries checksums
+ * for the corruption checks of wavect page "Compresión de pesos LLM sin
+ * pérdida vs 8-bit GGUF", section "Un piloto de producción de 14 días".
  */
 WCOMP_API int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_t cap, uint64_t* len,
                     void* stream);
@@ -294,8 +323,11 @@ WCOMP_API int wcomp_deserialize(const void* host_buf, uint64_t len, void* stream
 
 /*
  * Release a container.  The device memory is returned in stream order on
- * `stream`: work queued earlier on that stream may still use it.  NULL is a
- * no-op.
+ * `stream`: work queued earlier on that stream may still use it.  Containers
+ * made by one wcomp_encode_batched call share their blocks, which return to
+ * the pool on the stream of the last wcomp_free among them: a caller that
+ * frees them on different streams orders those streams first.  NULL is a
+ * no-op.  (Library housekeeping; the pages define no counterpart.)
  */
 WCOMP_API void wcomp_free(wcomp_container* c, void* stream);
 

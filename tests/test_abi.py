@@ -107,6 +107,13 @@ def test_batched_and_remaining_argument_errors_without_gpu(lib):
     assert lib.wcomp_info(P(256), None) == wcomp.EINVAL
 
 
+def test_debug_hook_is_inert_in_the_release_build(lib):
+    # the bounded-wait test hook exists in every build but acts only in debug
+    # builds; the release library answers without touching a device
+    assert lib.wcomp_debug_skip_first_copy(1) == wcomp.EUNSUPPORTED
+    assert lib.wcomp_debug_skip_first_copy(0) == wcomp.EUNSUPPORTED
+
+
 def test_every_status_has_its_own_message(lib):
     codes = [wcomp.OK, wcomp.EINVAL, wcomp.ENOMEM, wcomp.ECORRUPT, wcomp.ECUDA, wcomp.EUNSUPPORTED, wcomp.ETIMEOUT,
              wcomp.EINTERNAL, wcomp.EBOUNDS]

@@ -9,6 +9,12 @@ plain GEMV run through that build on edge cases (every BF16 pattern, ragged
 sizes, escapes on row and tile boundaries, partial k-blocks and units,
 batches) in a child process, each checked against the oracle, and no check
 may fire.
+
+The same build also makes the GEMV kernels' bounded waits run out without a
+fault: with the skip hook on, every warp leaves its first tensor copy
+unissued and waits for it (nothing will complete that wait), gives up after
+about a second, and the launch must report WCOMP_ETIMEOUT; with the hook off
+the next launch on the same context must be correct and report nothing.
 """
 import os
 import subprocess
@@ -89,3 +95,53 @@ def test_parity_cases_under_the_debug_build():
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT, lib], capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     assert "device_check 0" in r.stdout
+
+
+TIMEOUT_CHILD = r"""
+import sys, time
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+from decode_gemv_sign_gb300 import synth, wcomp as W
+from oracle import wcomp_oracle as O
+W.LIB_PATH = sys.argv[2]
+L = W.lib()
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+w = synth.gen_weights_np(synth.WeightSpec("g", 96, 2048, "t4", 0.02, 0.02, "normal", 1.0, seed=21))
+N, K = w.shape
+assert L.wcomp_device_check(None) == W.OK
+for scheme in O.SCHEMES:
+    c = W.encode(dev(w), scheme)
+    for B in (1, 4):
+        x = synth.gen_x_np(B, K, 30 + B)
+        yr = O.gemv(w, x)
+        for plain in (False, True):
+            assert L.wcomp_debug_skip_first_copy(1) == W.OK
+            t0 = time.time()
+            y = W.gemv_bf16(dev(w), dev(x)) if plain else W.gemv(c, dev(x))
+            torch.cuda.synchronize()
+            dt = time.time() - t0
+            st = L.wcomp_device_check(None)
+            assert st == W.ETIMEOUT, (scheme, B, plain, st)
+            assert 0.5 < dt < 30, dt
+            assert L.wcomp_debug_skip_first_copy(0) == W.OK
+            y = W.gemv_bf16(dev(w), dev(x)) if plain else W.gemv(c, dev(x))
+            y = y.cpu().numpy().astype(np.float64)
+            assert L.wcomp_device_check(None) == W.OK
+            assert np.abs(y - yr).max() <= 1e-4 * np.abs(yr).max()
+            print("timed out and recovered", scheme, B, plain, round(dt, 2))
+    c.free()
+print("ok")
+"""
+
+
+def test_bounded_waits_run_out_and_report_etimeout():
+    from decode_gemv_sign_gb300 import build
+
+    lib = build.build(debug=True)
+    r = subprocess.run([sys.executable, "-c", TIMEOUT_CHILD, ROOT, lib], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert r.stdout.count("timed out and recovered") == 8 and "ok" in r.stdout
