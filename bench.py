@@ -45,38 +45,9 @@ SCHEME_NAMES = {0: "bytesplit", 1: "k15"}
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
-# ---------------------------------------------------------------------------
 # Algorithmic bytes per launch (the minimum traffic each operation implies).
-# ---------------------------------------------------------------------------
-
-
-def container_read_bytes(info: dict, part: str) -> int:
-    """Bytes a decode ("decode") or fused GEMV ("gemv") must read from a container."""
-    n_tiles_b = 4 * (info["n_tiles"] + 1)
-    rows_b = 4 * (info["N"] + 1)
-    E = info["n_escapes"]
-    val = E if info["scheme"] == 0 else 2 * E
-    streams = info["bytes_codes"] + info["bytes_raw"]
-    if part == "decode":
-        return streams + n_tiles_b + 4 * E + val
-    return streams + rows_b + 4 * E + val
-
-
-def encode_bytes(info: dict) -> int:
-    # read the source once, write the container once
-    return 2 * info["n"] + info["serialized_bytes"] - 96
-
-
-def decode_bytes(info: dict) -> int:
-    return container_read_bytes(info, "decode") + 2 * info["n"]
-
-
-def gemv_bytes(info: dict, B: int) -> int:
-    return container_read_bytes(info, "gemv") + 2 * B * info["K"] + 4 * B * info["N"]
-
-
-def plain_bytes(N: int, K: int, B: int) -> int:
-    return 2 * N * K + 2 * B * K + 4 * B * N
+from decode_gemv_sign_gb300.accounting import (container_read_bytes, decode_bytes, encode_bytes,  # noqa: E402,F401
+                                               gemv_bytes, plain_bytes)
 
 
 # ---------------------------------------------------------------------------
@@ -608,7 +579,10 @@ def run_e2e(args, W, torch, hp, specs, src_flat, dist):
     result read back.  Two device copies of the batch alternate, so step k+1's
     inputs are copied on a second stream while step k computes (the copy of
     the first timed step lies inside the timed region too)."""
-    host_src = torch.empty(src_flat.shape, dtype=src_flat.dtype).pin_memory()
+    from decode_gemv_sign_gb300.hostmem import PinnedBuffer
+
+    host_buf = PinnedBuffer(torch, src_flat.numel(), src_flat.dtype)
+    host_src = host_buf.tensor
     host_src.copy_(src_flat)
     host_x = {B: hp.xs[B].cpu().pin_memory() for B in BATCHES}
     host_y = {k: torch.empty(y.shape, dtype=y.dtype).pin_memory() for k, y in hp.yf.items()}
@@ -663,7 +637,8 @@ def run_e2e(args, W, torch, hp, specs, src_flat, dist):
     ms = allmax(dist, a.elapsed_time(b))
     step_bytes = sum(r["bytes"] for r in hp.row_bytes().values())
     v = allsum(dist, step_bytes * args.steps) / (ms / 1e3) / 1e9
-    del flat2, views2
+    del flat2, views2, host_src
+    host_buf.release()
     return {"value": round(v, 1), "unit": "GB/s", "ms_per_step": round(ms / args.steps, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "step k+1's inputs are copied on a second stream while step k computes"}

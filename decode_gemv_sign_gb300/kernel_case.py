@@ -1,17 +1,25 @@
-"""Run one library operation on one seeded workload tensor set, for profiler captures.
+"""Run one library operation on a seeded slice of the benchmark's workload, for profiler captures.
 
-    python -m decode_gemv_sign_gb300.kernel_case --op decode --scheme k15 --reps 3
-    python -m decode_gemv_sign_gb300.kernel_case --op gemv --scheme bytesplit --batch 1
+    python -m decode_gemv_sign_gb300.kernel_case --op decode --scheme both --reps 2
+    python -m decode_gemv_sign_gb300.kernel_case --op gemv --scheme k15 --batch 1 --rows 4096
 
-The inputs are the first `--tensors` tensors of the dense-layer workload (all
-seven by default: 4 x 4096x4096 and 3 x 4096x11008, 386 MB of BF16, larger
-than L2), drawn on the device; the operation runs `--reps` times after the
-containers are built, as one batched launch per repetition.  Exits non-zero if
-a decode is not bit-exact.
+Inputs, drawn on the device:
+  * encode / decode: one layer of the checkpoint-shaped set (the 17 tensors
+    that follow the two embeddings in its first 16 GiB batch: 4 x 6144x6144,
+    2 x 16384x6144, 6144x16384, 8 x 2048x6144, 2 norms; 1.1 GB of BF16, far
+    larger than L2), or the first `--tensors` of them;
+  * gemv / gemv_bf16: the first `--rows` rows of the 16384x53248 GEMV weight
+    (all of them by default; 4096 rows are 436 MB of BF16), or with
+    `--dense12` the escape-free weight of the same shape.
+The operation runs `--reps` times after the containers are built, one
+batched launch per repetition.  Exits non-zero if a decode is not bit-exact
+or a GEMV kernel reports an error.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
+import json
 import os
 import sys
 
@@ -20,23 +28,35 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def layer_specs(count: int):
+    from decode_gemv_sign_gb300 import synth
+
+    return synth.checkpoint_batch(0)[2:2 + count]
+
+
 def main():
     import torch
 
-    from decode_gemv_sign_gb300 import build, synth
+    from decode_gemv_sign_gb300 import accounting, build, synth
     from decode_gemv_sign_gb300 import wcomp as W
 
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["encode", "decode", "gemv", "gemv_bf16"], required=True)
     ap.add_argument("--scheme", choices=["bytesplit", "k15", "both"], default="bytesplit",
-                    help="both: every tensor in both schemes, one batch (the benchmark's decode launch)")
+                    help="both: every tensor in both schemes, one batch (the benchmark's encode and decode)")
     ap.add_argument("--batch", type=int, default=1)
-    ap.add_argument("--tensors", type=int, default=7)
+    ap.add_argument("--tensors", type=int, default=17)
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--dense12", action="store_true")
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args()
     build.build()
     dev = torch.device("cuda")
-    specs = synth.workload_dense_layers()[: a.tensors]
+    if a.op in ("gemv", "gemv_bf16"):
+        base = synth.dense12_spec() if a.dense12 else synth.checkpoint_gemv_spec()
+        specs = [dataclasses.replace(base, N=min(a.rows, base.N))]
+    else:
+        specs = layer_specs(a.tensors)
     ws = [synth.gen_weights_torch(s, dev) for s in specs]
     if a.scheme == "both":
         specs = [s for s in specs for _ in (0, 1)]
@@ -50,21 +70,32 @@ def main():
                 c.free()
         torch.cuda.synchronize()
         return
-    cs = W.encode_batched(ws, schemes)
     xs = [synth.gen_x_torch(a.batch, s.K, 5 + i, dev) for i, s in enumerate(specs)]
+    if a.op == "gemv_bf16":
+        for _ in range(a.reps):
+            W.gemv_bf16_batched(ws, xs)
+        torch.cuda.synchronize()
+        print(json.dumps({"op": a.op, "algorithmic_bytes_per_rep": sum(
+            accounting.plain_bytes(s.N, s.K, a.batch) for s in specs)}))
+        return
+    cs = W.encode_batched(ws, schemes)
     outs = [torch.empty_like(w) for w in ws]
     for _ in range(a.reps):
         if a.op == "decode":
             W.decode_batched(cs, outs)
-        elif a.op == "gemv":
-            W.gemv_batched(cs, xs)
         else:
-            W.gemv_bf16_batched(ws, xs)
+            W.gemv_batched(cs, xs)
     torch.cuda.synchronize()
     if a.op == "decode":
         for w, o in zip(ws, outs):
             if not torch.equal(w, o):
                 sys.exit("decode mismatch")
+    if W.lib().wcomp_device_check(None) != W.OK:
+        sys.exit("device error word set")
+    infos = [c.info() for c in cs]
+    per = [accounting.decode_bytes(i) if a.op == "decode" else accounting.gemv_bytes(i, a.batch) for i in infos]
+    print(json.dumps({"op": a.op, "algorithmic_bytes_per_rep": sum(per),
+                      "elements": sum(i["n"] for i in infos), "escapes": sum(i["n_escapes"] for i in infos)}))
 
 
 if __name__ == "__main__":

@@ -124,7 +124,10 @@ class _HostStream:
         self.torch = torch
         self.batches = batches
         elems = max(sum((s.n + 7) // 8 * 8 for s in b) for b in batches) if batches else 0
-        self.host = [torch.empty(elems, dtype=torch.int16).pin_memory() for _ in range(2)]
+        from decode_gemv_sign_gb300.hostmem import PinnedBuffer
+
+        self._bufs = [PinnedBuffer(torch, elems, torch.int16) for _ in range(2)]
+        self.host = [b.tensor for b in self._bufs]
         self.dev = [torch.empty(elems, dtype=torch.int16, device=device) for _ in range(2)]
         self.copy = torch.cuda.Stream(device=device)
         self.ready = [torch.cuda.Event(), torch.cuda.Event()]
