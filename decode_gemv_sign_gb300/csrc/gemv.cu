@@ -76,7 +76,6 @@ constexpr int kRows = 16;      // weight rows per unit (the MMA's M side)
 constexpr int kKBlock = 128;   // columns per k-block (4 lanes x 32)
 constexpr int kCtasPerSm = 2;
 constexpr int kEscDepth = 16;  // escape corrections with their loads in flight together
-constexpr int kEscQ = 2;       // escapes a thread moves along per k-block (no transposed x)
 
 enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
@@ -87,6 +86,19 @@ enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 // only the high byte and decodes from registers.
 template <int SRC>
 constexpr int lut_rep() { return SRC == kK15 ? 8 : 0; }
+
+// Escapes a correction thread moves one stage along per k-block, and the most
+// stages a warp's ring keeps, per instantiation (XW: width of the transposed
+// x, 0 = none).  Measured on a 16384 x 53248 weight: K15, with 3 % escapes,
+// gains from deeper in-loop corrections (B = 1: 2 -> 4 cut 385 to 347 us;
+// B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at B = 4) and from
+// two stages, whose smaller shared-memory share leaves more L1 to the
+// corrections' gathers; with two batch tiles (NT = 2) deeper corrections
+// spill registers.
+template <int SRC, int NT, int XW>
+constexpr int esc_q() { return SRC != kK15 ? 2 : NT == 2 ? (XW == 0 ? 2 : 1) : XW == 0 ? 4 : 2; }
+template <int SRC>
+constexpr int max_stages() { return SRC == kK15 ? 2 : 4; }
 
 // One stage of one warp in shared memory, as the tensor copies write it (row
 // r of a box at r times its row length; regions start on 1024-byte
@@ -459,13 +471,15 @@ struct SmemAt {
 };
 
 template <int SRC, int NT, int XW>
-struct Smem : SmemAt<SRC, NT, XW,
-                     SmemAt<SRC, NT, XW, 4>::kBytes <= kSmemPerCta   ? 4
-                     : SmemAt<SRC, NT, XW, 3>::kBytes <= kSmemPerCta ? 3
-                                                                       : 2> {
-  static constexpr int kStages = SmemAt<SRC, NT, XW, 4>::kBytes <= kSmemPerCta   ? 4
-                                 : SmemAt<SRC, NT, XW, 3>::kBytes <= kSmemPerCta ? 3
+constexpr int ring_stages() {
+  return max_stages<SRC>() >= 4 && SmemAt<SRC, NT, XW, 4>::kBytes <= kSmemPerCta   ? 4
+         : max_stages<SRC>() >= 3 && SmemAt<SRC, NT, XW, 3>::kBytes <= kSmemPerCta ? 3
                                                                                    : 2;
+}
+
+template <int SRC, int NT, int XW>
+struct Smem : SmemAt<SRC, NT, XW, ring_stages<SRC, NT, XW>()> {
+  static constexpr int kStages = ring_stages<SRC, NT, XW>();
   static_assert(SmemAt<SRC, NT, XW, 2>::kBytes <= kSmemPerCta, "two stages must fit");
 };
 
@@ -599,13 +613,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // (row cj, batch slot cb, part cq) owns the escapes e = ce0 + cq + j cP
       // of row cj (with the transposed x: thread (cj, part tid % 16) owns
       // e = ce0 + part + 16 j, every batch row at once).  Each k-block moves
-      // kEscQ of them one stage along: A requests the position and value, B
+      // esc_q of them one stage along: A requests the position and value, B
       // (one k-block later) gathers x (and the raw byte), C (one more k-block
       // later) accumulates, so every load has a k-block's compute to land.
       // Escapes the loop does not reach are taken after it, kEscDepth at a
       // time.
       constexpr bool kXt = XW > 0;
-      constexpr int kQ = kXt ? 1 : kEscQ;
+      constexpr int kQ = esc_q<SRC, NT, XW>();
       constexpr int kXWords = kXt ? XW / 2 : 1;
       const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
       const uint32_t e_step = kXt ? uint32_t(kThreads / 16) : uint32_t(cP);
