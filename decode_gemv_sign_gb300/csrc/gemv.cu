@@ -390,7 +390,11 @@ __device__ __forceinline__ void compute_item(const RegTable& tab, uint32_t lut, 
 
 // x of k-block kb for this lane: batch rows g (and g + 8 when NT == 2),
 // columns 32 t .. 32 t + 31; zeros for batch rows >= B and columns past K.
-template <int NT>
+// With PF, the 128-byte lines of the same columns of k-block kb + 1 are
+// prefetched into L1, so the next call finds them there (measured on a
+// 16384 x 53248 weight: byte-split B = 4 289 -> 238 us, plain 283 -> 268 us;
+// K15 and two batch tiles gain nothing).
+template <int NT, bool PF>
 __device__ __forceinline__ void load_x(const GemvBatch& p, const Unit& m, uint32_t kb, int B, int lane,
                                        uint4 (&xv)[NT][4]) {
   const int g = lane >> 2, t = lane & 3;
@@ -404,6 +408,8 @@ __device__ __forceinline__ void load_x(const GemvBatch& p, const Unit& m, uint32
       const uint16_t* xr = p.x[m.ti] + int64_t(b) * K + int64_t(kb) * kKBlock + 32 * t;
 #pragma unroll
       for (int i = 0; i < 4; ++i) xv[nt][i] = ld_x_v4(xr + 8 * i);
+      if (PF && (t & 1) == 0 && int64_t(kb + 1) * kKBlock + 32 * t + 64 <= K)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(xr + kKBlock));
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) xv[nt][i] = make_uint4(0u, 0u, 0u, 0u);
@@ -704,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         while (!aborted && issued < done + kStages && issue_next()) {
         }
         uint4 xv[NT][4];
-        load_x<NT>(p, cur, kb, B, lane, xv);
+        load_x<NT, SRC != kK15 && NT == 1>(p, cur, kb, B, lane, xv);
         const uint32_t sidx = done % kStages;
         if (!aborted && __any_sync(0xffffffffu, !mbar_wait_bounded(bars + 8 * sidx, (done / kStages) & 1))) {
           aborted = true;  // the warp stops copying and waiting, and still runs the same instructions
