@@ -525,13 +525,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t lut = base_u32 + pad + S::kLutOff + uint32_t(lane % (kRep ? kRep : 1)) * 4;
   // the code-pair table of tensor ti, every thread writing its share
   auto build_lut = [&](int ti) {
-    if (!kRep) return;
-    const RegTable& t = p.d[ti].t;
-    for (uint32_t i = threadIdx.x; i < 256u * kRep; i += kThreads) {
-      const uint32_t v = i / kRep, c0 = v & 15, c1 = v >> 4;
-      const uint32_t h0 = (t.hi[c0 >> 2] >> (8 * (c0 & 3))) & 0xFF, e0 = (t.e0[c0 >> 2] >> (8 * (c0 & 3))) & 0x80;
-      const uint32_t h1 = (t.hi[c1 >> 2] >> (8 * (c1 & 3))) & 0xFF, e1 = (t.e0[c1 >> 2] >> (8 * (c1 & 3))) & 0x80;
-      lut_w[i] = e0 | (h0 << 8) | (e1 << 16) | (h1 << 24);
+    if constexpr (kRep > 0) {
+      const RegTable& t = p.d[ti].t;
+      for (uint32_t i = threadIdx.x; i < 256u * kRep; i += kThreads) {
+        const uint32_t v = i / kRep, c0 = v & 15, c1 = v >> 4;
+        const uint32_t h0 = (t.hi[c0 >> 2] >> (8 * (c0 & 3))) & 0xFF, e0 = (t.e0[c0 >> 2] >> (8 * (c0 & 3))) & 0x80;
+        const uint32_t h1 = (t.hi[c1 >> 2] >> (8 * (c1 & 3))) & 0xFF, e1 = (t.e0[c1 >> 2] >> (8 * (c1 & 3))) & 0x80;
+        lut_w[i] = e0 | (h0 << 8) | (e1 << 16) | (h1 << 24);
+      }
     }
   };
   if (first_unit < total_units) {
@@ -646,16 +647,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       // stage A: request positions and values of the next kQ escapes
       auto esc_request = [&]() {
-        okA = 0;
+        if constexpr (SRC != kPlain) {
+          okA = 0;
 #pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-          const uint32_t i = e_next + q * e_step;
-          const bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
-          okA |= uint32_t(ok) << q;
-          posA[q] = ok ? d.esc_pos[i] : uint32_t(rowbase);
-          valA[q] = ok ? load_esc_val(d, i) : 0u;  // value 0 and x 0: contributes exactly 0
+          for (int q = 0; q < kQ; ++q) {
+            const uint32_t i = e_next + q * e_step;
+            const bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
+            okA |= uint32_t(ok) << q;
+            posA[q] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+            valA[q] = ok ? load_esc_val(d, i) : 0u;  // value 0 and x 0: contributes exactly 0
+          }
+          e_next += kQ * e_step;
         }
-        e_next += kQ * e_step;
       };
       // stage C then B: accumulate the gathered escapes, gather the requested ones
       auto esc_advance = [&]() {
