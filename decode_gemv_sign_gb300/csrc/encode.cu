@@ -64,11 +64,20 @@ struct ZeroList {
   int count;
 };
 
-__device__ __forceinline__ int find_owner(const EncBatch& b, uint32_t x) {
-  int i = 0;
-  while (i + 1 < b.count && b.prefix[i + 1] <= x) ++i;
-  return i;
+// The last of entries 0 .. count - 1 whose prefix is at most x (binary search).
+__device__ __forceinline__ int owner_in(const uint32_t* prefix, int count, uint32_t x) {
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
 }
+
+__device__ __forceinline__ int find_owner(const EncBatch& b, uint32_t x) { return owner_in(b.prefix, b.count, x); }
 
 // Zero small byte ranges (section padding, histogram scratch); one CTA per range.
 __global__ void __launch_bounds__(256) zero_kernel(const __grid_constant__ ZeroList z) {
@@ -254,6 +263,12 @@ __device__ __forceinline__ void group_codes(const uint8_t* lut, const uint32_t (
   }
 }
 
+// Bit 4j + 3 set where nibble j of c is 15: its low three bits plus one carry
+// into bit 3, which must also be set.
+__device__ __forceinline__ uint32_t nibbles15(uint32_t c) {
+  return ((c & 0x77777777u) + 0x11111111u) & c & 0x88888888u;
+}
+
 // Codes in cw are given; clears codes past n, writes the group's sections
 // and returns its escape count.
 template <int SCHEME>
@@ -271,10 +286,7 @@ __device__ __forceinline__ uint32_t pack_group(const EncDesc& d, uint64_t g, con
   }
   uint32_t esc = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t c = cw[k];
-    esc += __popc(c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u);
-  }
+  for (int k = 0; k < 4; ++k) esc += __popc(nibbles15(cw[k]));
   uint8_t* m = d.main;
   *reinterpret_cast<uint4*>(m + d.off_codes + 16 * g) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   if (SCHEME == WCOMP_BYTESPLIT) {
@@ -308,8 +320,7 @@ __device__ __forceinline__ void stash_group(const EncDesc& d, uint32_t tile, uin
   const uint64_t base = g * kGroup;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t c = cw[k];
-    uint32_t m = c & (c >> 1) & (c >> 2) & (c >> 3) & 0x11111111u;
+    uint32_t m = nibbles15(cw[k]);
     while (m) {
       const int j = (__ffs(m) - 1) >> 2;
       m &= m - 1;
@@ -365,8 +376,7 @@ __global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_consta
   // nibble, so one lookup per element gives both codes
   __shared__ uint8_t lut2[512];
   __shared__ uint32_t red[kThreads / 32];
-  int pi = 0;
-  while (2 * (pi + 1) < bt.count && bt.prefix[pi + 1] <= blockIdx.x) ++pi;
+  const int pi = owner_in(bt.prefix, bt.count / 2, blockIdx.x);
   const EncDesc& d0 = bt.d[2 * pi];
   const EncDesc& d1 = bt.d[2 * pi + 1];
   const uint32_t tile = blockIdx.x - bt.prefix[pi];
@@ -385,11 +395,22 @@ __global__ void __launch_bounds__(kThreads) pack_twin_kernel(const __grid_consta
 #pragma unroll
     for (int q = 0; q < 8; ++q) lo[q] = prmt(wv[2 * q], wv[2 * q + 1], 0x6420);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t c0 = lut2[(wv[k] >> 7) & 511u], c1 = lut2[wv[k] >> 23];
-      const uint32_t pair = c0 | (c1 << 8);  // K15 codes in bits 0-3 and 8-11, byte-split in 4-7 and 12-15
-      cw1[k >> 2] += ((pair & 0xFu) | ((pair >> 4) & 0xF0u)) << (8 * (k & 3));
-      cw0[k >> 2] += (((pair >> 4) & 0xFu) | ((pair >> 8) & 0xF0u)) << (8 * (k & 3));
+    for (int i = 0; i < 4; ++i) {
+      // table bytes of elements 8i .. 8i + 7, four to a word (byte lane = element)
+      uint32_t T[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = wv[4 * i + 2 * h], w1 = wv[4 * i + 2 * h + 1];
+        const uint32_t b0 = lut2[(w0 >> 7) & 511u], b1 = lut2[w0 >> 23];
+        const uint32_t b2 = lut2[(w1 >> 7) & 511u], b3 = lut2[w1 >> 23];
+        T[h] = prmt(prmt(b0, b1, 0x0040u), prmt(b2, b3, 0x0040u), 0x5410u);
+      }
+      // code word: byte j = element 2j | element 2j + 1 << 4.  K15 codes are
+      // the low nibbles of the table bytes, byte-split codes the high nibbles.
+      const uint32_t k0 = T[0] & 0x0F0F0F0Fu, k1 = T[1] & 0x0F0F0F0Fu;
+      const uint32_t s0 = (T[0] >> 4) & 0x0F0F0F0Fu, s1 = (T[1] >> 4) & 0x0F0F0F0Fu;
+      cw1[i] = prmt(k0 | (k0 >> 4), k1 | (k1 >> 4), 0x6420u);
+      cw0[i] = prmt(s0 | (s0 >> 4), s1 | (s1 >> 4), 0x6420u);
     }
     esc = pack_group<WCOMP_BYTESPLIT>(d0, g, lo, cw0);
     esc |= pack_group<WCOMP_K15>(d1, g, lo, cw1) << 16;
