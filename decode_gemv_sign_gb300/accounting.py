@@ -3,9 +3,9 @@
 Byte counts from a container's description (wcomp_info as a dict): the code
 stream, the raw low bytes or K15 mantissa planes, the escape index the
 operation uses (per tile for decode, per row for the GEMV), the escape
-positions (4 bytes) and values (1 byte for byte-split, 2 for K15), plus what
-the operation writes (decode: 2 bytes per element; GEMV: x read once, y
-written as fp32).  These are the numerators of the roofline fractions.
+positions (4 bytes) and values (the whole 16-bit word, as the device
+container keeps them for both schemes), plus what the operation writes
+(decode: 2 bytes per element; GEMV: x read once, y written as fp32).  These are the numerators of the roofline fractions.
 """
 
 
@@ -14,7 +14,7 @@ def container_read_bytes(info: dict, part: str) -> int:
     n_tiles_b = 4 * (info["n_tiles"] + 1)
     rows_b = 4 * (info["N"] + 1)
     E = info["n_escapes"]
-    val = E if info["scheme"] == 0 else 2 * E
+    val = 2 * E
     streams = info["bytes_codes"] + info["bytes_raw"]
     if part == "decode":
         return streams + n_tiles_b + 4 * E + val

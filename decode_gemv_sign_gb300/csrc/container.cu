@@ -192,11 +192,22 @@ extern "C" int wcomp_serialize(const wcomp_container* c, void* host_buf, uint64_
   if (cap < L.serialized()) return WCOMP_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* out = static_cast<uint8_t*>(host_buf);
+  uint8_t* esc = out + kHeaderBytes + L.main_payload;
+  // the device keeps whole escape words; version 1 stores byte-split values
+  // as the high byte
+  std::vector<uint16_t> words(L.scheme == WCOMP_BYTESPLIT ? L.E : 0);
   cudaError_t e = cudaMemcpyAsync(out + kHeaderBytes, c->d_main, L.main_payload, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && L.esc_payload)
-    e = cudaMemcpyAsync(out + kHeaderBytes + L.main_payload, c->d_esc, L.esc_payload, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && L.E) {
+    memset(esc, 0, L.esc_payload);
+    e = cudaMemcpyAsync(esc + L.off_pos, c->d_esc + L.off_pos, L.sz_pos, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = L.scheme == WCOMP_BYTESPLIT
+              ? cudaMemcpyAsync(words.data(), c->d_esc + L.off_val, 2 * L.E, cudaMemcpyDeviceToHost, s)
+              : cudaMemcpyAsync(esc + L.off_val, c->d_esc + L.off_val, L.sz_val, cudaMemcpyDeviceToHost, s);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return map_cuda(e);
+  for (uint64_t r = 0; r < words.size(); ++r) esc[L.off_val + r] = uint8_t(words[r] >> 8);
   uint32_t crc = crc32_update(0, out + kHeaderBytes, L.main_payload + L.esc_payload);
   write_header(c, WCOMP_VERSION, L.main_payload + L.esc_payload, crc, out);
   return WCOMP_OK;
@@ -215,13 +226,13 @@ extern "C" int wcomp_serialize_compact(const wcomp_container* c, void* host_buf,
   uint8_t* out = static_cast<uint8_t*>(host_buf);
   uint8_t* p = out + kHeaderBytes;
   std::vector<uint32_t> tile(L.n_tiles + 1);
-  std::vector<uint8_t> val(L.sz_val);
+  std::vector<uint16_t> val(L.E);  // whole escape words
   // codes and raw bytes / planes in one copy (same offsets in both forms)
   cudaError_t e = cudaMemcpyAsync(p, c->d_main, L.off_tile, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(tile.data(), c->d_main + L.off_tile, L.sz_tile, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && L.E)
-    e = cudaMemcpyAsync(val.data(), c->d_esc + L.off_val, L.sz_val, cudaMemcpyDeviceToHost, s);
+    e = cudaMemcpyAsync(val.data(), c->d_esc + L.off_val, 2 * L.E, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return map_cuda(e);
   uint8_t* tc = p + C.off_tilecount;
@@ -230,10 +241,10 @@ extern "C" int wcomp_serialize_compact(const wcomp_container* c, void* host_buf,
   uint8_t* sym = p + C.off_sym;
   memset(sym, 0, padsec(C.sz_sym));
   if (L.scheme == WCOMP_BYTESPLIT) {
-    if (L.E) memcpy(sym, val.data(), L.E);
+    for (uint64_t r = 0; r < L.E; ++r) sym[r] = uint8_t(val[r] >> 8);  // the high byte
   } else {
     for (uint64_t r = 0; r < L.E; ++r) {
-      const uint32_t v = uint32_t(get16(val.data() + 2 * r)) >> 7;  // the 9-bit symbol
+      const uint32_t v = uint32_t(val[r]) >> 7;  // the 9-bit symbol
       const uint64_t bit = 9 * r;
       const uint32_t w = v << (bit & 7);
       sym[bit >> 3] |= uint8_t(w);
@@ -408,11 +419,25 @@ extern "C" int wcomp_deserialize(const void* host_buf, uint64_t len, void* strea
   c->L = L;
   memcpy(c->table, table, sizeof(table));
   cudaGetDevice(&c->device);
+  // the device escape section: positions, then whole 16-bit words (a
+  // byte-split value joins its high byte with the element's raw low byte)
+  std::vector<uint8_t> dev_esc(L.E ? L.esc_alloc : 0, 0);
+  if (L.E) {
+    memcpy(dev_esc.data() + L.off_pos, esc_src + L.off_pos, L.sz_pos);
+    uint8_t* w = dev_esc.data() + L.off_val;
+    const uint8_t* v = esc_src + L.off_val;
+    if (L.scheme == WCOMP_BYTESPLIT) {
+      const uint8_t* raw = main_src + L.off_raw;
+      for (uint64_t r = 0; r < L.E; ++r) put16(w + 2 * r, uint16_t((uint32_t(v[r]) << 8) | raw[get32(esc_src + L.off_pos + 4 * r)]));
+    } else {
+      memcpy(w, v, 2 * L.E);
+    }
+  }
   cudaError_t e = pool_alloc(reinterpret_cast<void**>(&c->d_main), L.main_alloc, s);
-  if (e == cudaSuccess && L.esc_payload) e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_payload, s);
+  if (e == cudaSuccess && L.E) e = pool_alloc(reinterpret_cast<void**>(&c->d_esc), L.esc_alloc, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_main, main_src, L.main_payload, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && L.esc_payload)
-    e = cudaMemcpyAsync(c->d_esc, esc_src, L.esc_payload, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && L.E)
+    e = cudaMemcpyAsync(c->d_esc, dev_esc.data(), L.esc_alloc, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     wcomp_free(c, stream);

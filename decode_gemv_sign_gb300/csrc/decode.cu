@@ -50,10 +50,7 @@ __device__ __forceinline__ void decode_tile(const TensorDesc& d, uint16_t* __res
     if (!WCOMP_DCHECK(e < d.E, 0)) continue;
     const uint32_t p = d.esc_pos[e];
     if (!WCOMP_DCHECK(p < d.n && p / kTile == tile, 0)) continue;
-    if (SCHEME == WCOMP_BYTESPLIT)
-      reinterpret_cast<uint8_t*>(out)[2 * uint64_t(p) + 1] = d.esc_val[e];  // high byte only
-    else
-      out[p] = reinterpret_cast<const uint16_t*>(d.esc_val)[e];
+    out[p] = d.esc_val[e];  // the whole word
   }
 }
 

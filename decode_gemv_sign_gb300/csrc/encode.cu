@@ -329,7 +329,7 @@ __device__ __forceinline__ void stash_group(const EncDesc& d, uint32_t tile, uin
       const uint32_t v = (pw >> (16 * (j & 1))) & 0xFFFF;
       if (!WCOMP_DCHECK(o < uint64_t(tile + 1) * d.stash_cap && o < uint64_t(d.n_tiles) * d.stash_cap, 3)) break;
       d.stash_pos[o] = uint32_t(base + 8 * k + j);
-      d.stash_val[o] = uint16_t(SCHEME == WCOMP_BYTESPLIT ? (v >> 8) : v);
+      d.stash_val[o] = uint16_t(v);  // the whole word (the device keeps whole escape words)
       ++o;
     }
   }
@@ -481,12 +481,11 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
   __shared__ uint32_t overflow;
   const int ti = find_owner(bt, blockIdx.x);
   const EncDesc& d = bt.d[ti];
-  const int SCHEME = d.scheme;
   const uint32_t t0 = (blockIdx.x - bt.prefix[ti]) * kCompactTiles;
   const uint32_t nt = min(kCompactTiles, d.n_tiles - t0);
   const uint32_t* tile_index = reinterpret_cast<const uint32_t*>(d.main + d.off_tile);
   uint32_t* pos = reinterpret_cast<uint32_t*>(d.esc + d.off_pos);
-  uint8_t* val = d.esc + d.off_val;
+  uint16_t* val = reinterpret_cast<uint16_t*>(d.esc + d.off_val);
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) overflow = 0;
   __syncthreads();
@@ -513,10 +512,7 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
           const uint32_t i = i0 + 32 * k + lane;
           if (i < count && first + i < d.E) {  // a count that disagrees with E is reported by the host
             pos[first + i] = p[k];
-            if (SCHEME == WCOMP_BYTESPLIT)
-              val[first + i] = uint8_t(v[k]);
-            else
-              reinterpret_cast<uint16_t*>(val)[first + i] = uint16_t(v[k]);
+            val[first + i] = uint16_t(v[k]);
           }
         }
       }
@@ -543,12 +539,8 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const __grid_constant
         if (((cw[e >> 3] >> (4 * (e & 7))) & 0xF) == kEscape && o < d.E) {
           const uint32_t p = uint32_t(base + e);
           if (!WCOMP_DCHECK(p < d.n, 3)) break;
-          const uint32_t v = d.w[p];
           pos[o] = p;
-          if (SCHEME == WCOMP_BYTESPLIT)
-            val[o] = uint8_t(v >> 8);
-          else
-            reinterpret_cast<uint16_t*>(val)[o] = uint16_t(v);
+          val[o] = d.w[p];
           ++o;
         }
       }
@@ -905,7 +897,7 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
   for (int i = 0; i < count; ++i) {
     Layout L = jobs[i].c->L;
     L.compute(L.scheme, L.N, L.K, hs[i].E);
-    if (L.E) esc_total += (L.esc_payload + 255) & ~uint64_t(255);
+    if (L.E) esc_total += (L.esc_alloc + 255) & ~uint64_t(255);
   }
   Arena* esc_arena = nullptr;
   if (esc_total) {
@@ -931,10 +923,10 @@ int encode_many(const uint16_t* const* ws, const int64_t* Ns, const int64_t* Ks,
       c->esc_arena = esc_arena;
       esc_arena->refs.fetch_add(1, std::memory_order_relaxed);
       c->d_esc = static_cast<uint8_t*>(esc_arena->block) + esc_off;
-      esc_off += (L.esc_payload + 255) & ~uint64_t(255);
+      esc_off += (L.esc_alloc + 255) & ~uint64_t(255);
       d.esc = c->d_esc;
       add_pad(z, c->d_esc, L.off_pos, L.sz_pos);
-      add_pad(z, c->d_esc, L.off_val, L.sz_val);
+      add_pad(z, c->d_esc, L.off_val, 2 * L.E);
       if (z.count + 2 > kMaxZero && (e = launch_zero(z, s)) != cudaSuccess) return fail3(e);
     }
   }

@@ -123,24 +123,15 @@ __device__ __forceinline__ int owner(const uint32_t* prefix, int count, uint32_t
   return i;
 }
 
-__device__ __forceinline__ uint32_t load_esc_val(const TensorDesc& d, uint32_t e) {
-  return d.scheme == WCOMP_BYTESPLIT ? uint32_t(d.esc_val[e]) : uint32_t(reinterpret_cast<const uint16_t*>(d.esc_val)[e]);
-}
+__device__ __forceinline__ uint32_t load_esc_val(const TensorDesc& d, uint32_t e) { return d.esc_val[e]; }
 
-// x * (w_true - w_placeholder) for one escape: `lo` is the placeholder's low
-// byte (byte-split; the escape value holds the high byte) and `val` the
-// escape value (the whole word for K15).
+// w_true - w_placeholder for one escape whose whole word is `val`: the
+// placeholder keeps the element's own low bits (byte-split: the raw low byte;
+// K15: the 7-bit mantissa) under symbol 0.
 template <int SCHEME>
-__device__ __forceinline__ float esc_delta(uint32_t val, uint32_t lo) {
-  uint32_t wt, wph;
-  if (SCHEME == WCOMP_BYTESPLIT) {
-    wph = lo;
-    wt = (val << 8) | lo;
-  } else {
-    wt = val;
-    wph = val & 0x7Fu;
-  }
-  return __uint_as_float(wt << 16) - __uint_as_float(wph << 16);
+__device__ __forceinline__ float esc_delta(uint32_t val) {
+  const uint32_t wph = val & (SCHEME == WCOMP_BYTESPLIT ? 0xFFu : 0x7Fu);
+  return __uint_as_float(val << 16) - __uint_as_float(wph << 16);
 }
 
 __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
@@ -600,11 +591,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const TensorDesc& dm = p.d[m.ti];
       const uint64_t e0 = dm.row_index[m.r0], e1 = dm.row_index[m.r0 + m.rows];
       if (e0 == e1) return;
-      const uint32_t vb = SRC == kBytesplit ? 1 : 2;
+      const uint32_t vb = 2;  // bytes per escape value
       const uint64_t plo = (4 * e0) & ~uint64_t(15), phi = (4 * e1 + 15) & ~uint64_t(15);
       const uint64_t vlo = (vb * e0) & ~uint64_t(15), vhi = (vb * e1 + 15) & ~uint64_t(15);
       prefetch_l2(reinterpret_cast<const uint8_t*>(dm.esc_pos) + plo, uint32_t(phi - plo));
-      prefetch_l2(dm.esc_val + vlo, uint32_t(vhi - vlo));
+      prefetch_l2(reinterpret_cast<const uint8_t*>(dm.esc_val) + vlo, uint32_t(vhi - vlo));
     };
     prefetch_escapes(cur);
     if (have_next) prefetch_escapes(nxt);
@@ -621,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // of row cj (with the transposed x: thread (cj, part tid % 16) owns
       // e = ce0 + part + 16 j, every batch row at once).  Each k-block moves
       // esc_q of them one stage along: A requests the position and value, B
-      // (one k-block later) gathers x (and the raw byte), C (one more k-block
+      // (one k-block later) gathers x, C (one more k-block
       // later) accumulates, so every load has a k-block's compute to land.
       // Escapes the loop does not reach are taken after it, kEscDepth at a
       // time.
@@ -634,14 +625,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t e_end = SRC != kPlain && cj < cur.rows && (kXt || cb < B) ? ce1 : 0;
       const uint16_t* xrow = kXt ? xt.p[cur.ti] : p.x[cur.ti] + int64_t(cb) * d.K;
       uint32_t posA[kQ], valA[kQ], okA = 0, okB = 0;  // stage masks: entries requested / gathered
-      uint32_t xB[kQ][kXWords], loB[kQ], valB[kQ];
+      uint32_t xB[kQ][kXWords], valB[kQ];
       float c = 0.f, cs[kXt ? XW : 1];
 #pragma unroll
       for (int b = 0; b < (kXt ? XW : 1); ++b) cs[b] = 0.f;
 #pragma unroll
       for (int q = 0; q < kQ; ++q) {
         posA[q] = uint32_t(rowbase);
-        valA[q] = loB[q] = valB[q] = 0u;
+        valA[q] = valB[q] = 0u;
 #pragma unroll
         for (int w = 0; w < kXWords; ++w) xB[q][w] = 0u;
       }
@@ -667,14 +658,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int q = 0; q < kQ; ++q) {
             if constexpr (kXt) {
-              const float delta = esc_delta<WCOMP_K15>(valB[q], 0u);
+              const float delta = esc_delta<WCOMP_K15>(valB[q]);
 #pragma unroll
               for (int h = 0; h < kXWords; ++h) {
                 cs[2 * h] = fmaf(bf16_lo(xB[q][h]), delta, cs[2 * h]);
                 cs[2 * h + 1] = fmaf(bf16_hi(xB[q][h]), delta, cs[2 * h + 1]);
               }
             } else {
-              c = fmaf(__uint_as_float(xB[q][0] << 16), esc_delta<SRC>(valB[q], loB[q]), c);
+              c = fmaf(__uint_as_float(xB[q][0] << 16), esc_delta<SRC>(valB[q]), c);
             }
           }
 #pragma unroll
@@ -682,7 +673,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint64_t k = uint64_t(posA[q]) - rowbase;
             const bool ok = ((okA >> q) & 1) && WCOMP_DCHECK(k < uint64_t(d.K), 1);
             valB[q] = ok ? valA[q] : 0u;
-            loB[q] = SRC == kBytesplit && ok ? uint32_t(d.raw[posA[q]]) : 0u;
             if constexpr (kXt) {
               const uint16_t* xr = xrow + k * XW;
               if (XW == 4) {
@@ -778,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               }
 #pragma unroll
               for (int v = 0; v < D; ++v) {
-                const float delta = esc_delta<WCOMP_K15>(val[v], 0u);
+                const float delta = esc_delta<WCOMP_K15>(val[v]);
 #pragma unroll
                 for (int h = 0; h < XW / 2; ++h) {
                   cs[2 * h] = fmaf(bf16_lo(wv[v][h]), delta, cs[2 * h]);
@@ -798,10 +788,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
         } else {
           // kEscDepth escapes at a time, all their loads in flight together
-          // (positions and values, then the x and raw-byte gathers); entries
-          // past the row's last escape contribute exactly zero
+          // (positions and values, then the x gathers); entries past the row's
+          // last escape contribute exactly zero
           for (uint32_t e = e_next; e < e_end; e += kEscDepth * e_step) {
-            uint32_t pos[kEscDepth], val[kEscDepth], lo[kEscDepth], xw[kEscDepth], okm = 0;
+            uint32_t pos[kEscDepth], val[kEscDepth], xw[kEscDepth], okm = 0;
 #pragma unroll
             for (int v = 0; v < kEscDepth; ++v) {
               const uint32_t i = e + v * e_step;
@@ -814,12 +804,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
             for (int v = 0; v < kEscDepth; ++v) {
               const bool ok = (okm >> v) & 1;
-              lo[v] = SRC == kBytesplit && ok ? uint32_t(d.raw[pos[v]]) : 0u;
               xw[v] = ok ? uint32_t(xrow[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
             }
 #pragma unroll
             for (int v = 0; v < kEscDepth; ++v)
-              c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v], lo[v]), c);
+              c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v]), c);
           }
           corr[par * kThreads + threadIdx.x] = c;
         }
@@ -909,8 +898,7 @@ __device__ __forceinline__ void warp_reduce_store(float (&s)[BT], int B, float* 
 template <int BT>
 __device__ __forceinline__ void add_escape(const TensorDesc& d, const uint16_t* __restrict__ x, int B, uint64_t rowbase,
                                            uint32_t p, uint32_t val, float (&s)[BT]) {
-  const float delta = d.scheme == WCOMP_BYTESPLIT ? esc_delta<WCOMP_BYTESPLIT>(val, d.raw[p])
-                                                  : esc_delta<WCOMP_K15>(val, 0u);
+  const float delta = d.scheme == WCOMP_BYTESPLIT ? esc_delta<WCOMP_BYTESPLIT>(val) : esc_delta<WCOMP_K15>(val);
   const int64_t k = int64_t(uint64_t(p) - rowbase);
 #pragma unroll
   for (int b = 0; b < BT; ++b)

@@ -38,6 +38,10 @@ struct Layout {
   uint64_t off_scratch;    // encoder scratch (not serialized)
   uint64_t main_alloc;
   uint64_t off_pos, off_val, esc_payload;
+  // On the device every escape value is the whole 16-bit word (byte-split's
+  // low byte repeats the raw byte), so no kernel re-reads the raw stream for
+  // an escape; the serialized form keeps byte-split values as the high byte.
+  uint64_t esc_alloc;
 
   void compute(int scheme_, int64_t N_, int64_t K_, uint64_t E_) {
     scheme = scheme_;
@@ -70,6 +74,7 @@ struct Layout {
     off_pos = 0;
     off_val = padsec(sz_pos);
     esc_payload = padsec(sz_pos) + padsec(sz_val);
+    esc_alloc = padsec(sz_pos) + padsec(2 * E);
   }
   uint64_t serialized() const { return kHeaderBytes + main_payload + esc_payload; }
 };
@@ -140,7 +145,7 @@ struct TensorDesc {
   const uint32_t* tile_index;
   const uint32_t* row_index;
   const uint32_t* esc_pos;
-  const uint8_t* esc_val;  // uint8 (byte-split) or uint16 (K15) entries
+  const uint16_t* esc_val;  // whole 16-bit words of the escaped elements
   uint64_t n;
   uint64_t E;              // escapes
   int64_t N, K;
@@ -160,7 +165,7 @@ inline TensorDesc make_desc(const wcomp_container* c) {
   d.tile_index = reinterpret_cast<const uint32_t*>(c->d_main + L.off_tile);
   d.row_index = reinterpret_cast<const uint32_t*>(c->d_main + L.off_row);
   d.esc_pos = reinterpret_cast<const uint32_t*>(c->d_esc + L.off_pos);
-  d.esc_val = c->d_esc + L.off_val;
+  d.esc_val = reinterpret_cast<const uint16_t*>(c->d_esc + L.off_val);
   d.n = L.n;
   d.E = L.E;
   d.N = L.N;
@@ -355,11 +360,6 @@ __device__ __forceinline__ uint32_t decode_elem_placeholder(const TensorDesc& d,
   return (hi << 8) | lo;
 }
 
-// Value of escape entry e (exact BF16 bits), given the raw byte when byte-split.
-__device__ __forceinline__ uint32_t escape_word(const TensorDesc& d, uint32_t e, uint32_t pos) {
-  if (d.scheme == WCOMP_BYTESPLIT) return (uint32_t(d.esc_val[e]) << 8) | d.raw[pos];
-  return reinterpret_cast<const uint16_t*>(d.esc_val)[e];
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
