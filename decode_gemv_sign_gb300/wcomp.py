@@ -139,9 +139,10 @@ def _bits16(t: torch.Tensor, what: str) -> torch.Tensor:
 class Container:
     """An encoded tensor living on the GPU (owned by the library)."""
 
-    def __init__(self, handle: int):
+    def __init__(self, handle: int, shape=None):
         self._h = handle
         self._info = None
+        self._shape = tuple(shape) if shape is not None else None  # (N, K) when the caller knows it
 
     @property
     def handle(self) -> int:
@@ -157,12 +158,20 @@ class Container:
         return self._info
 
     @property
+    def shape(self) -> tuple:
+        """(N, K), without a description call when the shape is known from the encode."""
+        if self._shape is None:
+            inf = self.info()
+            self._shape = (inf["N"], inf["K"])
+        return self._shape
+
+    @property
     def N(self) -> int:
-        return self.info()["N"]
+        return self.shape[0]
 
     @property
     def K(self) -> int:
-        return self.info()["K"]
+        return self.shape[1]
 
     @property
     def scheme(self) -> int:
@@ -190,7 +199,7 @@ def encode(w: torch.Tensor, scheme, stream=None) -> Container:
     h = P()
     _check(lib().wcomp_encode(P(w.data_ptr()), N, K, SCHEMES[scheme], P(_stream(stream)), ctypes.byref(h)),
            "wcomp_encode")
-    return Container(h.value)
+    return Container(h.value, (N, K))
 
 
 def encode_batched(ws: Sequence[torch.Tensor], schemes, stream=None) -> List[Container]:
@@ -212,7 +221,7 @@ def encode_batched(ws: Sequence[torch.Tensor], schemes, stream=None) -> List[Con
     _check(lib().wcomp_encode_batched(_ptr_array([w.data_ptr() for w in ws]), (ctypes.c_int64 * n)(*Ns),
                                       (ctypes.c_int64 * n)(*Ks), (ctypes.c_int * n)(*[SCHEMES[x] for x in schemes]),
                                       n, P(_stream(stream)), outs), "wcomp_encode_batched")
-    return [Container(outs[i]) for i in range(n)]
+    return [Container(outs[i], (Ns[i], Ks[i])) for i in range(n)]
 
 
 def decode(c: Container, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -230,13 +239,13 @@ def decode(c: Container, out: Optional[torch.Tensor] = None, stream=None) -> tor
 def gemv(c: Container, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """y[B, N] (fp32) = x[B, K] @ W.T with W decoded in registers."""
     x = _bits16(x, "x")
-    inf = c.info()
+    N, K = c.shape
     B = x.shape[0] if x.dim() == 2 else 1
-    if x.numel() != B * inf["K"]:
+    if x.numel() != B * K:
         raise ValueError("x has the wrong size")
     if y is None:
-        y = torch.empty((B, inf["N"]), dtype=torch.float32, device="cuda")
-    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * inf["N"]:
+        y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * N:
         raise ValueError("y must be a contiguous float32 tensor of B*N elements")
     _check(lib().wcomp_gemv(P(c.handle), P(x.data_ptr()), B, P(y.data_ptr()), P(_stream(stream))), "wcomp_gemv")
     return y
@@ -313,7 +322,8 @@ def decode_batched(cs: Sequence[Container], outs: Optional[List[torch.Tensor]] =
         outs = [torch.empty((c.N, c.K), dtype=torch.int16, device="cuda") for c in cs]
     for c, o in zip(cs, outs):
         _bits16(o, "out")
-        if o.numel() != c.info()["n"]:
+        N, K = c.shape
+        if o.numel() != N * K:
             raise ValueError("output has the wrong size")
     _check(lib().wcomp_decode_batched(_ptr_array([c.handle for c in cs]), _ptr_array([o.data_ptr() for o in outs]),
                                       len(cs), P(_stream(stream))), "wcomp_decode_batched")
