@@ -591,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const TensorDesc& dm = p.d[m.ti];
       const uint64_t e0 = dm.row_index[m.r0], e1 = dm.row_index[m.r0 + m.rows];
       if (e0 == e1) return;
+      // the ranges end inside the padded position and value sections
+      if (!WCOMP_DCHECK(e0 < e1 && e1 <= dm.E, 1)) return;
       const uint32_t vb = 2;  // bytes per escape value
       const uint64_t plo = (4 * e0) & ~uint64_t(15), phi = (4 * e1 + 15) & ~uint64_t(15);
       const uint64_t vlo = (vb * e0) & ~uint64_t(15), vhi = (vb * e1 + 15) & ~uint64_t(15);

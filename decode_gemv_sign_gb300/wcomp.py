@@ -260,11 +260,11 @@ def gemv_noalloc(c: Container, x: torch.Tensor, y: torch.Tensor, stream=None) ->
     array: do not let two of them run at the same time on different streams.
     """
     x = _bits16(x, "x")
-    inf = c.info()
+    N, K = c.shape
     B = x.shape[0] if x.dim() == 2 else 1
-    if x.numel() != B * inf["K"]:
+    if x.numel() != B * K:
         raise ValueError("x has the wrong size")
-    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * inf["N"]:
+    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != B * N:
         raise ValueError("y must be a contiguous float32 tensor of B*N elements")
     _check(lib().wcomp_gemv_noalloc(P(c.handle), P(x.data_ptr()), B, P(y.data_ptr()), P(_stream(stream))),
            "wcomp_gemv_noalloc")
