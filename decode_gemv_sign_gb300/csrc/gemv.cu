@@ -19,7 +19,8 @@
 // Work unit: 16 consecutive rows of one tensor.  A CTA of 8 warps takes a unit
 // and splits its K range into 8 runs of 128-column k-blocks; the warps' 16 x 8
 // (or 16 x 16) partial tiles are summed in shared memory in a fixed order.
-// Units come from a global counter, so tensors of any shape share one launch.
+// CTA i starts on unit i and takes further units from a global counter, so
+// tensors of any shape share one launch.
 //
 // Lane (g = lane / 4, t = lane % 4) of a warp owns rows g and g + 8 of the
 // unit and, in every k-block, the 32 columns 32 t .. 32 t + 31: one whole
@@ -507,8 +508,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (threadIdx.x == 0) {
-    first_unit = atomicAdd(slot, 1u);
-    next_unit[1] = atomicAdd(slot, 1u);
+    // every CTA starts on its own unit; the rest come from the counter, so a
+    // launch with fewer than two units per CTA never leaves one CTA holding
+    // two units while another has none
+    first_unit = blockIdx.x;
+    next_unit[1] = gridDim.x + atomicAdd(slot, 1u);
   }
   __syncthreads();
   uint32_t* lut_w = reinterpret_cast<uint32_t*>(smem + S::kLutOff);
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (have_next) prefetch_escapes(nxt);
     int par = 0;
     uint32_t grabbed = 0;
-    if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
+    if (threadIdx.x == 0) grabbed = gridDim.x + atomicAdd(slot, 1u);
     while (true) {
       float acc[NT][4];
 #pragma unroll
@@ -853,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       u_next = next_unit[par];
       par ^= 1;
-      if (threadIdx.x == 0) grabbed = atomicAdd(slot, 1u);
+      if (threadIdx.x == 0) grabbed = gridDim.x + atomicAdd(slot, 1u);
       have_next = u_next < total_units;
       if (have_next) {
         unit_of(p, u_next, cur.ti, warp, nxt);
