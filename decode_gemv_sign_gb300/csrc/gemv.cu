@@ -82,22 +82,28 @@ enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
 // Copies of the code-pair table per scheme (0: register lookups).  K15
 // needs two table bytes per element (the high byte and the exponent bit), so
-// one shared-memory lookup per code byte beats two register lookups; eight
-// copies, one per lane residue, keep bank conflicts down.  Byte-split needs
-// only the high byte and decodes from registers.
+// one shared-memory lookup per code byte beats two register lookups; sixteen
+// copies, one per lane residue mod 16, leave only lanes l and l + 16 able to
+// collide on a bank (measured on a 16384 x 53248 weight: 8 -> 16 copies cut
+// B = 1 from 332 to 317 us and B = 16 from 600 to 568 us; 32 copies, 32 KB a
+// CTA, took L1 from the corrections and were slower at B = 16).  Byte-split
+// needs only the high byte and decodes from registers.
 template <int SRC>
-constexpr int lut_rep() { return SRC == kK15 ? 8 : 0; }
+constexpr int lut_rep() { return SRC == kK15 ? 16 : 0; }
 
 // Escapes a correction thread moves one stage along per k-block, and the most
 // stages a warp's ring keeps, per instantiation (XW: width of the transposed
-// x, 0 = none).  Measured on a 16384 x 53248 weight: K15, with 3 % escapes,
-// gains from deeper in-loop corrections (B = 1: 2 -> 4 cut 385 to 347 us;
-// B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at B = 4) and from
-// two stages, whose smaller shared-memory share leaves more L1 to the
-// corrections' gathers; with two batch tiles (NT = 2) deeper corrections
-// spill registers.
+// x, 0 = none).  K15 without the transposed x moves one aligned quad (4);
+// the others move single entries.  Measured on a 16384 x 53248 weight: K15,
+// with 3 % escapes, gains from deeper in-loop corrections (B = 1: 2 -> 4 cut
+// 385 to 347 us, and quads with vector loads instead of four single entries
+// 316 to 310 us; B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at
+// B = 4) and from two stages, whose smaller shared-memory share leaves more L1
+// to the corrections and to x (three stages: B = 1 305 -> 313 us, B = 16
+// 569 -> 666 us); with two batch tiles (NT = 2) deeper corrections spill
+// registers.
 template <int SRC, int NT, int XW>
-constexpr int esc_q() { return SRC != kK15 ? 2 : NT == 2 ? (XW == 0 ? 2 : 1) : XW == 0 ? 4 : 2; }
+constexpr int esc_q() { return SRC != kK15 ? 2 : NT == 2 ? (XW == 0 ? 4 : 1) : XW == 0 ? 4 : 2; }
 template <int SRC>
 constexpr int max_stages() { return SRC == kK15 ? 2 : 4; }
 
@@ -133,6 +139,14 @@ template <int SCHEME>
 __device__ __forceinline__ float esc_delta(uint32_t val) {
   const uint32_t wph = val & (SCHEME == WCOMP_BYTESPLIT ? 0xFFu : 0x7Fu);
   return __uint_as_float(val << 16) - __uint_as_float(wph << 16);
+}
+
+// The same for the two escapes whose whole words are the halves of w.
+template <int SCHEME>
+__device__ __forceinline__ void esc_delta_pair(uint32_t w, float& d_lo, float& d_hi) {
+  constexpr uint32_t lm = SCHEME == WCOMP_BYTESPLIT ? 0xFFu : 0x7Fu;
+  d_lo = __uint_as_float(w << 16) - __uint_as_float((w & lm) << 16);
+  d_hi = __uint_as_float(w & 0xFFFF0000u) - __uint_as_float(w & (lm << 16));
 }
 
 __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
@@ -384,8 +398,9 @@ __device__ __forceinline__ void compute_item(const RegTable& tab, uint32_t lut, 
 // columns 32 t .. 32 t + 31; zeros for batch rows >= B and columns past K.
 // With PF, the 128-byte lines of the same columns of k-block kb + 1 are
 // prefetched into L1, so the next call finds them there (measured on a
-// 16384 x 53248 weight: byte-split B = 4 289 -> 238 us, plain 283 -> 268 us;
-// K15 and two batch tiles gain nothing).
+// 16384 x 53248 weight: byte-split B = 4 289 -> 238 us, plain 283 -> 268 us,
+// K15 B = 1 310 -> 306 us; K15 with the transposed x and two batch tiles gain
+// nothing).
 template <int NT, bool PF>
 __device__ __forceinline__ void load_x(const GemvBatch& p, const Unit& m, uint32_t kb, int B, int lane,
                                        uint4 (&xv)[NT][4]) {
@@ -614,15 +629,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
       const TensorDesc& d = p.d[cur.ti];
       // ---- escape corrections of this unit, run through the k-loop.  Thread
-      // (row cj, batch slot cb, part cq) owns the escapes e = ce0 + cq + j cP
-      // of row cj (with the transposed x: thread (cj, part tid % 16) owns
-      // e = ce0 + part + 16 j, every batch row at once).  Each k-block moves
-      // esc_q of them one stage along: A requests the position and value, B
-      // (one k-block later) gathers x, C (one more k-block
-      // later) accumulates, so every load has a k-block's compute to land.
-      // Escapes the loop does not reach are taken after it, kEscDepth at a
-      // time.
+      // (row cj, batch slot cb, part cq) owns the aligned quads of entries that
+      // start at (ce0 rounded down to 4) + 4 (cq + j cP) (with the transposed
+      // x: thread (cj, part tid % 16) owns the single entries e = ce0 + part +
+      // 16 j, every batch row at once).  Each k-block moves one quad (esc_q
+      // entries) one stage along: A requests the positions and values, B (one
+      // k-block later) gathers x, C (one more k-block later) accumulates, so
+      // every load has a k-block's compute to land.  What the loop does not
+      // reach is taken after it.
       constexpr bool kXt = XW > 0;
+      constexpr bool kQuads = SRC == kK15 && !kXt;  // K15 entries in aligned quads
       constexpr int kQ = esc_q<SRC, NT, XW>();
       constexpr int kXWords = kXt ? XW / 2 : 1;
       const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
@@ -633,6 +649,57 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       uint32_t posA[kQ], valA[kQ], okA = 0, okB = 0;  // stage masks: entries requested / gathered
       uint32_t xB[kQ][kXWords], valB[kQ];
       float c = 0.f, cs[kXt ? XW : 1];
+      // the quads (no transposed x): stage A's request, stage B's gathered x
+      // and values (entries outside the row zeroed)
+      uint32_t q_next = (ce0 & ~3u) + 4u * uint32_t(cq), qA = 0;
+      const uint32_t q_step = 4u * uint32_t(cP);
+      uint4 pA = make_uint4(0u, 0u, 0u, 0u);
+      uint2 vA = make_uint2(0u, 0u), vB = make_uint2(0u, 0u);
+      uint32_t xQ[4] = {0u, 0u, 0u, 0u};
+      // Quad q's positions and values: aligned vector loads (a quad that
+      // starts below E ends inside the position and value sections, which are
+      // padded to 32 bytes).
+      auto quad_load = [&](uint32_t q, uint4& pq, uint2& vq) {
+        if (!WCOMP_DCHECK(q < d.E, 1)) q = 0;
+        pq = *reinterpret_cast<const uint4*>(d.esc_pos + q);
+        vq = *reinterpret_cast<const uint2*>(d.esc_val + q);
+      };
+      // Gather x for the quad's entries; entries outside [ce0, ce1) (only in
+      // the row's first and last quads) read column 0 and get value 0 and x 0.
+      auto quad_gather = [&](uint32_t q, const uint4& pq, uint2 vq, uint32_t (&xq)[4], uint2& vout) {
+        const uint32_t rb = uint32_t(rowbase);
+        uint32_t k[4] = {pq.x - rb, pq.y - rb, pq.z - rb, pq.w - rb};
+        uint32_t live = 0xFu;
+        if (q < ce0 || q + 4u > ce1) {
+          const uint32_t lo = q < ce0 ? ce0 - q : 0u, hi = q + 4u > ce1 ? ce1 - q : 4u;
+          live = (0xFu << lo) & (0xFu >> (4u - hi));
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (!((live >> i) & 1u)) k[i] = 0u;
+          vq.x &= ((live & 1u) ? 0xFFFFu : 0u) | ((live & 2u) ? 0xFFFF0000u : 0u);
+          vq.y &= ((live & 4u) ? 0xFFFFu : 0u) | ((live & 8u) ? 0xFFFF0000u : 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (!WCOMP_DCHECK(uint64_t(k[i]) < uint64_t(d.K), 1)) k[i] = 0u;
+          xq[i] = xrow[k[i]];
+        }
+        if (live != 0xFu) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (!((live >> i) & 1u)) xq[i] = 0u;
+        }
+        vout = vq;
+      };
+      auto quad_accumulate = [&](const uint32_t (&xq)[4], uint2 vq) {
+        float d0, d1, d2, d3;
+        esc_delta_pair<SRC>(vq.x, d0, d1);
+        esc_delta_pair<SRC>(vq.y, d2, d3);
+        c = fmaf(__uint_as_float(xq[0] << 16), d0, c);
+        c = fmaf(__uint_as_float(xq[1] << 16), d1, c);
+        c = fmaf(__uint_as_float(xq[2] << 16), d2, c);
+        c = fmaf(__uint_as_float(xq[3] << 16), d3, c);
+      };
 #pragma unroll
       for (int b = 0; b < (kXt ? XW : 1); ++b) cs[b] = 0.f;
 #pragma unroll
@@ -644,7 +711,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       // stage A: request positions and values of the next kQ escapes
       auto esc_request = [&]() {
-        if constexpr (SRC != kPlain) {
+        if constexpr (kQuads) {
+          okA = 1;
+          qA = q_next;
+          quad_load(q_next, pA, vA);
+          q_next += q_step;
+        } else if constexpr (SRC != kPlain) {
           okA = 0;
 #pragma unroll
           for (int q = 0; q < kQ; ++q) {
@@ -659,7 +731,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       };
       // stage C then B: accumulate the gathered escapes, gather the requested ones
       auto esc_advance = [&]() {
-        if constexpr (SRC != kPlain) {
+        if constexpr (kQuads) {
+          if (okB) quad_accumulate(xQ, vB);
+          if (okA) quad_gather(qA, pA, vA, xQ, vB);
+          okB = okA;
+          okA = 0;
+        } else if constexpr (SRC != kPlain) {
           if (!(okA | okB)) return;  // nothing in flight (most k-blocks for byte-split's rare escapes)
 #pragma unroll
           for (int q = 0; q < kQ; ++q) {
@@ -701,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           okA = 0;
         }
       };
-      if (SRC != kPlain && e_next < e_end) esc_request();
+      if (SRC != kPlain && (kQuads ? q_next : e_next) < e_end) esc_request();
       for (uint32_t kb = cur.kb0; kb < cur.kb1; ++kb) {
         // every lane is done with the stage of the previous k-block, which the
         // copies below may refill
@@ -709,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         while (!aborted && issued < done + kStages && issue_next()) {
         }
         uint4 xv[NT][4];
-        load_x<NT, SRC != kK15 && NT == 1>(p, cur, kb, B, lane, xv);
+        load_x<NT, NT == 1 && XW == 0>(p, cur, kb, B, lane, xv);
         const uint32_t sidx = done % kStages;
         if (!aborted && __any_sync(0xffffffffu, !mbar_wait_bounded(bars + 8 * sidx, (done / kStages) & 1))) {
           aborted = true;  // the warp stops copying and waiting, and still runs the same instructions
@@ -724,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if constexpr (SRC != kPlain) {
           esc_advance();
           // no new requests in the last k-block: what is left goes to the batches below
-          if (kb + 1 < cur.kb1 && e_next < e_end) esc_request();
+          if (kb + 1 < cur.kb1 && (kQuads ? q_next : e_next) < e_end) esc_request();
         }
       }
       // ---- unit end: partial tiles, escape corrections, fixed-order sums
@@ -793,28 +870,44 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int b = 0; b < (kXt ? XW : 1); ++b) corr[(par * kRows + cj) * 16 + b] = cs[b];
           }
         } else {
-          // kEscDepth escapes at a time, all their loads in flight together
-          // (positions and values, then the x gathers); entries past the row's
-          // last escape contribute exactly zero
-          for (uint32_t e = e_next; e < e_end; e += kEscDepth * e_step) {
-            uint32_t pos[kEscDepth], val[kEscDepth], xw[kEscDepth], okm = 0;
-#pragma unroll
-            for (int v = 0; v < kEscDepth; ++v) {
-              const uint32_t i = e + v * e_step;
-              bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
-              pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
-              ok = ok && WCOMP_DCHECK(uint64_t(pos[v]) - rowbase < uint64_t(d.K), 1);
-              okm |= uint32_t(ok) << v;
-              val[v] = ok ? load_esc_val(d, i) : 0u;
+          if constexpr (kQuads) {
+            // two quads at a time, all their loads in flight together
+            for (uint32_t q = q_next; q < e_end; q += 2u * q_step) {
+              const bool two = q + q_step < e_end;
+              uint4 p0, p1 = make_uint4(0u, 0u, 0u, 0u);
+              uint2 v0, v1 = make_uint2(0u, 0u), w0, w1 = make_uint2(0u, 0u);
+              uint32_t x0[4], x1[4] = {0u, 0u, 0u, 0u};
+              quad_load(q, p0, v0);
+              if (two) quad_load(q + q_step, p1, v1);
+              quad_gather(q, p0, v0, x0, w0);
+              if (two) quad_gather(q + q_step, p1, v1, x1, w1);
+              quad_accumulate(x0, w0);
+              if (two) quad_accumulate(x1, w1);
             }
-#pragma unroll
-            for (int v = 0; v < kEscDepth; ++v) {
-              const bool ok = (okm >> v) & 1;
-              xw[v] = ok ? uint32_t(xrow[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
+          } else {
+            // kEscDepth escapes at a time, all their loads in flight together
+            // (positions and values, then the x gathers); entries past the row's
+            // last escape contribute exactly zero
+            for (uint32_t e = e_next; e < e_end; e += kEscDepth * e_step) {
+              uint32_t pos[kEscDepth], val[kEscDepth], xw[kEscDepth], okm = 0;
+  #pragma unroll
+              for (int v = 0; v < kEscDepth; ++v) {
+                const uint32_t i = e + v * e_step;
+                bool ok = i < e_end && WCOMP_DCHECK(i < d.E, 1);
+                pos[v] = ok ? d.esc_pos[i] : uint32_t(rowbase);
+                ok = ok && WCOMP_DCHECK(uint64_t(pos[v]) - rowbase < uint64_t(d.K), 1);
+                okm |= uint32_t(ok) << v;
+                val[v] = ok ? load_esc_val(d, i) : 0u;
+              }
+  #pragma unroll
+              for (int v = 0; v < kEscDepth; ++v) {
+                const bool ok = (okm >> v) & 1;
+                xw[v] = ok ? uint32_t(xrow[int64_t(uint64_t(pos[v]) - rowbase)]) : 0u;
+              }
+  #pragma unroll
+              for (int v = 0; v < kEscDepth; ++v)
+                c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v]), c);
             }
-#pragma unroll
-            for (int v = 0; v < kEscDepth; ++v)
-              c = fmaf(__uint_as_float(xw[v] << 16), esc_delta<SRC>(val[v]), c);
           }
           corr[par * kThreads + threadIdx.x] = c;
         }
