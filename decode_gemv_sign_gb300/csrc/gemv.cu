@@ -93,17 +93,18 @@ constexpr int lut_rep() { return SRC == kK15 ? 16 : 0; }
 
 // Escapes a correction thread moves one stage along per k-block, and the most
 // stages a warp's ring keeps, per instantiation (XW: width of the transposed
-// x, 0 = none).  K15 without the transposed x moves one aligned quad (4);
+// x, 0 = none).  K15 up to 8 batch rows moves one aligned quad (4 entries);
 // the others move single entries.  Measured on a 16384 x 53248 weight: K15,
 // with 3 % escapes, gains from deeper in-loop corrections (B = 1: 2 -> 4 cut
 // 385 to 347 us, and quads with vector loads instead of four single entries
 // 316 to 310 us; B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at
-// B = 4) and from two stages, whose smaller shared-memory share leaves more L1
+// B = 4, and quads 375 -> 363 us at B = 2, 422 -> 408 us at B = 8) and from
+// two stages, whose smaller shared-memory share leaves more L1
 // to the corrections and to x (three stages: B = 1 305 -> 313 us, B = 16
 // 569 -> 666 us); with two batch tiles (NT = 2) deeper corrections spill
 // registers.
 template <int SRC, int NT, int XW>
-constexpr int esc_q() { return SRC != kK15 ? 2 : NT == 2 ? (XW == 0 ? 4 : 1) : XW == 0 ? 4 : 2; }
+constexpr int esc_q() { return SRC != kK15 ? 2 : XW <= 8 ? 4 : 1; }
 template <int SRC>
 constexpr int max_stages() { return SRC == kK15 ? 2 : 4; }
 
@@ -147,6 +148,15 @@ __device__ __forceinline__ void esc_delta_pair(uint32_t w, float& d_lo, float& d
   constexpr uint32_t lm = SCHEME == WCOMP_BYTESPLIT ? 0xFFu : 0x7Fu;
   d_lo = __uint_as_float(w << 16) - __uint_as_float((w & lm) << 16);
   d_hi = __uint_as_float(w & 0xFFFF0000u) - __uint_as_float(w & (lm << 16));
+}
+
+// 32 bytes of x (one column of the 16-wide transposed x) in one load: one
+// request per escape instead of two (measured on a 16384 x 53248 weight: K15
+// B = 16 568 -> 537 us, B = 9 508 -> 496 us).
+__device__ __forceinline__ void ld_x_v8(const uint16_t* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
 }
 
 __device__ __forceinline__ uint4 ld_x_v4(const uint16_t* p) {
@@ -629,16 +639,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
       const TensorDesc& d = p.d[cur.ti];
       // ---- escape corrections of this unit, run through the k-loop.  Thread
-      // (row cj, batch slot cb, part cq) owns the aligned quads of entries that
-      // start at (ce0 rounded down to 4) + 4 (cq + j cP) (with the transposed
-      // x: thread (cj, part tid % 16) owns the single entries e = ce0 + part +
-      // 16 j, every batch row at once).  Each k-block moves one quad (esc_q
-      // entries) one stage along: A requests the positions and values, B (one
-      // k-block later) gathers x, C (one more k-block later) accumulates, so
-      // every load has a k-block's compute to land.  What the loop does not
-      // reach is taken after it.
+      // (row cj, batch slot cb, part cq) owns the entries e = ce0 + cq + j cP
+      // of row cj; with the transposed x, thread (cj, part tid % 16) owns
+      // e = ce0 + part + 16 j and adds each to every batch row at once.  K15
+      // up to 8 batch rows moves aligned quads instead: the part's quads start
+      // at (ce0 rounded down to 4) + 4 (part + j parts).  Each k-block moves
+      // esc_q entries one stage along: A requests the positions and values, B
+      // (one k-block later) gathers x, C (one more k-block later) accumulates,
+      // so every load has a k-block's compute to land.  What the loop does
+      // not reach is taken after it.
       constexpr bool kXt = XW > 0;
-      constexpr bool kQuads = SRC == kK15 && !kXt;  // K15 entries in aligned quads
+      constexpr bool kQuads = SRC == kK15 && XW <= 8;  // K15 entries in aligned quads
       constexpr int kQ = esc_q<SRC, NT, XW>();
       constexpr int kXWords = kXt ? XW / 2 : 1;
       const uint64_t rowbase = uint64_t(cur.r0 + cj) * uint64_t(d.K);
@@ -649,13 +660,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       uint32_t posA[kQ], valA[kQ], okA = 0, okB = 0;  // stage masks: entries requested / gathered
       uint32_t xB[kQ][kXWords], valB[kQ];
       float c = 0.f, cs[kXt ? XW : 1];
-      // the quads (no transposed x): stage A's request, stage B's gathered x
-      // and values (entries outside the row zeroed)
-      uint32_t q_next = (ce0 & ~3u) + 4u * uint32_t(cq), qA = 0;
-      const uint32_t q_step = 4u * uint32_t(cP);
+      // the quads: stage A's request, stage B's gathered x and values
+      // (entries outside the row zeroed)
+      uint32_t q_next = (ce0 & ~3u) + 4u * uint32_t(kXt ? (threadIdx.x & 15) : cq), qA = 0;
+      const uint32_t q_step = 4u * uint32_t(kXt ? 16 : cP);
       uint4 pA = make_uint4(0u, 0u, 0u, 0u);
       uint2 vA = make_uint2(0u, 0u), vB = make_uint2(0u, 0u);
-      uint32_t xQ[4] = {0u, 0u, 0u, 0u};
+      uint32_t xQ[4][kXWords];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int w = 0; w < kXWords; ++w) xQ[i][w] = 0u;
       // Quad q's positions and values: aligned vector loads (a quad that
       // starts below E ends inside the position and value sections, which are
       // padded to 32 bytes).
@@ -666,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       };
       // Gather x for the quad's entries; entries outside [ce0, ce1) (only in
       // the row's first and last quads) read column 0 and get value 0 and x 0.
-      auto quad_gather = [&](uint32_t q, const uint4& pq, uint2 vq, uint32_t (&xq)[4], uint2& vout) {
+      auto quad_gather = [&](uint32_t q, const uint4& pq, uint2 vq, uint32_t (&xq)[4][kXWords], uint2& vout) {
         const uint32_t rb = uint32_t(rowbase);
         uint32_t k[4] = {pq.x - rb, pq.y - rb, pq.z - rb, pq.w - rb};
         uint32_t live = 0xFu;
@@ -682,23 +697,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           if (!WCOMP_DCHECK(uint64_t(k[i]) < uint64_t(d.K), 1)) k[i] = 0u;
-          xq[i] = xrow[k[i]];
+          if constexpr (XW == 0) {
+            xq[i][0] = xrow[k[i]];
+          } else if constexpr (XW == 4) {
+            const uint2 v = *reinterpret_cast<const uint2*>(xrow + uint64_t(k[i]) * XW);
+            xq[i][0] = v.x;
+            xq[i][1 % kXWords] = v.y;
+          } else {
+            const uint4 v = *reinterpret_cast<const uint4*>(xrow + uint64_t(k[i]) * XW);
+            xq[i][0] = v.x;
+            xq[i][1 % kXWords] = v.y;
+            xq[i][2 % kXWords] = v.z;
+            xq[i][3 % kXWords] = v.w;
+          }
         }
         if (live != 0xFu) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            if (!((live >> i) & 1u)) xq[i] = 0u;
+#pragma unroll
+            for (int w = 0; w < kXWords; ++w)
+              if (!((live >> i) & 1u)) xq[i][w] = 0u;
         }
         vout = vq;
       };
-      auto quad_accumulate = [&](const uint32_t (&xq)[4], uint2 vq) {
-        float d0, d1, d2, d3;
-        esc_delta_pair<SRC>(vq.x, d0, d1);
-        esc_delta_pair<SRC>(vq.y, d2, d3);
-        c = fmaf(__uint_as_float(xq[0] << 16), d0, c);
-        c = fmaf(__uint_as_float(xq[1] << 16), d1, c);
-        c = fmaf(__uint_as_float(xq[2] << 16), d2, c);
-        c = fmaf(__uint_as_float(xq[3] << 16), d3, c);
+      auto quad_accumulate = [&](const uint32_t (&xq)[4][kXWords], uint2 vq) {
+        float dl[4];
+        esc_delta_pair<SRC>(vq.x, dl[0], dl[1]);
+        esc_delta_pair<SRC>(vq.y, dl[2], dl[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (kXt) {
+#pragma unroll
+            for (int h = 0; h < kXWords; ++h) {
+              cs[2 * h] = fmaf(bf16_lo(xq[i][h]), dl[i], cs[2 * h]);
+              cs[2 * h + 1] = fmaf(bf16_hi(xq[i][h]), dl[i], cs[2 * h + 1]);
+            }
+          } else {
+            c = fmaf(__uint_as_float(xq[i][0] << 16), dl[i], c);
+          }
+        }
       };
 #pragma unroll
       for (int b = 0; b < (kXt ? XW : 1); ++b) cs[b] = 0.f;
@@ -762,6 +799,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint2 v = ok ? *reinterpret_cast<const uint2*>(xr) : make_uint2(0u, 0u);
                 xB[q][0] = v.x;
                 xB[q][1 % kXWords] = v.y;
+              } else if (XW == 16) {
+                uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (ok) ld_x_v8(xr, r);
+#pragma unroll
+                for (int h = 0; h < 8; ++h) xB[q][h % kXWords] = r[h];
               } else {
 #pragma unroll
                 for (int h = 0; h < XW / 8; ++h) {
@@ -819,7 +861,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // thread (row cj, part tid % 16 of 16): every batch row at once
           // from the transposed x; the 16 parts of a row (one half-warp) are
           // summed by a fixed shuffle tree
-          {
+          if constexpr (kQuads) {
+            for (uint32_t q = q_next; q < e_end; q += q_step) {
+              uint4 p0;
+              uint2 v0, w0;
+              uint32_t x0[4][kXWords];
+              quad_load(q, p0, v0);
+              quad_gather(q, p0, v0, x0, w0);
+              quad_accumulate(x0, w0);
+            }
+          } else {
             constexpr int D = XW >= 16 ? kEscDepth / 4 : kEscDepth / 2;
             for (uint32_t e = e_next; e < e_end; e += D * e_step) {
               uint32_t pos[D], val[D];
@@ -840,6 +891,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                   const uint2 q2 = *reinterpret_cast<const uint2*>(xr);
                   wv[v][0] = q2.x;
                   wv[v][1 % (XW / 2)] = q2.y;
+                } else if (XW == 16) {
+                  uint32_t r[8];
+                  ld_x_v8(xr, r);
+#pragma unroll
+                  for (int h = 0; h < 8; ++h) wv[v][h % (XW / 2)] = r[h];
                 } else {
 #pragma unroll
                   for (int q = 0; q < XW / 8; ++q) {
@@ -876,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               const bool two = q + q_step < e_end;
               uint4 p0, p1 = make_uint4(0u, 0u, 0u, 0u);
               uint2 v0, v1 = make_uint2(0u, 0u), w0, w1 = make_uint2(0u, 0u);
-              uint32_t x0[4], x1[4] = {0u, 0u, 0u, 0u};
+              uint32_t x0[4][kXWords], x1[4][kXWords] = {};
               quad_load(q, p0, v0);
               if (two) quad_load(q + q_step, p1, v1);
               quad_gather(q, p0, v0, x0, w0);
