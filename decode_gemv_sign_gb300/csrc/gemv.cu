@@ -1201,13 +1201,14 @@ template <int SRC, int NT, int XW>
 int prepare_kernel() {
   auto kern = gemv_kernel<SRC, NT, XW>;
   constexpr uint32_t smem = Smem<SRC, NT, XW>::kBytes;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) return -1;
+  // set up once per instantiation (racing first calls both do the same idempotent work)
   static std::atomic<int> per_sm_cache{0};
-  int per_sm = per_sm_cache.load(std::memory_order_relaxed);
+  int per_sm = per_sm_cache.load(std::memory_order_acquire);
   if (!per_sm) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) return -1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm <= 0)
       per_sm = 1;
-    per_sm_cache.store(per_sm, std::memory_order_relaxed);
+    per_sm_cache.store(per_sm, std::memory_order_release);
   }
   return per_sm;
 }
