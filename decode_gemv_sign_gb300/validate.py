@@ -14,14 +14,17 @@ encoded with one batched call per scheme, decoded with one batched call and
 compared with its source on the device.  With ``source="host"`` the batches
 live in pinned host memory, as a checkpoint read from storage would: each one
 is copied to the device on a copy stream while the previous batch is encoded
-and decoded (two host and two device buffers alternate).  With
-``source="device"`` each batch is drawn straight on the device (no transfer),
-for runs over the whole set.
+and decoded (two host and two device buffers alternate); the host buffers are
+filled by drawing the synthetic tensors on the device and copying them back,
+in place of reading shards.  With ``source="device"`` each batch is drawn
+straight on the device (no transfer), for runs over the whole set.  Both
+modes draw the same bytes.
 
 Optional checks per tensor:
   * ``hashes``: BLAKE2b-128 of the source bytes (taken on the host from the
     bytes the pipeline was given) and of every decoded copy (read back); the
-    two must agree;
+    two must agree.  The hashes run in a pool of host threads while the GPU
+    goes on, and a batch's records are logged once its hashes are in;
   * ``corrupt_every`` (k > 0): every k-th tensor (and scheme) is serialized in
     both forms, one seeded byte of each is flipped on the host, and
     wcomp_deserialize must refuse both as corrupt (the CRC-32 over header and
@@ -169,11 +172,21 @@ class _HostStream:
 
 
 def _fill_host(specs, views):
-    """Draw the batch's weights on the host (torch's CPU generator)."""
+    """Fill the batch's pinned host views, standing in for reading the shards
+    from storage.  Each tensor is drawn on the device (the same draw as
+    ``source="device"``, so both modes validate the same bytes) on a stream of
+    its own and copied into its host view; torch's CPU generator took tens of
+    seconds per GB, which would have made the synthetic draw, not the
+    pipeline, the bound of a host-streamed run."""
+    import torch
+
     from decode_gemv_sign_gb300 import synth
 
-    for s, v in zip(specs, views):
-        v.copy_(synth.gen_weights_torch(s, "cpu"))
+    fill_stream = torch.cuda.Stream()
+    with torch.cuda.stream(fill_stream):
+        for s, v in zip(specs, views):
+            v.copy_(synth.gen_weights_torch(s, "cuda"), non_blocking=True)
+    fill_stream.synchronize()
 
 
 def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int = 16 << 30,
@@ -220,6 +233,8 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
                 for s in batch:
                     if s.name in todo_names:
                         src_hash[s.name] = hasher.submit(tensor_hash, host_src[s.name] if host_src else src[s.name].cpu())
+            # records of this batch, completed once their hashes are in
+            pending = []
             for sc in schemes:
                 items = [s for s, c in todo if c == sc]
                 if not items:
@@ -235,17 +250,22 @@ def validate(specs: Sequence, schemes: Sequence[int] = (0, 1), batch_bytes: int 
                            "escapes": inf["n_escapes"], "serialized_bytes": inf["serialized_bytes"],
                            "serialized_compact_bytes": inf["serialized_compact_bytes"],
                            "entropy_bpw": inf["entropy_bpw"], "exact": exact}
-                    if hasher:
-                        rec["source_hash"] = src_hash[s.name].result()
-                        rec["decoded_hash"] = tensor_hash(o)
+                    # the decoded bytes are read back here (in stream order) and
+                    # hashed by the pool while the GPU goes on
+                    dec_hash = hasher.submit(tensor_hash, o.cpu()) if hasher else None
                     if corrupt_every > 0 and index[s.name] % corrupt_every == 0:
                         rec["corruption"] = corruption_check(W, c, 7919 * index[s.name] + sc)
-                    done[(s.name, sc)] = rec
-                    if log:
-                        log.write(json.dumps(rec) + "\n")
+                    pending.append((s.name, sc, rec, dec_hash))
                 for c in cs:
                     c.free(stream)
                 del outs
+            for name, sc, rec, dec_hash in pending:
+                if hasher:
+                    rec["source_hash"] = src_hash[name].result()
+                    rec["decoded_hash"] = dec_hash.result()
+                done[(name, sc)] = rec
+                if log:
+                    log.write(json.dumps(rec) + "\n")
             if log:
                 log.flush()
             if feeder:
