@@ -1194,21 +1194,23 @@ uint32_t unit_prefix(GemvBatch& b, const int64_t* Ns) {
   return units;
 }
 
-// Resident CTAs per SM of one instantiation, asked once (the shared-memory
-// limit is set on every launch: it is an attribute of the function in the
-// current device's context).
+// Resident CTAs per SM of one instantiation on device `dev`, with its
+// shared-memory limit set (an attribute of the function in that device's
+// context): done once per instantiation and device; racing first calls do
+// the same idempotent work.
+constexpr int kPrepDevices = 64;
 template <int SRC, int NT, int XW>
-int prepare_kernel() {
+int prepare_kernel(int dev) {
   auto kern = gemv_kernel<SRC, NT, XW>;
   constexpr uint32_t smem = Smem<SRC, NT, XW>::kBytes;
-  // set up once per instantiation (racing first calls both do the same idempotent work)
-  static std::atomic<int> per_sm_cache{0};
-  int per_sm = per_sm_cache.load(std::memory_order_acquire);
+  static std::atomic<int> per_sm_cache[kPrepDevices];
+  const bool cached = dev >= 0 && dev < kPrepDevices;
+  int per_sm = cached ? per_sm_cache[dev].load(std::memory_order_acquire) : 0;
   if (!per_sm) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) return -1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm <= 0)
       per_sm = 1;
-    per_sm_cache.store(per_sm, std::memory_order_release);
+    if (cached) per_sm_cache[dev].store(per_sm, std::memory_order_release);
   }
   return per_sm;
 }
@@ -1221,7 +1223,7 @@ int launch(GemvBatch& b, const TmaBatch& tm, const int64_t* Ns, int B, int dev, 
   if (st != WCOMP_OK) return st;
   uint32_t* slot = nullptr;
   if ((st = counter_slot(dev, &slot)) != WCOMP_OK) return st;
-  const int per_sm = prepare_kernel<SRC, NT, XW>();
+  const int per_sm = prepare_kernel<SRC, NT, XW>(dev);
   if (per_sm < 0) return map_cuda(cudaGetLastError());
   XtBatch xt;
   memset(&xt, 0, sizeof(xt));
@@ -1515,9 +1517,9 @@ uint32_t* noalloc_error_word(int dev) {
 }
 
 template <int SRC, int NT>
-int launch_on(GemvBatch& b, const TmaBatch& tm, int64_t N, int B, int sms, uint32_t* slot, cudaStream_t s) {
+int launch_on(GemvBatch& b, const TmaBatch& tm, int64_t N, int B, int dev, int sms, uint32_t* slot, cudaStream_t s) {
   const uint32_t units = unit_prefix(b, &N);
-  const int per_sm = prepare_kernel<SRC, NT, 0>();
+  const int per_sm = prepare_kernel<SRC, NT, 0>(dev);
   if (per_sm < 0) return map_cuda(cudaGetLastError());
   XtBatch xt;
   memset(&xt, 0, sizeof(xt));
@@ -1560,7 +1562,7 @@ extern "C" int wcomp_gemv_noalloc(const wcomp_container* c, const uint16_t* d_x,
   if (!tm) return WCOMP_ENOMEM;
   memcpy(tm->m[0], c->tmap, sizeof(c->tmap));
   if (c->L.scheme == WCOMP_BYTESPLIT)
-    return B <= 8 ? launch_on<kBytesplit, 1>(b, *tm, N, B, sms, scratch, s)
-                  : launch_on<kBytesplit, 2>(b, *tm, N, B, sms, scratch, s);
-  return B <= 8 ? launch_on<kK15, 1>(b, *tm, N, B, sms, scratch, s) : launch_on<kK15, 2>(b, *tm, N, B, sms, scratch, s);
+    return B <= 8 ? launch_on<kBytesplit, 1>(b, *tm, N, B, dev, sms, scratch, s)
+                  : launch_on<kBytesplit, 2>(b, *tm, N, B, dev, sms, scratch, s);
+  return B <= 8 ? launch_on<kK15, 1>(b, *tm, N, B, dev, sms, scratch, s) : launch_on<kK15, 2>(b, *tm, N, B, dev, sms, scratch, s);
 }
