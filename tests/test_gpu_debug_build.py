@@ -57,7 +57,7 @@ for w in cases:
         c = W.encode(dev(w), scheme)
         assert W.serialize(c) == O.serialize(ref)
         assert np.array_equal(W.decode(c).cpu().numpy().view(np.uint16).reshape(w.shape), w)
-        for B in (1, 2, 4, 9, 16):
+        for B in (1, 2, 4, 8, 9, 16):
             x = synth.gen_x_np(B, K, 50 + B)
             y = W.gemv(c, dev(x)).cpu().numpy().astype(np.float64)
             yn = torch.empty((B, N), dtype=torch.float32, device="cuda")

@@ -249,6 +249,43 @@ def test_escapes_on_row_and_tile_boundaries(W, scheme, shape):
     c.free()
 
 
+def _escapes_per_row(N, K, seed):
+    """W[N, K] of common symbols with row r holding r % 11 escapes (rare
+    exponents) at seeded columns, so that a row's first escape entry falls at
+    every residue mod 4 of the stream and rows with 0..10 escapes alternate
+    (each row's first and last groups of four entries are partial)."""
+    rng = np.random.default_rng(seed)
+    common = np.array([0x3C, 0x3D, 0x3E, 0x3F, 0xBC, 0xBD, 0xBE, 0xBF, 0x3B, 0xBB, 0x3A, 0xBA, 0x39, 0xB9, 0x38])
+    hi = common[rng.integers(0, 15, size=(N, K))]
+    lo = rng.integers(0, 128, size=(N, K))  # exponent bit 0 clear: 15 nine-bit symbols too
+    w = ((hi << 8) | lo).astype(np.uint16)
+    for r in range(N):
+        cols = rng.choice(K, size=r % 11, replace=False)
+        w[r, cols] = ((0x40 + rng.integers(0, 4, size=cols.size)) << 8 | rng.integers(0, 256, size=cols.size)).astype(np.uint16)
+    return w
+
+
+@pytest.mark.parametrize("scheme", O.SCHEMES)
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 8, 9, 16])
+def test_gemv_escape_counts_per_row(W, scheme, B):
+    """Rows with 0..10 escapes each, over several 16-row units and every
+    alignment of a row's entries in the escape stream: the fused GEMV (single
+    entries, aligned groups of four, transposed x) matches the oracle, and the
+    output's guard regions stay intact."""
+    N, K = 83, 2048
+    w = _escapes_per_row(N, K, 900 + B)
+    ref = O.encode(w, scheme)
+    counts = np.bincount(np.asarray(ref.esc_pos) // K, minlength=N)
+    assert counts.tolist() == [r % 11 for r in range(N)]
+    x = synth.gen_x_np(B, K, 910 + B)
+    c = W.encode(dev(w), scheme)
+    g = Guarded((B, N), torch.float32)
+    check_gemv(W.gemv(c, dev(x), g.out), O.gemv(w, x))
+    g.check()
+    W.device_check()
+    c.free()
+
+
 @pytest.mark.parametrize("scheme", O.SCHEMES)
 def test_gemv_one_hot_exact_and_zero(W, scheme):
     spec = synth.WeightSpec("o", 64, 256, "normal", 0.02, 0.05, "normal", 1.0, seed=5)
