@@ -80,16 +80,20 @@ constexpr int kEscDepth = 16;  // escape corrections with their loads in flight 
 
 enum Src { kBytesplit = WCOMP_BYTESPLIT, kK15 = WCOMP_K15, kPlain = 2 };
 
-// Copies of the code-pair table per scheme (0: register lookups).  K15
-// needs two table bytes per element (the high byte and the exponent bit), so
-// one shared-memory lookup per code byte beats two register lookups; sixteen
-// copies, one per lane residue mod 16, leave only lanes l and l + 16 able to
-// collide on a bank (measured on a 16384 x 53248 weight: 8 -> 16 copies cut
-// B = 1 from 332 to 317 us and B = 16 from 600 to 568 us; 32 copies, 32 KB a
-// CTA, took L1 from the corrections and were slower at B = 16).  Byte-split
-// needs only the high byte and decodes from registers.
-template <int SRC>
-constexpr int lut_rep() { return SRC == kK15 ? 16 : 0; }
+// Copies of the code-pair table per instantiation (0: register lookups).
+// K15 needs two table bytes per element (the high byte and the exponent bit),
+// so at B <= 4 one shared-memory lookup per code byte beats two register
+// lookups; sixteen copies, one per lane residue mod 16, leave only lanes l and
+// l + 16 able to collide on a bank (measured on a 16384 x 53248 weight: 8 -> 16
+// copies cut B = 1 from 332 to 317 us and B = 16 from 600 to 568 us; 32
+// copies, 32 KB a CTA, took L1 from the corrections and were slower at B = 16).
+// Above B = 4 the transposed-x gathers of the corrections want that L1 more
+// than the decode wants the table: register lookups took B = 8 from 408 to
+// 403 us and B = 16 from 539 to 523 us (and B = 1 from 305 to 350 us, B = 2
+// from 363 to 367 us, so the table stays there).  Byte-split needs only the
+// high byte and decodes from registers.
+template <int SRC, int NT, int XW>
+constexpr int lut_rep() { return SRC == kK15 && NT == 1 && XW <= 4 ? 16 : 0; }
 
 // Escapes a correction thread moves one stage along per k-block, and the most
 // stages a warp's ring keeps, per instantiation (XW: width of the transposed
@@ -319,12 +323,12 @@ __device__ __forceinline__ void pairs8(const RegTable& tab, uint32_t cw, uint32_
 // exponent bit (bit 7) and high byte of the low nibble's symbol, then those of
 // the high nibble's symbol (byte-split: 0, symbol, 0, symbol).  lut is this
 // lane's copy (lut_rep copies interleaved word by word, lane % lut_rep).
-template <int SRC>
+template <int SRC, int REP>
 __device__ __forceinline__ void pairs8_lut(uint32_t lut, uint32_t cw, uint32_t l0, uint32_t l1, uint32_t (&P)[4]) {
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
     const uint32_t v = prmt(cw, 0u, 0x4440u + b);
-    const uint32_t T = lds32(lut + v * (lut_rep<SRC>() * 4));
+    const uint32_t T = lds32(lut + v * (REP * 4));
     const uint32_t w = prmt(b < 2 ? l0 : l1, T, (b & 1) ? 0x7352u : 0x7150u);
     P[b] = SRC == kK15 ? ((w & ~0x00800080u) | (T & 0x00800080u)) : w;
   }
@@ -335,7 +339,7 @@ __device__ __forceinline__ void pairs8_lut(uint32_t lut, uint32_t cw, uint32_t l
 // k-block that ends past K (FULL false) a lane whose columns are all past K
 // (live false) feeds zero weights: its zero-filled codes would decode to the
 // table's first symbol, which need not be finite.
-template <int SRC, int NT, bool FULL>
+template <int SRC, int NT, bool FULL, int REP>
 __device__ __forceinline__ void compute_item(const RegTable& tab, uint32_t lut, uint32_t st, int lane, bool live,
                                              const uint4 (&xv)[NT][4], float (&acc)[NT][4]) {
   const uint32_t g = uint32_t(lane) >> 2, t = uint32_t(lane) & 3;
@@ -376,8 +380,8 @@ __device__ __forceinline__ void compute_item(const RegTable& tab, uint32_t lut, 
     // register lookups, replaced by the exponent bit in the table lookups
 #pragma unroll
     for (int q = 0; q < 7; ++q) {
-      lg[q] = lut_rep<SRC>() ? wg[q] : wg[q] & 0x7F7F7F7Fu;
-      lh[q] = lut_rep<SRC>() ? wh[q] : wh[q] & 0x7F7F7F7Fu;
+      lg[q] = REP ? wg[q] : wg[q] & 0x7F7F7F7Fu;
+      lh[q] = REP ? wh[q] : wh[q] & 0x7F7F7F7Fu;
     }
     lg[7] = k15_tail(wg);
     lh[7] = k15_tail(wh);
@@ -385,9 +389,9 @@ __device__ __forceinline__ void compute_item(const RegTable& tab, uint32_t lut, 
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t P[4], H[4];
-    if (lut_rep<SRC>()) {
-      pairs8_lut<SRC>(lut, cg[i], lg[2 * i], lg[2 * i + 1], P);
-      pairs8_lut<SRC>(lut, ch[i], lh[2 * i], lh[2 * i + 1], H);
+    if (REP) {
+      pairs8_lut<SRC, REP>(lut, cg[i], lg[2 * i], lg[2 * i + 1], P);
+      pairs8_lut<SRC, REP>(lut, ch[i], lh[2 * i], lh[2 * i + 1], H);
     } else {
       pairs8<SRC>(tab, cg[i], lg[2 * i], lg[2 * i + 1], P);
       pairs8<SRC>(tab, ch[i], lh[2 * i], lh[2 * i + 1], H);
@@ -488,7 +492,7 @@ struct SmemAt {
   static constexpr uint32_t kCorr = SRC == kPlain ? 0 : XW > 0 ? 2 * kRows * 16 : 2 * kThreads;  // floats
   static constexpr uint32_t kCorrOff = kPartOff + 4 * kPart;
   static constexpr uint32_t kLutOff = kCorrOff + 4 * kCorr;
-  static constexpr uint32_t kLut = 256 * lut_rep<SRC>();  // words
+  static constexpr uint32_t kLut = 256 * lut_rep<SRC, NT, XW>();  // words
   static constexpr uint32_t kUnitOff = kLutOff + 4 * kLut;  // first unit, next unit x 2
   static constexpr uint32_t kBytes = kUnitOff + 16 + 1024;
 };
@@ -541,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
   uint32_t* lut_w = reinterpret_cast<uint32_t*>(smem + S::kLutOff);
-  constexpr int kRep = lut_rep<SRC>();
+  constexpr int kRep = lut_rep<SRC, NT, XW>();
   const uint32_t lut = base_u32 + pad + S::kLutOff + uint32_t(lane % (kRep ? kRep : 1)) * 4;
   // the code-pair table of tensor ti, every thread writing its share
   auto build_lut = [&](int ti) {
@@ -836,9 +840,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         const uint32_t st = ring + sidx * StageGeom<SRC>::kBytes;
         if (kb + 1 < cur.nkb || cur.kvalid == kKBlock)
-          compute_item<SRC, NT, true>(d.t, lut, st, lane, true, xv, acc);
+          compute_item<SRC, NT, true, kRep>(d.t, lut, st, lane, true, xv, acc);
         else
-          compute_item<SRC, NT, false>(d.t, lut, st, lane, uint32_t(32 * (lane & 3)) < cur.kvalid, xv, acc);
+          compute_item<SRC, NT, false, kRep>(d.t, lut, st, lane, uint32_t(32 * (lane & 3)) < cur.kvalid, xv, acc);
         ++done;
         if constexpr (SRC != kPlain) {
           esc_advance();
