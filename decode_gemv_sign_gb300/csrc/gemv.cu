@@ -106,11 +106,12 @@ constexpr int lut_rep() { return SRC == kK15 && NT == 1 && XW <= 4 ? 16 : 0; }
 // two stages, whose smaller shared-memory share leaves more L1
 // to the corrections and to x (three stages: B = 1 305 -> 313 us, B = 16
 // 569 -> 666 us); with two batch tiles (NT = 2) deeper corrections spill
-// registers.
+// registers.  Byte-split with two batch tiles also keeps two stages (three:
+// B = 9 277 -> 272 us, B = 16 322 -> 318 us with two).
 template <int SRC, int NT, int XW>
 constexpr int esc_q() { return SRC != kK15 ? 2 : XW <= 8 ? 4 : 1; }
-template <int SRC>
-constexpr int max_stages() { return SRC == kK15 ? 2 : 4; }
+template <int SRC, int NT>
+constexpr int max_stages() { return SRC == kK15 || (SRC == kBytesplit && NT == 2) ? 2 : 4; }
 
 // One stage of one warp in shared memory, as the tensor copies write it (row
 // r of a box at r times its row length; regions start on 1024-byte
@@ -499,8 +500,8 @@ struct SmemAt {
 
 template <int SRC, int NT, int XW>
 constexpr int ring_stages() {
-  return max_stages<SRC>() >= 4 && SmemAt<SRC, NT, XW, 4>::kBytes <= kSmemPerCta   ? 4
-         : max_stages<SRC>() >= 3 && SmemAt<SRC, NT, XW, 3>::kBytes <= kSmemPerCta ? 3
+  return max_stages<SRC, NT>() >= 4 && SmemAt<SRC, NT, XW, 4>::kBytes <= kSmemPerCta   ? 4
+         : max_stages<SRC, NT>() >= 3 && SmemAt<SRC, NT, XW, 3>::kBytes <= kSmemPerCta ? 3
                                                                                    : 2;
 }
 
