@@ -103,11 +103,11 @@ constexpr int lut_rep() { return SRC == kK15 && NT == 1 && XW <= 4 ? 16 : 0; }
 // 385 to 347 us, and quads with vector loads instead of four single entries
 // 316 to 310 us; B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at
 // B = 4, and quads 375 -> 363 us at B = 2, 422 -> 408 us at B = 8) and from
-// two stages, whose smaller shared-memory share leaves more L1
-// to the corrections and to x (three stages: B = 1 305 -> 313 us, B = 16
-// 569 -> 666 us); with two batch tiles (NT = 2) deeper corrections spill
-// registers.  Byte-split with two batch tiles also keeps two stages (three:
-// B = 9 277 -> 272 us, B = 16 322 -> 318 us with two).
+// two stages, whose smaller shared-memory share leaves more L1 to the
+// corrections and to x (three stages: B = 1 305 -> 313 us, B = 16 569 -> 666
+// us); with two batch tiles (NT = 2) deeper corrections spill registers.
+// Byte-split with two batch tiles also keeps two stages (against three: B = 9
+// 277 -> 272 us, B = 16 322 -> 318 us).
 template <int SRC, int NT, int XW>
 constexpr int esc_q() { return SRC != kK15 ? 2 : XW <= 8 ? 4 : 1; }
 template <int SRC, int NT>
