@@ -537,12 +537,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int i = 0; i < kStages; ++i) mbar_init_u32(bars + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // Every CTA starts on its own unit; the rest come from the counter, so a
+  // launch with fewer than two units per CTA never leaves one CTA holding two
+  // units while another has none.  A launch with a CTA for every unit leaves
+  // the counter alone (no round trips to it; it stays zero).
+  const bool counted = gridDim.x < total_units;
+  auto grab = [&]() -> uint32_t { return counted ? gridDim.x + atomicAdd(slot, 1u) : total_units; };
   if (threadIdx.x == 0) {
-    // every CTA starts on its own unit; the rest come from the counter, so a
-    // launch with fewer than two units per CTA never leaves one CTA holding
-    // two units while another has none
     first_unit = blockIdx.x;
-    next_unit[1] = gridDim.x + atomicAdd(slot, 1u);
+    next_unit[1] = grab();
   }
   __syncthreads();
   uint32_t* lut_w = reinterpret_cast<uint32_t*>(smem + S::kLutOff);
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (have_next) prefetch_escapes(nxt);
     int par = 0;
     uint32_t grabbed = 0;
-    if (threadIdx.x == 0) grabbed = gridDim.x + atomicAdd(slot, 1u);
+    if (threadIdx.x == 0) grabbed = grab();
     while (true) {
       float acc[NT][4];
 #pragma unroll
@@ -1011,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       u_next = next_unit[par];
       par ^= 1;
-      if (threadIdx.x == 0) grabbed = gridDim.x + atomicAdd(slot, 1u);
+      if (threadIdx.x == 0) grabbed = grab();
       have_next = u_next < total_units;
       if (have_next) {
         unit_of(p, u_next, cur.ti, warp, nxt);
@@ -1029,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncwarp();
   // The last CTA to finish returns the counter slot to zero for the next launch.
-  if (threadIdx.x == 0) {
+  if (counted && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(slot + 1, 1u) == gridDim.x - 1) {
       atomicExch(slot, 0u);
@@ -1251,7 +1254,9 @@ int launch(GemvBatch& b, const TmaBatch& tm, const int64_t* Ns, int B, int dev, 
     transpose_x_kernel<kXw><<<blocks, 256, 0, s>>>(b, xt, B);
     count_launches(1);
   }
-  gemv_kernel<SRC, NT, XW><<<per_sm * sms, kThreads, Smem<SRC, NT, XW>::kBytes, s>>>(b, tm, units, B, slot,
+  // no more CTAs than units: a CTA without a unit would only cost its launch
+  const uint32_t grid = std::max<uint32_t>(1u, std::min<uint32_t>(uint32_t(per_sm * sms), units));
+  gemv_kernel<SRC, NT, XW><<<grid, kThreads, Smem<SRC, NT, XW>::kBytes, s>>>(b, tm, units, B, slot,
                                                                                      base + 2 * kSlots, xt);
   count_launches(1);
   const cudaError_t e = cudaGetLastError();
@@ -1528,7 +1533,8 @@ int launch_on(GemvBatch& b, const TmaBatch& tm, int64_t N, int B, int dev, int s
   if (per_sm < 0) return map_cuda(cudaGetLastError());
   XtBatch xt;
   memset(&xt, 0, sizeof(xt));
-  gemv_kernel<SRC, NT, 0><<<per_sm * sms, kThreads, Smem<SRC, NT, 0>::kBytes, s>>>(b, tm, units, B, slot, slot + 2, xt);
+  const uint32_t grid = std::max<uint32_t>(1u, std::min<uint32_t>(uint32_t(per_sm * sms), units));
+  gemv_kernel<SRC, NT, 0><<<grid, kThreads, Smem<SRC, NT, 0>::kBytes, s>>>(b, tm, units, B, slot, slot + 2, xt);
   count_launches(1);
   return map_cuda(cudaGetLastError());
 }
