@@ -20,7 +20,8 @@
 // and splits its K range into 8 runs of 128-column k-blocks; the warps' 16 x 8
 // (or 16 x 16) partial tiles are summed in shared memory in a fixed order.
 // CTA i starts on unit i and takes further units from a global counter, so
-// tensors of any shape share one launch.
+// tensors of any shape share one launch; a launch with one CTA per unit (up
+// to two units per resident CTA slot) leaves the counter alone.
 //
 // Lane (g = lane / 4, t = lane % 4) of a warp owns rows g and g + 8 of the
 // unit and, in every k-block, the 32 columns 32 t .. 32 t + 31: one whole
@@ -43,11 +44,12 @@
 // flight and finishes, so no launch can hang.
 //
 // Escapes.  An escaped weight decodes to the placeholder (symbol 0, so
-// |w| < 2^-125); after a unit's k-blocks, threads add x * (w_true -
-// w_placeholder) over the unit's escapes (found in O(1) through the row
-// index) and the parts are summed in a fixed order.  For K15 at B >= 3 the
-// corrections read a copy of x transposed to [K][4, 8 or 16], made by a
-// pre-pass, so one thread takes every batch row of an escape at once.
+// |w| < 2^-125); threads add x * (w_true - w_placeholder) over the unit's
+// escapes (found in O(1) through the row index), moved through the k-loop in
+// a three-stage register pipeline and finished at the unit's end, and the
+// parts are summed in a fixed order.  For K15 at B >= 2 the corrections read
+// a copy of x transposed to [K][4, 8 or 16], made by a pre-pass, so one
+// thread takes every batch row of an escape at once.
 // Results never depend on which warp ran which unit: no atomics touch the
 // sums.
 #include <string.h>
