@@ -172,7 +172,7 @@ WCOMP_API int wcomp_decode(const wcomp_container* c, uint16_t* d_out, void* stre
  * 16-byte aligned take a slower element-by-element path with the same result
  * contract.
  * Memory: the work counters live in a device buffer the library allocates
- * with cudaMalloc on first use per device; a K15 container at B >= 2 also
+ * with cudaMalloc on first use per device; a K15 container at B >= 3 also
  * takes a transposed copy of x (K * 4..16 * 2 bytes) from the library's
  * stream-ordered pool for the duration of the call.  wcomp_gemv_noalloc
  * allocates nothing.
