@@ -103,8 +103,8 @@ constexpr int lut_rep() { return SRC == kK15 && NT == 1 && XW <= 4 ? 16 : 0; }
 // the others move single entries.  Measured on a 16384 x 53248 weight: K15,
 // with 3 % escapes, gains from deeper in-loop corrections (B = 1: 2 -> 4 cut
 // 385 to 347 us, and quads with vector loads instead of four single entries
-// 316 to 310 us; B = 2..8 with the transposed x: 1 -> 2 cut 483 to 400 us at
-// B = 4, and quads 375 -> 363 us at B = 2, 422 -> 408 us at B = 8) and from
+// 316 to 310 us; B = 3..8 with the transposed x: 1 -> 2 cut 483 to 400 us at
+// B = 4, and quads 422 -> 408 us at B = 8) and from
 // two stages, whose smaller shared-memory share leaves more L1 to the
 // corrections and to x (three stages: B = 1 305 -> 313 us, B = 16 569 -> 666
 // us); with two batch tiles (NT = 2) deeper corrections spill registers.
