@@ -410,6 +410,39 @@ def time_launches(fn, stream, reps: int = 10) -> float:
     return a.elapsed_time(b) / reps
 
 
+def layer_rows(W, torch, hp, stream, peak) -> dict:
+    """GEMV over the first layer of the batch (its 15 matrices, two norms left
+    out) in one batched call per scheme, against one batched plain GEMV: the
+    serving-shaped use of the same containers the step encodes."""
+    from decode_gemv_sign_gb300 import synth
+
+    idx = [i for i in range(2, 19) if hp.specs[i].N > 1]
+    dev = hp.gemv_w.device
+    n = sum(hp.specs[i].n for i in idx)
+    infos = hp.infos
+    out = {"tensors": len(idx), "weights": n,
+           "shapes": sorted({f"{hp.specs[i].N}x{hp.specs[i].K}" for i in idx})}
+    for B in BATCHES:
+        xs = [synth.gen_x_torch(B, hp.specs[i].K, 7000 + 31 * B + i, dev) for i in idx]
+        ys = [torch.empty((B, hp.specs[i].N), dtype=torch.float32, device=dev) for i in idx]
+        tp = time_launches(lambda: W.gemv_bf16_batched([hp.src[i] for i in idx], xs, ys, stream=stream), stream)
+        row = {"plain_ms": round(tp, 4),
+               "plain_GB/s": round(plain_bytes_total(hp, idx, B) / (tp / 1e3) / 1e9, 1)}
+        for s in (0, 1):
+            cs = [hp.containers[2 * i + s] for i in idx]
+            tf = time_launches(lambda: W.gemv_batched(cs, xs, ys, stream=stream), stream)
+            nbytes = sum(gemv_bytes(infos[2 * i + s], B) for i in idx)
+            row[f"{SCHEME_NAMES[s]}_ms"] = round(tf, 4)
+            row[f"{SCHEME_NAMES[s]}_over_plain"] = round(tf / tp, 4)
+            row[f"{SCHEME_NAMES[s]}_frac_of_peak"] = round(nbytes / (tf / 1e3) / 1e9 / peak, 4)
+        out[f"b{B}"] = row
+    return out
+
+
+def plain_bytes_total(hp, idx, B) -> int:
+    return sum(plain_bytes(hp.specs[i].N, hp.specs[i].K, B) for i in idx)
+
+
 def make_gemv(W, torch, dev):
     """The 16384x53248 GEMV weight, its containers and x per batch size."""
     from decode_gemv_sign_gb300 import synth
@@ -501,6 +534,8 @@ def run_ours(args):
                        for s in (0, 1)} for B in BATCHES}
     # the dense 12-bit ablation: the same GEMV on an escape-free weight (byte-split E = 0)
     ablation = dense12_rows(W, torch, dev, stream, peak)
+    # one layer's matrices in one batched call (serving-shaped GEMVs)
+    layer = layer_rows(W, torch, hp, stream, peak)
 
     # Dominant kernel: decode_kernel, the step's largest share of library GPU
     # time (launch list in profiles/); its launches in the batched decode
@@ -526,6 +561,7 @@ def run_ours(args):
         "kernels": kernels,
         "fused_over_plain_time": ratio,
         "dense12_ablation": ablation,
+        "layer_gemv": layer,
         "decode_exact": exact,
         "device_check": dev_check,
         "escape_rate": {SCHEME_NAMES[s]: round(sum(i["n_escapes"] for i in infos if i["scheme"] == s) /
