@@ -69,6 +69,19 @@ int sm_count(int device) {
   return cache[device];
 }
 
+uint64_t l2_size(int device) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  std::lock_guard<std::mutex> g(mu);
+  if (device < 0 || device >= 64) return 0;
+  if (!cache[device]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, device) != cudaSuccess || v <= 0) v = -1;
+    cache[device] = v;
+  }
+  return cache[device] > 0 ? uint64_t(cache[device]) : 0;
+}
+
 // CRC-32 (IEEE 802.3 polynomial, reflected, initial value and final xor 0xFFFFFFFF).
 static uint32_t crc_table[256];
 static std::once_flag crc_once;

@@ -623,11 +623,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       ++ckb;
       return true;
     };
-    // Ask L2 for a unit's escape positions and values (two bulk prefetches,
-    // issued a unit ahead), so the corrections at its end find them there.
-    auto prefetch_escapes = [&](const Unit& m) {
+    // Ask L2 for a unit's escape positions and values (two bulk prefetches),
+    // so that the corrections find them there: a unit ahead where the whole
+    // grid streams less than the L2 holds in one unit (span: every CTA's rows
+    // times K at 1.5 bytes an element), at the unit's start where it streams
+    // less than twice that (the corrections use a unit's escapes in the first
+    // half of its k-loop), and not at all past that, where the prefetched
+    // lines are evicted before use and read twice (16384 x 53248, K15, B = 1:
+    // 305 -> 297 us without the prefetch; 6144 x 16384, B = 16: 91.6 -> 87.5
+    // us with it).  `late`: the unit is starting and was not prefetched ahead.
+    auto prefetch_escapes = [&](const Unit& m, bool ahead, bool late) {
       if (SRC == kPlain || threadIdx.x != 0) return;
       const TensorDesc& dm = p.d[m.ti];
+      const uint64_t span = uint64_t(gridDim.x) * kRows * uint64_t(dm.K) * 3 / 2;
+      if (ahead ? span > p.l2_bytes : (span > 2 * p.l2_bytes || (late && span <= p.l2_bytes))) return;
       const uint64_t e0 = dm.row_index[m.r0], e1 = dm.row_index[m.r0 + m.rows];
       if (e0 == e1) return;
       // the ranges end inside the padded position and value sections
@@ -638,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       prefetch_l2(reinterpret_cast<const uint8_t*>(dm.esc_pos) + plo, uint32_t(phi - plo));
       prefetch_l2(reinterpret_cast<const uint8_t*>(dm.esc_val) + vlo, uint32_t(vhi - vlo));
     };
-    prefetch_escapes(cur);
-    if (have_next) prefetch_escapes(nxt);
+    prefetch_escapes(cur, false, false);
+    if (have_next) prefetch_escapes(nxt, true, false);
     int par = 0;
     uint32_t grabbed = 0;
     if (threadIdx.x == 0) grabbed = grab();
@@ -1021,8 +1030,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (have_next) {
         unit_of(p, u_next, cur.ti, warp, nxt);
         row_escapes(nxt, ne0, ne1);
-        prefetch_escapes(nxt);
+        prefetch_escapes(nxt, true, false);
       }
+      prefetch_escapes(cur, false, true);
     }
   }
   // A warp that gave up waiting lets its copies in flight land (bounded)
@@ -1271,6 +1281,7 @@ int launch(GemvBatch& b, const TmaBatch& tm, const int64_t* Ns, int B, int dev, 
     count_launches(1);
   }
   const uint32_t grid = gemv_grid(units, uint32_t(per_sm * sms));
+  b.l2_bytes = l2_size(dev);
   gemv_kernel<SRC, NT, XW><<<grid, kThreads, Smem<SRC, NT, XW>::kBytes, s>>>(b, tm, units, B, slot,
                                                                                      base + 2 * kSlots, xt);
   count_launches(1);
@@ -1551,6 +1562,7 @@ int launch_on(GemvBatch& b, const TmaBatch& tm, int64_t N, int B, int dev, int s
   XtBatch xt;
   memset(&xt, 0, sizeof(xt));
   const uint32_t grid = gemv_grid(units, uint32_t(per_sm * sms));
+  b.l2_bytes = l2_size(dev);
   gemv_kernel<SRC, NT, 0><<<grid, kThreads, Smem<SRC, NT, 0>::kBytes, s>>>(b, tm, units, B, slot, slot + 2, xt);
   count_launches(1);
   return map_cuda(cudaGetLastError());

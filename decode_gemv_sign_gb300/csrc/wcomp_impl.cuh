@@ -192,6 +192,7 @@ struct GemvBatch {
   float* y[kMaxBatch];
   uint32_t set_prefix[kMaxBatch + 1];   // first global row set of each tensor
   int count;
+  uint64_t l2_bytes;                    // the device's L2 size (sizes the escape prefetch)
 };
 
 // ---------------------------------------------------------------------------
@@ -409,6 +410,7 @@ uint32_t debug_take_gemv();
 // returning them to the driver at every synchronization).
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t s);
 int sm_count(int device);
+uint64_t l2_size(int device);
 int map_cuda(cudaError_t e);
 void count_launches(uint64_t k);
 
