@@ -577,7 +577,7 @@ struct Job {
 };
 
 // Histogram blocks for a tensor of n elements in a batch whose histogrammed
-// tensors hold total_n elements: about six blocks per SM spread over the
+// tensors hold total_n elements: about 24 blocks per SM spread over the
 // batch in proportion to size, but never fewer than keep every thread at or
 // below kHistMaxChunks 8-element chunks (the 16-bit counter bound in
 // hist_kernel), and never more than one chunk per thread.
