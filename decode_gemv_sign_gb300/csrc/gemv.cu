@@ -264,9 +264,16 @@ struct Unit {
   uint32_t kb0, kb1;   // this warp's k-blocks [kb0, kb1)
   uint32_t kvalid;     // valid columns of the tensor's last k-block (32..128)
   uint32_t nkb;        // k-blocks per row
+  uint32_t rot;        // the warp walks [kb0, kb1) from kb0 + rot, wrapping around
 };
 
-__device__ __forceinline__ void unit_of(const GemvBatch& p, uint32_t u, int start, int warp, Unit& m) {
+// rot_mul: 0 (every warp walks its k-range in order), or the factor that
+// spreads the starting offsets of successive units over ranges of at least 16
+// k-blocks, where the walk was measured to gain (16384 x 53248 and 6144 x
+// 16384, K15 B = 4: 364 -> 331 and 65.1 -> 63.0 us); on six k-blocks a warp
+// (K = 6144) it made no difference either way.
+__device__ __forceinline__ void unit_of(const GemvBatch& p, uint32_t u, int start, int warp, Unit& m,
+                                        uint32_t rot_mul) {
   m.ti = owner(p.set_prefix, p.count, u, start);
   const TensorDesc& d = p.d[m.ti];
   m.r0 = int64_t(u - p.set_prefix[m.ti]) * kRows;
@@ -275,6 +282,14 @@ __device__ __forceinline__ void unit_of(const GemvBatch& p, uint32_t u, int star
   m.kvalid = uint32_t(d.K - int64_t(m.nkb - 1) * kKBlock);
   m.kb0 = uint32_t(uint64_t(m.nkb) * warp / kWarps);
   m.kb1 = uint32_t(uint64_t(m.nkb) * (warp + 1) / kWarps);
+  const uint32_t span = m.kb1 - m.kb0;
+  m.rot = span >= 16 ? uint32_t(uint64_t(u) * rot_mul % span) : 0u;
+}
+
+// The i-th k-block (kb0 <= i < kb1) in the warp's walk of unit m.
+__device__ __forceinline__ uint32_t kb_at(const Unit& m, uint32_t i) {
+  const uint32_t a = i + m.rot;
+  return a >= m.kb1 ? a - (m.kb1 - m.kb0) : a;
 }
 
 // Bring k-block kb of unit m into the stage at `st` (one lane of the warp):
@@ -539,6 +554,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int i = 0; i < kStages; ++i) mbar_init_u32(bars + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // K15 with the transposed x (B = 3..8): the warps of unit u walk their
+  // k-ranges from offset 7u (mod the range), so that the CTAs do not all read
+  // the same lines of x at the same moment (16384 x 53248, B = 4: 364 -> 331
+  // us; B = 8: 397 -> 385 us).  The offset depends on the unit only, so the
+  // order of every sum, and the result, is the same on every call.  Elsewhere
+  // the walk made no gain or lost: the L1 prefetch of x at B <= 8 already hides
+  // those reads (byte-split B = 1 216 -> 223 us with it), and K15 at B = 9..16
+  // lost 6 %.
+  constexpr bool kRot = SRC == kK15 && (XW == 4 || XW == 8);
+  constexpr uint32_t rot_mul = kRot ? 7u : 0u;
   // Every CTA starts on its own unit; the rest come from the counter, so a
   // launch with fewer than two units per CTA never leaves one CTA holding two
   // units while another has none.  A launch with a CTA for every unit leaves
@@ -595,11 +620,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       e0 = d.row_index[m.r0 + cj];
       e1 = d.row_index[m.r0 + cj + 1];
     };
-    unit_of(p, u, 0, warp, cur);
+    unit_of(p, u, 0, warp, cur, rot_mul);
     row_escapes(cur, ce0, ce1);
     bool have_next = u_next < total_units;
     if (have_next) {
-      unit_of(p, u_next, cur.ti, warp, nxt);
+      unit_of(p, u_next, cur.ti, warp, nxt, rot_mul);
       row_escapes(nxt, ne0, ne1);
     }
     // The copy cursor: the next k-block to copy, in `cur` (ahead == 0) or
@@ -617,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (ahead == 1 && ckb >= nxt.kb1) return false;
       if (lane == 0 && !(skip_first_copy && issued == 0)) {
         const uint32_t sidx = issued % kStages;
-        issue_item<SRC>(tm, ahead == 0 ? cur : nxt, ckb, ring + sidx * StageGeom<SRC>::kBytes, bars + 8 * sidx);
+        issue_item<SRC>(tm, ahead == 0 ? cur : nxt, kRot ? kb_at(ahead == 0 ? cur : nxt, ckb) : ckb, ring + sidx * StageGeom<SRC>::kBytes, bars + 8 * sidx);
       }
       ++issued;
       ++ckb;
@@ -847,14 +872,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         while (!aborted && issued < done + kStages && issue_next()) {
         }
         uint4 xv[NT][4];
-        load_x<NT, NT == 1 && XW == 0>(p, cur, kb, B, lane, xv);
+        const uint32_t kr = kRot ? kb_at(cur, kb) : kb;  // the k-block this step computes
+        load_x<NT, NT == 1 && XW == 0>(p, cur, kr, B, lane, xv);
         const uint32_t sidx = done % kStages;
         if (!aborted && __any_sync(0xffffffffu, !mbar_wait_bounded(bars + 8 * sidx, (done / kStages) & 1))) {
           aborted = true;  // the warp stops copying and waiting, and still runs the same instructions
           if (lane == 0) atomicOr(err, 1u);
         }
         const uint32_t st = ring + sidx * StageGeom<SRC>::kBytes;
-        if (kb + 1 < cur.nkb || cur.kvalid == kKBlock)
+        if (kr + 1 < cur.nkb || cur.kvalid == kKBlock)
           compute_item<SRC, NT, true, kRep>(d.t, lut, st, lane, true, xv, acc);
         else
           compute_item<SRC, NT, false, kRep>(d.t, lut, st, lane, uint32_t(32 * (lane & 3)) < cur.kvalid, xv, acc);
@@ -1028,7 +1054,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (threadIdx.x == 0) grabbed = grab();
       have_next = u_next < total_units;
       if (have_next) {
-        unit_of(p, u_next, cur.ti, warp, nxt);
+        unit_of(p, u_next, cur.ti, warp, nxt, rot_mul);
         row_escapes(nxt, ne0, ne1);
         prefetch_escapes(nxt, true, false);
       }

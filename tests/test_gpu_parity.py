@@ -173,6 +173,28 @@ def test_gemv_matches_oracle(W, scheme, B):
     c.free()
 
 
+@pytest.mark.parametrize("B", [3, 4, 6, 8])
+def test_gemv_k15_walk_offsets(W, B):
+    """K15 at B = 3..8 walks each warp's k-blocks from a per-unit offset
+    (wrapping) where a warp has at least 16 of them: with 17 per warp
+    (K = 17408) the first units start at offsets 0, 7, 14, 4, 11; with 41
+    (K = 41984) and 96 rows at 0, 7, .., 35; with 5 (K = 5120) in order.
+    Every sum must still cover each k-block once, and the result must not
+    depend on the call."""
+    for seed, (N, K) in enumerate([(80, 17408), (96, 41984), (80, 5120)]):
+        spec = synth.WeightSpec("r", N, K, "t4", 0.02, 0.005, "normal", 1.0, seed=500 + 10 * B + seed)
+        w = synth.gen_weights_np(spec)
+        x = synth.gen_x_np(B, K, 600 + 10 * B + seed)
+        c = W.encode(dev(w), 1)
+        g = Guarded((B, N), torch.float32)
+        y = W.gemv(c, dev(x), g.out)
+        check_gemv(y, O.gemv(w, x))
+        g.check()
+        assert torch.equal(y, W.gemv(c, dev(x)))
+        W.device_check()
+        c.free()
+
+
 @pytest.mark.parametrize("scheme", O.SCHEMES + (2,))
 @pytest.mark.parametrize("shape", [(37, 96), (64, 160), (9, 2080), (8, 32), (130, 1056)])
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 9, 16])
