@@ -21,7 +21,9 @@
 // (or 16 x 16) partial tiles are summed in shared memory in a fixed order.
 // CTA i starts on unit i and takes further units from a global counter, so
 // tensors of any shape share one launch; a launch with one CTA per unit (up
-// to two units per resident CTA slot) leaves the counter alone.
+// to two units per resident CTA slot) leaves the counter alone.  K15 with the
+// transposed x walks each run from an offset that depends on the unit (runs of
+// 16 k-blocks or more), so the CTAs do not all read the same x lines at once.
 //
 // Lane (g = lane / 4, t = lane % 4) of a warp owns rows g and g + 8 of the
 // unit and, in every k-block, the 32 columns 32 t .. 32 t + 31: one whole
