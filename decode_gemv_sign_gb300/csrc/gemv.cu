@@ -22,8 +22,9 @@
 // CTA i starts on unit i and takes further units from a global counter, so
 // tensors of any shape share one launch; a launch with one CTA per unit (up
 // to two units per resident CTA slot) leaves the counter alone.  K15 with the
-// transposed x walks each run from an offset that depends on the unit (runs of
-// 16 k-blocks or more), so the CTAs do not all read the same x lines at once.
+// transposed x, and the plain GEMV above B = 8, walk each run from an offset
+// that depends on the unit (runs of 16 k-blocks or more), so the CTAs do not
+// all read the same x lines at once.
 //
 // Lane (g = lane / 4, t = lane % 4) of a warp owns rows g and g + 8 of the
 // unit and, in every k-block, the 32 columns 32 t .. 32 t + 31: one whole
@@ -556,15 +557,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int i = 0; i < kStages; ++i) mbar_init_u32(bars + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // K15 with the transposed x (B = 3..8): the warps of unit u walk their
-  // k-ranges from offset 7u (mod the range), so that the CTAs do not all read
-  // the same lines of x at the same moment (16384 x 53248, B = 4: 364 -> 331
-  // us; B = 8: 397 -> 385 us).  The offset depends on the unit only, so the
-  // order of every sum, and the result, is the same on every call.  Elsewhere
-  // the walk made no gain or lost: the L1 prefetch of x at B <= 8 already hides
-  // those reads (byte-split B = 1 216 -> 223 us with it), and K15 at B = 9..16
-  // lost 6 %.
-  constexpr bool kRot = SRC == kK15 && (XW == 4 || XW == 8);
+  // K15 with the transposed x (B = 3..8) and the plain GEMV at B = 9..16: the
+  // warps of unit u walk their k-ranges from offset 7u (mod the range), so
+  // that the CTAs do not all read the same lines of x at the same moment
+  // (16384 x 53248: K15 B = 4 364 -> 331 us, B = 8 397 -> 385 us; plain B = 9
+  // 305 -> 286 us, B = 16 356 -> 347 us).  The offset depends on the unit
+  // only, so the order of every sum, and the result, is the same on every
+  // call.  Elsewhere the walk made no gain or lost: the L1 prefetch of x at
+  // B <= 8 already hides those reads (byte-split B = 1 216 -> 223 us with it),
+  // K15 at B = 9..16 lost 6 %, and byte-split at B = 9..16 gained 1-3 % on
+  // that weight but lost 2 % on a layer's matrices.
+  constexpr bool kRot = (SRC == kK15 && (XW == 4 || XW == 8)) || (SRC == kPlain && NT == 2);
   constexpr uint32_t rot_mul = kRot ? 7u : 0u;
   // Every CTA starts on its own unit; the rest come from the counter, so a
   // launch with fewer than two units per CTA never leaves one CTA holding two

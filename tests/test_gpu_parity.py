@@ -195,6 +195,22 @@ def test_gemv_k15_walk_offsets(W, B):
         c.free()
 
 
+@pytest.mark.parametrize("B", [9, 16])
+def test_plain_gemv_walk_offsets(W, B):
+    """The plain GEMV above B = 8 walks each warp's k-blocks from the same
+    per-unit offsets as K15 at B = 3..8 (17 and 41 k-blocks a warp here)."""
+    for seed, (N, K) in enumerate([(80, 17408), (96, 41984)]):
+        spec = synth.WeightSpec("p", N, K, "t4", 0.02, 0.005, "normal", 1.0, seed=700 + 10 * B + seed)
+        w = synth.gen_weights_np(spec)
+        x = synth.gen_x_np(B, K, 800 + 10 * B + seed)
+        g = Guarded((B, N), torch.float32)
+        y = W.gemv_bf16(dev(w), dev(x), g.out)
+        check_gemv(y, O.gemv(w, x))
+        g.check()
+        assert torch.equal(y, W.gemv_bf16(dev(w), dev(x)))
+        W.device_check()
+
+
 @pytest.mark.parametrize("scheme", O.SCHEMES + (2,))
 @pytest.mark.parametrize("shape", [(37, 96), (64, 160), (9, 2080), (8, 32), (130, 1056)])
 @pytest.mark.parametrize("B", [1, 2, 4, 8, 9, 16])
